@@ -1,0 +1,159 @@
+"""Seeded synthetic inputs for the W4A16 group-quantized matmul.
+
+This module builds the inputs that both the CPU oracle and the CUDA path
+consume: packed 4-bit codes, bf16 group scales, packed 4-bit zero points and
+bf16 activations, all in the canonical layout
+
+    qweight int32 [N, K/8]     nibble j (bits 4j..4j+3) of word c holds k = 8c + j
+    scales  bf16  [N, K/G]     one scale per (output row, K-group)
+    zeros   int32 [N, ceil(K/G/8)]  nibble j of word c holds group 8c + j
+
+It holds no part of the method's arithmetic (no dequantisation, no products,
+no sums): only random-number generation, rounding of the sampled reals to
+bf16 and bit packing of the sampled integers.
+
+Generator: SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom
+number generators", OOPSLA 2014), one stream per tensor; uniform reals from
+the top 53 bits; normals by the Box-Muller transform (cosine branch); codes
+from the top 4 bits.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "splitmix64_stream", "uniform01", "normal01", "f32_to_bf16_bits",
+    "bf16_bits_to_f32", "pack_nibbles_rows", "make_codes", "make_qweight",
+    "make_scales", "make_zeros", "make_x", "make_problem", "TENSOR_IDS",
+]
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# stream id of every tensor a problem draws
+TENSOR_IDS = {"x": 1, "qweight": 2, "scales": 3, "zeros": 4,
+              "qweight_up": 5, "scales_up": 6, "zeros_up": 7}
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def splitmix64_stream(state0: int, n: int, offset: int = 0) -> np.ndarray:
+    """Outputs offset+1 .. offset+n of SplitMix64 started at ``state0``.
+
+    Output i (1-based) is mix(state0 + i * gamma) modulo 2^64.
+    """
+    with np.errstate(over="ignore"):
+        i = np.arange(offset + 1, offset + n + 1, dtype=np.uint64)
+        return _mix(np.uint64(state0 & 0xFFFFFFFFFFFFFFFF) + i * _GAMMA)
+
+
+def _stream_state(seed: int, tensor_id: int) -> int:
+    with np.errstate(over="ignore"):
+        a = _mix(np.array([seed & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64))[0]
+        b = _mix(np.array([(tensor_id + 1) & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64))[0]
+        return int(a ^ b)
+
+
+def uniform01(bits: np.ndarray) -> np.ndarray:
+    """[0, 1) reals in float64 from the top 53 bits of each draw."""
+    return (bits >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normal01(bits_a: np.ndarray, bits_b: np.ndarray) -> np.ndarray:
+    """Standard normals (Box-Muller, cosine branch) in float64."""
+    u1 = ((bits_a >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)  # (0, 1]
+    u2 = (bits_b >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even); uint16 bits."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    bias = np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
+    r = ((u + bias) >> np.uint64(16)).astype(np.uint16)
+    nan = np.isnan(f)
+    if nan.any():
+        r = np.where(nan, np.uint16(0x7FC0), r)
+    return r
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    b = np.ascontiguousarray(np.asarray(b, dtype=np.uint16))
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def pack_nibbles_rows(vals: np.ndarray) -> np.ndarray:
+    """Pack a [R, C] array of 0..15 integers into int32 [R, ceil(C/8)], nibble j of word c = column 8c+j.
+
+    Columns past C in the last word are zero.
+    """
+    vals = np.asarray(vals, dtype=np.uint32)
+    R, C = vals.shape
+    W = (C + 7) // 8
+    padded = np.zeros((R, W * 8), dtype=np.uint32)
+    padded[:, :C] = vals & np.uint32(0xF)
+    padded = padded.reshape(R, W, 8)
+    words = np.zeros((R, W), dtype=np.uint32)
+    for j in range(8):
+        words |= padded[:, :, j] << np.uint32(4 * j)
+    return words.view(np.int32)
+
+
+def make_codes(N: int, K: int, seed: int, tid: int) -> np.ndarray:
+    """Uniform 4-bit codes q[n][k] in 0..15, uint8 [N, K] (top 4 bits of each draw)."""
+    bits = splitmix64_stream(_stream_state(seed, tid), N * K)
+    return (bits >> np.uint64(60)).astype(np.uint8).reshape(N, K)
+
+
+def make_qweight(N: int, K: int, seed: int, tid: int = TENSOR_IDS["qweight"]) -> np.ndarray:
+    assert K % 8 == 0
+    return pack_nibbles_rows(make_codes(N, K, seed, tid))
+
+
+def make_scales(N: int, Kg: int, lo: float, hi: float, seed: int,
+                tid: int = TENSOR_IDS["scales"]) -> np.ndarray:
+    """bf16 bits [N, Kg], uniform in [lo, hi) (float64 -> float32 -> bf16, each to nearest even)."""
+    u = uniform01(splitmix64_stream(_stream_state(seed, tid), N * Kg))
+    return f32_to_bf16_bits((lo + (hi - lo) * u).astype(np.float32)).reshape(N, Kg)
+
+
+def make_zeros(N: int, Kg: int, seed: int, tid: int = TENSOR_IDS["zeros"]) -> np.ndarray:
+    """Packed 4-bit zero points, int32 [N, ceil(Kg/8)], each uniform in 0..15."""
+    bits = splitmix64_stream(_stream_state(seed, tid), N * Kg)
+    z = (bits >> np.uint64(60)).astype(np.uint8).reshape(N, Kg)
+    return pack_nibbles_rows(z)
+
+
+def make_x(M: int, K: int, seed: int, x_scale: float = 1.0,
+           tid: int = TENSOR_IDS["x"]) -> np.ndarray:
+    """bf16 bits [M, K] of N(0, 1) * x_scale (float64 -> float32 -> bf16)."""
+    n = M * K
+    bits = splitmix64_stream(_stream_state(seed, tid), 2 * n)
+    z = normal01(bits[0::2], bits[1::2]) * x_scale
+    return f32_to_bf16_bits(z.astype(np.float32)).reshape(M, K)
+
+
+def make_problem(M: int, N: int, K: int, group: int, sym: bool,
+                 scale_range=(0.005, 0.02), x_scale: float = 1.0, seed: int = 0,
+                 gateup: bool = False) -> dict:
+    """All host arrays of one problem. With ``gateup`` a second weight (the up
+    projection, same shapes) is drawn from its own streams."""
+    assert K % group == 0 and K % 8 == 0
+    Kg = K // group
+    lo, hi = scale_range
+    p = {"M": M, "N": N, "K": K, "group": group, "sym": bool(sym), "seed": seed,
+         "x": make_x(M, K, seed, x_scale),
+         "qweight": make_qweight(N, K, seed),
+         "scales": make_scales(N, Kg, lo, hi, seed),
+         "zeros": None if sym else make_zeros(N, Kg, seed)}
+    if gateup:
+        p["qweight_up"] = make_qweight(N, K, seed, TENSOR_IDS["qweight_up"])
+        p["scales_up"] = make_scales(N, Kg, lo, hi, seed, TENSOR_IDS["scales_up"])
+        p["zeros_up"] = None if sym else make_zeros(N, Kg, seed, TENSOR_IDS["zeros_up"])
+    return p

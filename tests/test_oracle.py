@@ -1,0 +1,265 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+* a hand-worked example (tests/golden/dequant_worked_example.txt);
+* exact rational brute force on tiny inputs (fractions.Fraction: every bf16
+  value and every product is a dyadic rational, so the exact sum is known and
+  the float64 oracle must sit within the float64 summation bound of it);
+* closed forms: all codes equal to the zero point give y = 0; constant codes
+  give (c - z) * sum_g s_g * sum_{k in g} x_k; a one-hot x selects one
+  dequantised weight exactly; power-of-two scaling of the scales scales y
+  exactly;
+* the logistic function's textbook value sigma(1) = e / (1 + e) for SiLU.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "dequant_worked_example.txt")
+
+
+def _load_golden():
+    d = {}
+    with open(GOLDEN) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            k, v = line.split(":", 1)
+            d[k.strip()] = v.split()
+    N, K, G = int(d["N"][0]), int(d["K"][0]), int(d["G"][0])
+    q = np.array([int(h, 16) for h in d["qweight"]], dtype=np.uint32).view(np.int32).reshape(N, K // 8)
+    s = np.array([int(h, 16) for h in d["scales"]], dtype=np.uint16).reshape(N, K // G)
+    z = np.array([int(h, 16) for h in d["zeros"]], dtype=np.uint32).view(np.int32).reshape(N, -1)
+    x = np.array([int(h, 16) for h in d["x"]], dtype=np.uint16).reshape(-1, K)
+    f = lambda key: np.array([float(v) for v in d[key]])
+    return dict(N=N, K=K, G=G, q=q, s=s, z=z, x=x, w_sym=f("w_sym").reshape(N, K),
+                w_asym=f("w_asym").reshape(N, K), y_sym=f("y_sym").reshape(-1, N),
+                y_asym=f("y_asym").reshape(-1, N))
+
+
+def test_golden_codes_nibble_order():
+    g = _load_golden()
+    codes = [[oracle.code(g["q"], g["K"], n, k) for k in range(g["K"])] for n in range(g["N"])]
+    assert codes[0] == list(range(16))
+    assert codes[1] == [7, 6, 5, 4, 3, 2, 1, 0, 15, 14, 13, 12, 11, 10, 9, 8]
+    assert [oracle.zero(g["z"], 2, False, 0, j) for j in range(2)] == [3, 12]
+    assert [oracle.zero(g["z"], 2, False, 1, j) for j in range(2)] == [0, 15]
+    assert oracle.zero(g["z"], 2, True, 1, 1) == 8
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_golden_dequant_and_gemm(sym):
+    g = _load_golden()
+    z = None if sym else g["z"]
+    w = oracle.dequant(g["q"], g["s"], z, g["N"], g["K"], g["G"], sym)
+    np.testing.assert_array_equal(w, g["w_sym"] if sym else g["w_asym"])
+    y, a = oracle.gemm(g["x"], g["q"], g["s"], z, 2, g["N"], g["K"], g["G"], sym)
+    np.testing.assert_array_equal(y, g["y_sym"] if sym else g["y_asym"])
+    # sum |x w| of the first row (x = 1) is the sum of |w| over the row
+    np.testing.assert_array_equal(a[0], np.abs(w).sum(axis=1))
+
+
+# --------------------------------------------------------------------------
+# exact rational brute force
+
+def _fr_bf16(bits):
+    return Fraction(float(synth.bf16_bits_to_f32(np.array([bits], dtype=np.uint16))[0]))
+
+
+def _brute(codes, zeros_mat, scales, x, G):
+    """Exact y[m][n] from the unpacked code / zero matrices (never from packed words)."""
+    M, K = x.shape
+    N = codes.shape[0]
+    xs = [[_fr_bf16(x[m, k]) for k in range(K)] for m in range(M)]
+    y = [[Fraction(0)] * N for _ in range(M)]
+    a = [[Fraction(0)] * N for _ in range(M)]
+    for n in range(N):
+        w = [(int(codes[n, k]) - int(zeros_mat[n, k // G])) * _fr_bf16(scales[n, k // G])
+             for k in range(K)]
+        for m in range(M):
+            y[m][n] = sum((xs[m][k] * w[k] for k in range(K)), Fraction(0))
+            a[m][n] = sum((abs(xs[m][k] * w[k]) for k in range(K)), Fraction(0))
+    return y, a
+
+
+@pytest.mark.parametrize("sym,G,M,N,K", [(True, 8, 3, 5, 32), (False, 8, 2, 4, 64),
+                                         (False, 16, 3, 3, 48), (True, 64, 1, 2, 128)])
+def test_bruteforce_exact(sym, G, M, N, K):
+    seed = 11 + K + N
+    codes = synth.make_codes(N, K, seed, 2)
+    Kg = K // G
+    zmat = (np.full((N, Kg), 8, dtype=np.uint8) if sym
+            else synth.make_codes(N, Kg, seed, 4))
+    q = synth.pack_nibbles_rows(codes)
+    z = None if sym else synth.pack_nibbles_rows(zmat)
+    s = synth.make_scales(N, Kg, 0.005, 0.02, seed)
+    x = synth.make_x(M, K, seed)
+    y, a = oracle.gemm(x, q, s, z, M, N, K, G, sym)
+    ye, ae = _brute(codes, zmat, s, x, G)
+    gamma = 1.01 * K * 2.0 ** -53
+    for m in range(M):
+        for n in range(N):
+            err = abs(Fraction(y[m, n]) - ye[m][n])
+            assert err <= gamma * ae[m][n], (m, n, float(err))
+            assert abs(Fraction(a[m, n]) - ae[m][n]) <= gamma * ae[m][n]
+
+
+def test_bruteforce_detects_transposed_weight():
+    """A weight read transposed (w[k][n] for w[n][k]) must disagree with the exact sum."""
+    N = K = 16
+    codes = synth.make_codes(N, K, 5, 2)
+    s = np.full((N, 2), 0x3F80, dtype=np.uint16)  # 1.0
+    x = synth.make_x(1, K, 5)
+    ye, _ = _brute(codes.T.copy(), np.full((N, 2), 8), s, x, 8)
+    y, _ = oracle.gemm(x, synth.pack_nibbles_rows(codes), s, None, 1, N, K, 8, True)
+    assert any(abs(Fraction(y[0, n]) - ye[0][n]) > 0 for n in range(N))
+
+
+# --------------------------------------------------------------------------
+# closed forms
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_codes_equal_zero_give_zero(sym):
+    M, N, K, G = 3, 24, 256, 64
+    Kg = K // G
+    zmat = np.full((N, Kg), 8, np.uint8) if sym else synth.make_codes(N, Kg, 3, 4)
+    codes = np.repeat(zmat, G, axis=1)
+    q = synth.pack_nibbles_rows(codes)
+    z = None if sym else synth.pack_nibbles_rows(zmat)
+    s = synth.make_scales(N, Kg, 0.005, 0.02, 3)
+    x = synth.make_x(M, K, 3)
+    y, a = oracle.gemm(x, q, s, z, M, N, K, G, sym)
+    assert np.all(y == 0.0) and np.all(a == 0.0)
+
+
+@pytest.mark.parametrize("c,sym", [(0, True), (15, True), (11, False), (3, False)])
+def test_constant_code_closed_form(c, sym):
+    M, N, K, G = 2, 16, 512, 128
+    Kg = K // G
+    codes = np.full((N, K), c, np.uint8)
+    zmat = np.full((N, Kg), 8, np.uint8) if sym else synth.make_codes(N, Kg, 9, 4)
+    q = synth.pack_nibbles_rows(codes)
+    z = None if sym else synth.pack_nibbles_rows(zmat)
+    s = synth.make_scales(N, Kg, 0.005, 0.02, 9)
+    x = synth.make_x(M, K, 9)
+    y, a = oracle.gemm(x, q, s, z, M, N, K, G, sym)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    sf = synth.bf16_bits_to_f32(s).astype(np.float64)
+    xg = xf.reshape(M, Kg, G).sum(axis=2)                    # sum_{k in g} x_k
+    expect = (c - zmat.astype(np.float64))[None] * sf[None] * xg[:, None, :]
+    expect = expect.sum(axis=2)                              # sum over groups
+    tol = 2 * K * 2.0 ** -53 * a
+    assert np.all(np.abs(y - expect) <= tol + 1e-300)
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_one_hot_x_selects_weight(sym):
+    N, K, G = 20, 256, 64
+    Kg = K // G
+    codes = synth.make_codes(N, K, 21, 2)
+    zmat = np.full((N, Kg), 8, np.uint8) if sym else synth.make_codes(N, Kg, 21, 4)
+    q = synth.pack_nibbles_rows(codes)
+    z = None if sym else synth.pack_nibbles_rows(zmat)
+    s = synth.make_scales(N, Kg, 0.005, 0.02, 21)
+    ks = [0, 7, 64, 131, 255]
+    x = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = 0x3F80  # 1.0
+    y, _ = oracle.gemm(x, q, s, z, len(ks), N, K, G, sym)
+    sf = synth.bf16_bits_to_f32(s).astype(np.float64)
+    for i, k in enumerate(ks):
+        expect = (codes[:, k].astype(np.float64) - zmat[:, k // G]) * sf[:, k // G]
+        np.testing.assert_array_equal(y[i], expect)
+
+
+def test_power_of_two_scale_scales_output_exactly():
+    M, N, K, G = 2, 12, 256, 128
+    p = synth.make_problem(M, N, K, G, False, seed=4)
+    y1, _ = oracle.gemm(p["x"], p["qweight"], p["scales"], p["zeros"], M, N, K, G, False)
+    s2 = (p["scales"].astype(np.uint32) + (1 << 7)).astype(np.uint16)  # exponent + 1 -> x2
+    y2, _ = oracle.gemm(p["x"], p["qweight"], s2, p["zeros"], M, N, K, G, False)
+    np.testing.assert_array_equal(y2, 2.0 * y1)
+
+
+def test_threads_do_not_change_results():
+    p = synth.make_problem(3, 40, 512, 64, False, seed=6)
+    args = (p["x"], p["qweight"], p["scales"], p["zeros"], 3, 40, 512, 64, False)
+    y1, a1 = oracle.gemm(*args, nthreads=1)
+    y8, a8 = oracle.gemm(*args, nthreads=0)
+    np.testing.assert_array_equal(y1, y8)
+    np.testing.assert_array_equal(a1, a8)
+
+
+def test_gemm_at_matches_full():
+    p = synth.make_problem(5, 48, 256, 64, False, seed=8)
+    args = (p["x"], p["qweight"], p["scales"], p["zeros"], 5, 48, 256, 64, False)
+    y, a = oracle.gemm(*args)
+    rng = np.random.default_rng(0)
+    mi = rng.integers(0, 5, 50)
+    ni = rng.integers(0, 48, 50)
+    ys, as_ = oracle.gemm_at(*args, mi, ni)
+    np.testing.assert_array_equal(ys, y[mi, ni])
+    np.testing.assert_array_equal(as_, a[mi, ni])
+
+
+def test_bad_arguments_rejected():
+    p = synth.make_problem(1, 16, 128, 64, True, seed=1)
+    with pytest.raises(ValueError):
+        oracle.gemm(p["x"], p["qweight"], p["scales"], None, 1, 16, 128, 48, True)  # K % G
+    with pytest.raises(ValueError):
+        oracle.gemm_at(p["x"], p["qweight"], p["scales"], None, 1, 16, 128, 64, True, [1], [0])
+
+
+# --------------------------------------------------------------------------
+# fused SiLU(gate) * up
+
+def test_silu_textbook_values():
+    assert oracle.silu_mul(1.0, 1.0) == pytest.approx(math.e / (1.0 + math.e), rel=1e-15)
+    assert oracle.silu_mul(1.0, 1.0) == pytest.approx(0.7310585786300049, rel=1e-15)
+    assert oracle.silu_mul(0.0, 5.0) == 0.0
+    assert oracle.silu_mul(40.0, 2.0) == 80.0
+    v = oracle.silu_mul(-800.0, 1.0)
+    assert v == 0.0 and math.copysign(1.0, v) < 0
+    assert oracle.silu_mul(-1.0, 1.0) == pytest.approx(-1.0 / (1.0 + math.e), rel=1e-15)
+
+
+@pytest.mark.parametrize("sym", [True, False])
+def test_gateup_closed_forms(sym):
+    M, N, K, G = 3, 16, 256, 64
+    Kg = K // G
+    p = synth.make_problem(M, N, K, G, sym, seed=13, gateup=True)
+    # zero points kept <= 14 so that the code z + 1 below exists
+    zmat = np.full((N, Kg), 8, np.uint8) if sym else synth.make_codes(N, Kg, 13, 4) % 15
+    z = None if sym else synth.pack_nibbles_rows(zmat)
+    mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    # gate codes equal to the zero point: g = 0 and h = 0
+    qg0 = synth.pack_nibbles_rows(np.repeat(zmat, G, axis=1))
+    h, g, u, _, _ = oracle.gateup_silu_at(p["x"], qg0, p["scales"], z, p["qweight_up"],
+                                          p["scales_up"], z, M, N, K, G, sym, mi, ni)
+    assert np.all(g == 0.0) and np.all(h == 0.0)
+    # up codes z + 1 with unit scales: u = sum_k x_k exactly (bf16 sums of <= 256 terms
+    # stay exact in float64), and h = SiLU(g) * sum_k x_k
+    qu1 = synth.pack_nibbles_rows(np.repeat(zmat + 1, G, axis=1))
+    ones = np.full((N, Kg), 0x3F80, np.uint16)
+    h, g, u, _, _ = oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], z, qu1, ones, z,
+                                          M, N, K, G, sym, mi, ni)
+    xs = [sum(Fraction(float(v)) for v in synth.bf16_bits_to_f32(p["x"][m])) for m in range(M)]
+    np.testing.assert_array_equal(u, np.array([float(xs[m]) for m in mi]))
+    codes_g = synth.make_codes(N, K, 13, 2)
+    ge, _ = _brute(codes_g, zmat, p["scales"], p["x"], G)
+    for i, (m, n) in enumerate(zip(mi, ni)):
+        gv = float(ge[m][n])
+        assert g[i] == pytest.approx(gv, rel=1e-13, abs=1e-300)
+        assert h[i] == pytest.approx(gv / (1.0 + math.exp(-gv)) * float(xs[m]), rel=1e-12)
+
+
+def test_silu_bound_reduces_to_gemm_part_when_exact():
+    # with no accumulation error allowed the bound is the relative part only
+    b = oracle.silu_bound(np.array([2.0]), np.array([1.0]), np.array([3.0]),
+                          np.array([0.0]), np.array([0.0]))
+    assert b[0] == 2.0 * 2.0 ** -7

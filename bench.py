@@ -1,0 +1,350 @@
+"""Throughput of the W4A16 group-quantized matmul on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+
+Default workload: one-row decode through one feed-forward block's weights,
+i.e. one step = the gate+up GEMV (M=1, K=5120, N=34816, group 128, z=8) and the
+down GEMV (M=1, K=17408, N=5120), each on its own seeded synthetic input.
+Metric: effective HBM GB/s = algorithmic bytes of the step (packed codes +
+bf16 scales + zero points + x + y) / device time. Prompt workloads report
+TFLOP/s (2*M*K*N) instead.
+
+L2 is defeated by rotating over enough weight copies that one rotation moves
+more than four times the 129 MB L2 (decode) ; the prompt GEMM is compute-bound
+and runs on one copy.
+
+Prints ONE JSON line (rank 0). Under torchrun with N > 1 every rank runs the
+same workload on its own GPU (replicas: the matmul shards with no exchange);
+value = all ranks' bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth.workloads import WORKLOADS, algorithmic_bytes, gemm_flops  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT = "decode_ffn_m1"  # gate+up GEMV followed by the down GEMV
+
+
+def step_parts(workload: str):
+    """[(name, params)] of the calls one step makes."""
+    if workload == DEFAULT:
+        return [("decode_gateup_m1_k5120_n34816", WORKLOADS["decode_gateup_m1_k5120_n34816"]),
+                ("decode_down_m1_k17408_n5120", WORKLOADS["decode_down_m1_k17408_n5120"])]
+    return [(workload, WORKLOADS[workload])]
+
+
+def part_units(w):
+    """(units per call, metric unit, is_flops)"""
+    if w["kind"] == "gateup":
+        return gemm_flops(w["M"], 2 * w["N"], w["K"]), "TFLOP/s", True
+    return algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"]), "GB/s", False
+
+
+def metric_name(workload):
+    parts = step_parts(workload)
+    if part_units(parts[0][1])[2]:
+        return "W4A16 fused gate/up GEMM TFLOP/s (M=4096, K=5120, 2x17408)"
+    return "W4A16 GEMM eff. HBM GB/s (M=1..16)"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 - 0.3 <= t <= t1 + 0.3] or [r for _, r in self.rows[-5:]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CUDA arm
+# ---------------------------------------------------------------------------
+def run_cuda(args, rank, world):
+    import torch
+    import gemm_w4a16_group_gb300 as w4
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    w4.lib()
+    peaks = load_peaks()
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    parts = []
+    for name, w in step_parts(args.workload):
+        p = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
+                               x_scale=w["x_scale"], seed=0, gateup=w["kind"] == "gateup")
+        units, unit, is_flops = part_units(w)
+        wbytes = algorithmic_bytes(1, w["N"], w["K"], w["group"], w["sym"]) * (2 if w["kind"] == "gateup" else 1)
+        parts.append(dict(name=name, w=w, p=p, units=units, unit=unit, is_flops=is_flops, wbytes=wbytes))
+    # weight copies to rotate through so that L2 never holds the next call's weights
+    total_w = sum(pt["wbytes"] for pt in parts)
+    copies = 1 if parts[0]["is_flops"] else max(2, math.ceil(4 * L2_BYTES / total_w) + 1)
+    for pt in parts:
+        p, w = pt["p"], pt["w"]
+        zd = None if p["zeros"] is None else up(p["zeros"])
+        if w["kind"] == "gateup":
+            packed = w4.repack_gateup(up(p["qweight"]), up(p["scales"]), zd, up(p["qweight_up"]),
+                                      up(p["scales_up"]), None if p["zeros_up"] is None else up(p["zeros_up"]),
+                                      w["N"], w["K"], w["group"], w["sym"])
+        else:
+            packed = w4.repack(up(p["qweight"]), up(p["scales"]), zd, w["N"], w["K"], w["group"], w["sym"])
+        pt["packed"] = [packed] + [packed.clone() for _ in range(copies - 1)]
+        pt["x"] = up(p["x"])
+        pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+        pt["x_host"] = torch.from_numpy(p["x"].view(np.int16)).pin_memory()
+        pt["y_host"] = torch.empty((w["M"], w["N"]), dtype=torch.int16).pin_memory()
+        del pt["p"]
+    torch.cuda.synchronize()
+
+    def call(pt, c, x=None, y=None):
+        w = pt["w"]
+        fn = w4.gateup_silu if w["kind"] == "gateup" else w4.gemm
+        fn(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"],
+           out=pt["y"] if y is None else y, stream=stream)
+
+    nsteps, nwarm = args.steps, args.warmup
+    # events around every call: per-launch durations of the dominant call
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in parts] for _ in range(nsteps)]
+    for i in range(nwarm):
+        for pt in parts:
+            call(pt, i % copies)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    t_begin = time.time()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(nsteps):
+        for j, pt in enumerate(parts):
+            ev[i][j][0].record(stream)
+            call(pt, (nwarm + i) % copies)
+            ev[i][j][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if w4.kernel_status() != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during the timed region")
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    per_call_ms = [float(np.mean([ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(nsteps)]))
+                   for j in range(len(parts))]
+
+    # end to end: pinned host x -> device, the calls, device y -> pinned host, every step
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    xd = [torch.empty_like(pt["x"]) for pt in parts]
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for i in range(nsteps):
+        for j, pt in enumerate(parts):
+            xd[j].copy_(pt["x_host"].view(pt["x"].dtype), non_blocking=True)
+            call(pt, (nwarm + nsteps + i) % copies, x=xd[j])
+            pt["y_host"].copy_(pt["y"].view(torch.int16), non_blocking=True)
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    e2e_ms = e_start.elapsed_time(e_stop)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        return None
+
+    units_step = sum(pt["units"] for pt in parts)
+    is_flops = parts[0]["is_flops"]
+    scale = 1e-12 if is_flops else 1e-9
+    value = world * units_step * nsteps / (ms * 1e-3) * scale
+    e2e = world * units_step * nsteps / (e2e_ms * 1e-3) * scale
+    dom = max(range(len(parts)), key=lambda j: parts[j]["units"])
+    d = parts[dom]
+    achieved = d["units"] / (per_call_ms[dom] * 1e-3) * scale
+    peak = peaks["bf16_tflops"] if is_flops else peaks["hbm_gbs"]
+    clocks = sampler.summary(t_begin, t_end)
+    h2d = sum(pt["x"].numel() * 2 for pt in parts)
+    d2h = sum(pt["y"].numel() * 2 for pt in parts)
+    line = {
+        "metric": metric_name(args.workload), "value": round(value, 2), "unit": parts[0]["unit"],
+        "n_gpus": world, "steps": nsteps, "warmup": nwarm, "ms_per_step": ms / nsteps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload table)",
+        "config": {"workload": args.workload, "calls_per_step": [pt["name"] for pt in parts],
+                   "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
+                          if copies > 1 else "compute-bound; one weight copy"),
+                   "parallelism": f"replicas x{world}", "per_call_ms": [round(v, 5) for v in per_call_ms]},
+        "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
+                     "achieved": round(achieved, 2), "peak": peak, "unit": d["unit"],
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_src": peaks["src"] + (" bf16 burst" if is_flops else " copy")},
+        "e2e": {"value": round(e2e, 2), "unit": parts[0]["unit"], "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": nsteps * len(parts),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def cpu_baseline(workload, budget_s=10.0, steps=None):
+    """The float64 oracle as it stands, on every host core, over a bounded
+    sample of the workload; returns value in the workload's unit."""
+    import oracle
+    parts = step_parts(workload)
+    probs = []
+    for name, w in parts:
+        p = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
+                               x_scale=w["x_scale"], seed=0, gateup=w["kind"] == "gateup")
+        probs.append((name, w, p))
+    is_flops = part_units(parts[0][1])[2]
+    units_done, t_total, reps, desc = 0.0, 0.0, 0, ""
+    while True:
+        for name, w, p in probs:
+            if w["kind"] == "gateup":
+                rows = 16  # sample of M rows x every output column
+                mi = np.repeat(np.arange(rows), w["N"])
+                ni = np.tile(np.arange(w["N"]), rows)
+                t0 = time.perf_counter()
+                oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["qweight_up"],
+                                      p["scales_up"], p["zeros_up"], w["M"], w["N"], w["K"], w["group"],
+                                      w["sym"], mi, ni)
+                t_total += time.perf_counter() - t0
+                units_done += gemm_flops(rows, 2 * w["N"], w["K"])
+                desc = f"{rows} of {w['M']} rows x all {2 * w['N']} gate/up columns"
+            else:
+                t0 = time.perf_counter()
+                oracle.gemm(p["x"], p["qweight"], p["scales"], p["zeros"], w["M"], w["N"], w["K"], w["group"],
+                            w["sym"])
+                t_total += time.perf_counter() - t0
+                units_done += algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"])
+                desc = "whole step"
+        reps += 1
+        if (steps is not None and reps >= steps) or (steps is None and t_total >= budget_s):
+            break
+    scale = 1e-12 if is_flops else 1e-9
+    return {"value": units_done / t_total * scale, "unit": "TFLOP/s" if is_flops else "GB/s",
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{desc}, {reps} repetition(s), {t_total:.1f} s", "seconds": t_total, "reps": reps}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        cpu_baseline(args.workload, steps=1)
+    cb = cpu_baseline(args.workload, steps=max(1, args.steps if args.steps <= 20 else 20))
+    return {"impl": "reference", "metric": metric_name(args.workload), "value": round(cb["value"], 4),
+            "unit": cb["unit"], "n_gpus": 1, "steps": cb["reps"], "warmup": args.warmup,
+            "ms_per_step": cb["seconds"] * 1e3 / cb["reps"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": round(cb["value"], 4), "unit": cb["unit"], "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=[DEFAULT] + list(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl")
+        line = run_cuda(args, rank, world)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

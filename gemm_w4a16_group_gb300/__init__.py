@@ -1,0 +1,211 @@
+"""GB300 (sm_103a) W4A16 group-quantized matmul: thin Python binding.
+
+Every call marshals torch tensors into the C ABI of ``include/w4a16.h`` and
+runs on the current CUDA stream; all arithmetic happens in the CUDA library
+(``_build/libw4a16_gb300.so``, built in-tree by ``build.py``). There is no
+CPU or PyTorch fallback: if the library cannot be loaded every call raises.
+
+    packed = repack(qweight, scales, zeros, N, K, group, sym)     # once per weight
+    y = gemm(x, packed, N, K, group, sym)                          # y = x . dequant(W)^T
+    pg = repack_gateup(qg, sg, zg, qu, su, zu, N, K, group, sym)
+    h = gateup_silu(x, pg, N, K, group, sym)                       # SiLU(x Wg^T) * (x Wu^T)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "EXPORTS", "W4A16Error", "lib", "library_path", "repacked_bytes", "gateup_repacked_bytes",
+    "repack", "repack_gateup", "gemm", "gateup_silu", "dequantize", "kernel_status",
+    "set_kernel_override", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
+]
+
+# symbols declared in include/w4a16.h
+EXPORTS = (
+    "w4a16_repacked_bytes", "w4a16_repack", "w4a16_gateup_repacked_bytes", "w4a16_repack_gateup",
+    "w4a16_gemm", "w4a16_gateup_silu", "w4a16_dequantize", "w4a16_kernel_status",
+    "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
+)
+KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC = 0, 1, 2, 3
+
+
+class W4A16Error(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(auto_build: bool = True) -> ctypes.CDLL:
+    """The loaded CUDA library (compiled first if missing or stale and nvcc is present)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if auto_build and not _build.up_to_date():
+        try:
+            _build.build()
+        except Exception as e:  # fall through to the load error below
+            if not os.path.exists(_build.LIB):
+                raise W4A16Error(f"CUDA library missing and build failed: {e}") from e
+    if not os.path.exists(_build.LIB):
+        raise W4A16Error(f"CUDA library not built: {_build.LIB}")
+    L = ctypes.CDLL(_build.LIB)
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.w4a16_repacked_bytes.argtypes = [i32, i32, i32, i32]
+    L.w4a16_repacked_bytes.restype = sz
+    L.w4a16_gateup_repacked_bytes.argtypes = [i32, i32, i32, i32]
+    L.w4a16_gateup_repacked_bytes.restype = sz
+    L.w4a16_repack.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
+    L.w4a16_repack.restype = i32
+    L.w4a16_repack_gateup.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P, P]
+    L.w4a16_repack_gateup.restype = i32
+    L.w4a16_gemm.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P]
+    L.w4a16_gemm.restype = i32
+    L.w4a16_gateup_silu.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
+    L.w4a16_gateup_silu.restype = i32
+    L.w4a16_dequantize.argtypes = [P, i32, i32, i32, i32, P, P]
+    L.w4a16_dequantize.restype = i32
+    L.w4a16_kernel_status.argtypes = []
+    L.w4a16_kernel_status.restype = i32
+    L.w4a16_strerror.argtypes = [i32]
+    L.w4a16_strerror.restype = ctypes.c_char_p
+    L.w4a16_last_cuda_error.argtypes = []
+    L.w4a16_last_cuda_error.restype = i32
+    L.w4a16_set_kernel_override.argtypes = [i32]
+    L.w4a16_set_kernel_override.restype = i32
+    _lib = L
+    return L
+
+
+def strerror(rc: int) -> str:
+    return lib().w4a16_strerror(rc).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = f"{what}: {strerror(rc)} (status {rc}"
+        if rc == -4:
+            msg += f", cudaError {lib().w4a16_last_cuda_error()}"
+        raise W4A16Error(msg + ")")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtypes, name):
+    if t is None:
+        return None
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16_types():
+    torch = _torch()
+    return (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def repacked_bytes(N: int, K: int, group: int, sym: bool) -> int:
+    return int(lib().w4a16_repacked_bytes(N, K, group, int(sym)))
+
+
+def gateup_repacked_bytes(N_each: int, K: int, group: int, sym: bool) -> int:
+    return int(lib().w4a16_gateup_repacked_bytes(N_each, K, group, int(sym)))
+
+
+def repack(qweight, scales, zeros, N, K, group, sym, stream=None, out=None):
+    """Canonical (qweight int32 [N, K/8], scales bf16 [N, K/G], zeros int32) -> packed uint8 tensor."""
+    torch = _torch()
+    nbytes = repacked_bytes(N, K, group, sym)
+    if nbytes == 0:
+        raise W4A16Error("repack: unsupported sizes")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    rc = lib().w4a16_repack(_ptr(qweight, (torch.int32,), "qweight"), _ptr(scales, _bf16_types(), "scales"),
+                            _ptr(zeros, (torch.int32,), "zeros"), N, K, group, int(sym),
+                            ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    _check(rc, "w4a16_repack")
+    return out
+
+
+def repack_gateup(qw_gate, sc_gate, z_gate, qw_up, sc_up, z_up, N_each, K, group, sym, stream=None):
+    torch = _torch()
+    nbytes = gateup_repacked_bytes(N_each, K, group, sym)
+    if nbytes == 0:
+        raise W4A16Error("repack_gateup: unsupported sizes")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=qw_gate.device)
+    i32, b16 = (torch.int32,), _bf16_types()
+    rc = lib().w4a16_repack_gateup(_ptr(qw_gate, i32, "qw_gate"), _ptr(sc_gate, b16, "sc_gate"),
+                                   _ptr(z_gate, i32, "z_gate"), _ptr(qw_up, i32, "qw_up"),
+                                   _ptr(sc_up, b16, "sc_up"), _ptr(z_up, i32, "z_up"), N_each, K, group,
+                                   int(sym), ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    _check(rc, "w4a16_repack_gateup")
+    return out
+
+
+def gemm(x, packed, N, K, group, sym, out=None, stream=None):
+    """y[M, N] (bf16) = x[M, K] (bf16) . dequant(W)^T."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    rc = lib().w4a16_gemm(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), None, None,
+                          M, N, K, group, int(sym), _ptr(out, _bf16_types(), "out"), _stream(stream))
+    _check(rc, "w4a16_gemm")
+    return out
+
+
+def gateup_silu(x, packed_gateup, N_each, K, group, sym, out=None, stream=None):
+    """h[M, N_each] (bf16) = SiLU(x Wg^T) * (x Wu^T)."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    if out is None:
+        out = torch.empty((M, N_each), dtype=torch.bfloat16, device=x.device)
+    rc = lib().w4a16_gateup_silu(_ptr(x, _bf16_types(), "x"), _ptr(packed_gateup, (torch.uint8,), "packed"),
+                                 M, N_each, K, group, int(sym), _ptr(out, _bf16_types(), "out"),
+                                 _stream(stream))
+    _check(rc, "w4a16_gateup_silu")
+    return out
+
+
+def dequantize(packed, N, K, group, sym, stream=None):
+    """float32 [N, K] = (q - z) * scale, read back through the kernels' unpack."""
+    torch = _torch()
+    out = torch.empty((N, K), dtype=torch.float32, device=packed.device)
+    rc = lib().w4a16_dequantize(_ptr(packed, (torch.uint8,), "packed"), N, K, group, int(sym),
+                                ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    _check(rc, "w4a16_dequantize")
+    return out
+
+
+def kernel_status() -> int:
+    """Synchronise and return (and clear) the kernels' timeout flag: 0 or -5."""
+    return int(lib().w4a16_kernel_status())
+
+
+def set_kernel_override(which: int) -> int:
+    return int(lib().w4a16_set_kernel_override(which))

@@ -1,0 +1,210 @@
+// C ABI (include/w4a16.h): argument checks, device checks and kernel choice.
+// Nothing is launched when a check fails; every check that needs no GPU runs
+// before the first CUDA call.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "w4a16.h"
+#include "w4a16_internal.h"
+
+using namespace w4a16;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_override{0};
+
+// Device error word set by kernels whose bounded waits gave up.
+__device__ int g_kernel_error;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int status = W4A16_OK;
+  int sm_count = 0;
+  int *err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return W4A16_ERR_CUDA;
+}
+
+// Current device's properties and error-word address (looked up once per device).
+int current_device(DeviceInfo &out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+      d.status = W4A16_ERR_UNSUPPORTED;  // the kernels are built for sm_103a only
+    } else {
+      void *p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_kernel_error)) != cudaSuccess) return cuda_fail(e);
+      d.err = static_cast<int *>(p);
+      d.sm_count = sms;
+      d.status = W4A16_OK;
+    }
+    d.ready = true;
+  }
+  out = d;
+  return d.status;
+}
+
+bool sizes_ok(long long M, long long N, long long K, int group) {
+  const long long lim = (1LL << 31) / 16;
+  if (group != 64 && group != 128) return false;
+  if (M < 1 || N < 1 || K < 64 || M >= lim || N >= lim || K >= lim) return false;
+  return K % group == 0;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int finish_launch(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : cuda_fail(e); }
+
+}  // namespace
+
+extern "C" {
+
+size_t w4a16_repacked_bytes(int N, int K, int group, int sym) {
+  if (!sizes_ok(1, N, K, group)) return 0;
+  return make_layout(N, K, group, sym ? 1 : 0).total;
+}
+
+size_t w4a16_gateup_repacked_bytes(int N_each, int K, int group, int sym) {
+  if (!sizes_ok(1, N_each, K, group)) return 0;
+  const long long rows = 2LL * ((N_each + 127) / 128 * 128);
+  if (rows >= (1LL << 31) / 16) return 0;
+  return make_layout((int)rows, K, group, sym ? 1 : 0).total;
+}
+
+int w4a16_repack(const int32_t *qweight, const uint16_t *scales, const int32_t *zeros, int N, int K,
+                 int group, int sym, void *packed, w4a16_stream_t stream) {
+  if (!qweight || !scales || !packed || (!sym && !zeros)) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(1, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(qweight, 4) || !aligned(scales, 2) || (zeros && !aligned(zeros, 4)))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const Layout L = make_layout(N, K, group, sym ? 1 : 0);
+  return finish_launch(launch_repack(qweight, scales, sym ? nullptr : zeros, nullptr, nullptr, nullptr, N,
+                                     false, L, static_cast<uint8_t *>(packed),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const int32_t *z_gate,
+                        const int32_t *qw_up, const uint16_t *sc_up, const int32_t *z_up, int N_each, int K,
+                        int group, int sym, void *packed, w4a16_stream_t stream) {
+  if (!qw_gate || !sc_gate || !qw_up || !sc_up || !packed) return W4A16_ERR_INVALID_ARG;
+  if (!sym && (!z_gate || !z_up)) return W4A16_ERR_INVALID_ARG;
+  if (w4a16_gateup_repacked_bytes(N_each, K, group, sym) == 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(qw_gate, 4) || !aligned(qw_up, 4) || !aligned(sc_gate, 2) ||
+      !aligned(sc_up, 2) || (z_gate && !aligned(z_gate, 4)) || (z_up && !aligned(z_up, 4)))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const int rows = 2 * ((N_each + 127) / 128 * 128);
+  const Layout L = make_layout(rows, K, group, sym ? 1 : 0);
+  return finish_launch(launch_repack(qw_gate, sc_gate, sym ? nullptr : z_gate, qw_up, sc_up,
+                                     sym ? nullptr : z_up, N_each, true, L, static_cast<uint8_t *>(packed),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, const int32_t *zeros, int M,
+               int N, int K, int group, int sym, uint16_t *y, w4a16_stream_t stream) {
+  if (!x || !packed || !y) return W4A16_ERR_INVALID_ARG;
+  if (scales || zeros) return W4A16_ERR_INVALID_ARG;  // reserved: they travel inside `packed`
+  if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false,
+             reinterpret_cast<cudaStream_t>(stream), d.err};
+  const int ov = g_override.load();
+  if (M == 1 && ov == 1) return finish_launch(launch_gemv_m1(c, d.sm_count));
+  if (M <= 16 && ov != 3) {
+    if (M == 1 && ov == 0) return finish_launch(launch_gemv_m1(c, d.sm_count));
+    return finish_launch(launch_smallm_mma(c, d.sm_count));
+  }
+  return finish_launch(launch_prompt_tc(c, d.sm_count));
+}
+
+int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N_each, int K, int group,
+                      int sym, uint16_t *h, w4a16_stream_t stream) {
+  if (!x || !packed_gateup || !h) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N_each, K, group) || w4a16_gateup_repacked_bytes(N_each, K, group, sym) == 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(h, 16) || !aligned(packed_gateup, 256)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym ? 1 : 0, true,
+             reinterpret_cast<cudaStream_t>(stream), d.err};
+  if (M <= 16 && g_override.load() != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
+  return finish_launch(launch_prompt_tc(c, d.sm_count));
+}
+
+int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float *w_out,
+                     w4a16_stream_t stream) {
+  if (!packed || !w_out) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(1, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(w_out, 16)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const Layout L = make_layout(N, K, group, sym ? 1 : 0);
+  return finish_launch(launch_dequantize(static_cast<const uint8_t *>(packed), L, N, w_out,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_kernel_status(void) {
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_kernel_error, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+  if (v != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_kernel_error, &zero, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    return W4A16_ERR_TIMEOUT;
+  }
+  return W4A16_OK;
+}
+
+const char *w4a16_strerror(int status) {
+  switch (status) {
+    case W4A16_OK: return "ok";
+    case W4A16_ERR_INVALID_ARG: return "invalid argument (size, group, null pointer or reserved argument)";
+    case W4A16_ERR_MISALIGNED: return "misaligned pointer (x, y, h need 16 bytes; packed needs 256)";
+    case W4A16_ERR_UNSUPPORTED: return "unsupported device (built for sm_103a)";
+    case W4A16_ERR_CUDA: return "CUDA error (see w4a16_last_cuda_error)";
+    case W4A16_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    default: return "unknown status";
+  }
+}
+
+int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
+
+int w4a16_set_kernel_override(int which) {
+  if (which < 0 || which > 3) return -1;
+  return g_override.exchange(which);
+}
+
+}  // extern "C"

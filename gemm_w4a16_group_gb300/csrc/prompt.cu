@@ -1,0 +1,503 @@
+// Prompt-regime GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   y[m][n] = sum_g scale[n][g] * sum_{k in g} x[m][k] * (q[n][k] - z[n][g])
+//
+// The integer (q - z) is exact in bf16 and each product with a bf16 x is exact
+// in float32, so the tensor core sums one group's products into a TMEM tile
+// (fp32), and CUDA cores fold it into a register accumulator with the group's
+// scale in float32. Rounding a dequantised (q - z) * scale to bf16 before the
+// MMA, as the TensorFold PR #859 prompt GEMM does ("each weight rounded once to
+// bf16"), would cost up to 2^-9 per weight; this split keeps every weight
+// exact. The feed-forward gate is fused as in the GRIMOIRE v1.8 release notes
+// ("INT4 prompt processing"): the CTA's 256 columns are 128 gate rows and the
+// 128 matching up rows, so h = SiLU(g) * u is formed from the two float32
+// accumulators before a single bf16 rounding.
+//
+// One persistent CTA per SM, 512 threads, warp-specialised:
+//   warp 0       TMA producer: x tile [128 x 64] (128-byte swizzle), packed codes of
+//                256 rows x 64 k, and per four groups the scale (+ zero) block
+//   warp 1       TMEM allocator and the single MMA-issuing thread:
+//                D[b] (+)= A . B^T, M = 128, N = 256, K = 16, b = group parity
+//   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
+//                128-byte-swizzled K-major B tile; scale block -> float32
+//   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b];
+//                per tile, the bf16 store (or SiLU(gate) * up)
+// Every wait is bounded; a wait that gives up sets the device error word and
+// every role leaves its loop, drains what it started and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "w4a16_internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int SL = 4;  // x + codes ring
+constexpr int SB = 3;  // dequantised B ring
+constexpr int SS = 2;  // scale-block ring (4 groups each)
+constexpr int kThreads = 512;
+
+constexpr int A_BYTES = BM * BK * 2;   // 16384
+constexpr int B_BYTES = BN * BK * 2;   // 32768
+constexpr int Q_BYTES = BN * BK / 2;   // 8192
+constexpr int RS_BYTES = 16 * kScaleBlockBytes;  // 2048
+constexpr int RZ_BYTES = 16 * kZeroBlockBytes;   // 512
+constexpr int SC_FLOATS = 4 * BN;                // float32 scales of one block
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + SL * A_BYTES;
+constexpr int OFF_Q = OFF_B + SB * B_BYTES;
+constexpr int OFF_RS = OFF_Q + SL * Q_BYTES;
+constexpr int OFF_RZ = OFF_RS + SS * RS_BYTES;
+constexpr int OFF_SC = OFF_RZ + SS * RZ_BYTES;
+constexpr int OFF_BAR = OFF_SC + SS * SC_FLOATS * 4;
+// barriers: full_L, empty_L [SL]; full_B, empty_B [SB]; full_S, conv_S, empty_S [SS];
+// tfull, tempty [2]; mma_done [1]
+constexpr int NBARS = 2 * SL + 2 * SB + 3 * SS + 2 * 2 + 1;
+constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+constexpr int SMEM_USED = OFF_MISC + 16;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+
+static_assert(OFF_B % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+
+struct PromptParams {
+  uint16_t *y;
+  int M, N, K;     // N: output columns (N_each for gate/up)
+  int ld;          // y row stride (elements)
+  int mtiles, ntiles;
+  int nk;          // K / 64
+  int ng;          // K / group
+  int spg;         // 64-wide stages per group (1 or 2)
+  int *err;
+};
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t full_L(int i) const { return base + 8 * i; }
+  __device__ uint32_t empty_L(int i) const { return base + 8 * (SL + i); }
+  __device__ uint32_t full_B(int i) const { return base + 8 * (2 * SL + i); }
+  __device__ uint32_t empty_B(int i) const { return base + 8 * (2 * SL + SB + i); }
+  __device__ uint32_t full_S(int i) const { return base + 8 * (2 * SL + 2 * SB + i); }
+  __device__ uint32_t conv_S(int i) const { return base + 8 * (2 * SL + 2 * SB + SS + i); }
+  __device__ uint32_t empty_S(int i) const { return base + 8 * (2 * SL + 2 * SB + 2 * SS + i); }
+  __device__ uint32_t tfull(int i) const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + i); }
+  __device__ uint32_t tempty(int i) const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + 2 + i); }
+  __device__ uint32_t mma_done() const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + 4); }
+};
+
+__device__ __forceinline__ void give_up(volatile int *abort_flag, int *err) {
+  *abort_flag = 1;
+  atomicExch(err, kErrTimeout);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <bool SYM, bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1)
+    prompt_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
+                     PromptParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  Bars bars{sbase + OFF_BAR};
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntot = p.mtiles * p.ntiles;
+
+  if (tid == 0) {
+    for (int i = 0; i < SL; ++i) {
+      mbar_init(bars.full_L(i), 1);
+      mbar_init(bars.empty_L(i), 128 + 1);  // 128 dequant threads + one MMA commit
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(bars.full_B(i), 128);
+      mbar_init(bars.empty_B(i), 1);
+    }
+    for (int i = 0; i < SS; ++i) {
+      mbar_init(bars.full_S(i), 1);
+      mbar_init(bars.conv_S(i), 128);
+      mbar_init(bars.empty_S(i), 256);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.tfull(i), 1);
+      mbar_init(bars.tempty(i), 256);
+    }
+    mbar_init(bars.mma_done(), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Register split (launched with 128 per thread = 65536): warpgroup 0 gives
+  // back to 40, warpgroup 1 to 96, warpgroups 2-3 take 184:
+  // 128*40 + 128*96 + 256*184 = 64512 <= 65536.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+    if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_s);
+      if (!SYM) tma_prefetch_desc(&tm_z);
+      uint32_t ls = 0, sc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+        const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+        for (int kb = 0; kb < p.nk; ++kb) {
+          if (kb % (4 * p.spg) == 0) {
+            const int slot = sc % SS;
+            if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : RZ_BYTES));
+            const int blk = kb / (4 * p.spg);
+            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, nt * 16, bars.full_S(slot));
+            if (!SYM)
+              tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, nt * 16, bars.full_S(slot));
+            ++sc;
+          }
+          const int slot = ls % SL;
+          if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(bars.full_L(slot), A_BYTES + Q_BYTES);
+          tma_load_2d(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM, bars.full_L(slot));
+          tma_load_2d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, nt * 16, bars.full_L(slot));
+          ++ls;
+        }
+      }
+      if (!ok) {
+        give_up(abort_flag, p.err);
+        // let every copy already issued land before the CTA can exit
+        for (uint32_t i = 0; i < SL && i < ls; ++i) {
+          const uint32_t u = ls - 1 - i;
+          mbar_wait_drain(bars.full_L(u % SL), (u / SL) & 1);
+        }
+        for (uint32_t i = 0; i < SS && i < sc; ++i) {
+          const uint32_t u = sc - 1 - i;
+          mbar_wait_drain(bars.full_S(u % SS), (u / SS) & 1);
+        }
+      }
+    }
+    } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t ls = 0, bs = 0, gc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+        for (int gi = 0; ok && gi < p.ng; ++gi) {
+          const int b = gc & 1;
+          if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+          for (int ks = 0; ks < p.spg; ++ks) {
+            const int sl = ls % SL, sb = bs % SB;
+            if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(bars.full_B(sb), (bs / SB) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t adesc = sw128_desc(sbase + OFF_A + sl * A_BYTES);
+            const uint64_t bdesc = sw128_desc(sbase + OFF_B + sb * B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
+              tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
+            }
+            tc_commit(bars.empty_L(sl));
+            tc_commit(bars.empty_B(sb));
+            ++ls;
+            ++bs;
+          }
+          if (!ok) break;
+          tc_commit(bars.tfull(b));
+          ++gc;
+        }
+      }
+      if (!ok) give_up(abort_flag, p.err);
+      // every MMA issued by this thread completes before TMEM can be freed
+      tc_commit(bars.mma_done());
+      mbar_wait_drain(bars.mma_done(), 0);
+    }
+    }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
+    // ------------------------------------------------------------------ dequantisers
+    const int dw = warp - 4, dt = tid - 128;
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t ls = 0, bs = 0, sc = 0;
+    int cur = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+      for (int kb = 0; kb < p.nk; ++kb) {
+        const int gi = kb / p.spg;
+        if (kb % (4 * p.spg) == 0) {
+          cur = sc % SS;
+          if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
+          // scale block -> float32 columns: thread dt owns tile dt>>3, g = dt&7
+          const int ti = dt >> 3, tg = dt & 7;
+          const uint4 raw = *reinterpret_cast<const uint4 *>(smem + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
+          float *scf = reinterpret_cast<float *>(smem + OFF_SC) + cur * SC_FLOATS;
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            scf[j * BN + 16 * ti + tg] = bf16lo_to_f32(rw[j]);
+            scf[j * BN + 16 * ti + tg + 8] = bf16hi_to_f32(rw[j]);
+          }
+          mbar_arrive(bars.conv_S(cur));
+          ++sc;
+        }
+        const int sl = ls % SL, sb = bs % SB;
+        if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bars.empty_B(sb), ((bs / SB) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        const uint8_t *qs = smem + OFF_Q + sl * Q_BYTES;
+        uint8_t *bt = smem + OFF_B + sb * B_BYTES;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int i = dw + 4 * r;  // 16-row tile within the CTA's 256 rows
+          uint32_t zg, zg8;
+          if (SYM) {
+            zg = zg8 = zero_pair(8);
+          } else {
+            const uint32_t zb = smem[OFF_RZ + cur * RZ_BYTES + (i * 8 + g) * 4 + (gi & 3)];
+            zg = zero_pair(zb & 0xF);
+            zg8 = zero_pair(zb >> 4);
+          }
+          const uint4 q = *reinterpret_cast<const uint4 *>(qs + (i * 32 + lane) * 16);
+          uint32_t u[4][4];
+          unpack_word(q.x, zg, zg8, u[0]);
+          unpack_word(q.y, zg, zg8, u[1]);
+          unpack_word(q.z, zg, zg8, u[2]);
+          unpack_word(q.w, zg, zg8, u[3]);
+          // row 16i+g holds k = 16t + 4s + {0,1} in u[s][0] and {2,3} in u[s][2];
+          // row 16i+g+8 likewise in u[s][1], u[s][3]
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int n = 16 * i + g + 8 * h;
+            uint8_t *row = bt + (n >> 3) * 1024 + (n & 7) * 128;
+            const uint4 lo = make_uint4(u[0][h], u[0][2 + h], u[1][h], u[1][2 + h]);
+            const uint4 hi = make_uint4(u[2][h], u[2][2 + h], u[3][h], u[3][2 + h]);
+            *reinterpret_cast<uint4 *>(row + (((2 * t) ^ (n & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4 *>(row + (((2 * t + 1) ^ (n & 7)) << 4)) = hi;
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bars.full_B(sb));
+        mbar_arrive(bars.empty_L(sl));
+        ++ls;
+        ++bs;
+      }
+    }
+    if (!ok) give_up(abort_flag, p.err);
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31 = tile rows
+    const int hf = (warp - 8) >> 2;  // columns 128*hf .. +127
+    float acc[128];
+    uint32_t gc = 0, sc = 0;
+    int cur = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+      const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+      for (int gi = 0; gi < p.ng; ++gi) {
+        if ((gi & 3) == 0) {
+          cur = sc % SS;
+          if (!mbar_wait(bars.conv_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
+          ++sc;
+        }
+        const int b = gc & 1;
+        if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const float *scp = reinterpret_cast<const float *>(smem + OFF_SC) + cur * SC_FLOATS + (gi & 3) * BN + hf * 128;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          float d[32];
+          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + hf * 128 + ch * 32), d);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 s4 = *reinterpret_cast<const float4 *>(scp + ch * 32 + c);
+            float2 a0 = make_float2(acc[ch * 32 + c], acc[ch * 32 + c + 1]);
+            float2 a1 = make_float2(acc[ch * 32 + c + 2], acc[ch * 32 + c + 3]);
+            a0 = __ffma2_rn(make_float2(s4.x, s4.y), make_float2(d[c], d[c + 1]), a0);
+            a1 = __ffma2_rn(make_float2(s4.z, s4.w), make_float2(d[c + 2], d[c + 3]), a1);
+            acc[ch * 32 + c] = a0.x;
+            acc[ch * 32 + c + 1] = a0.y;
+            acc[ch * 32 + c + 2] = a1.x;
+            acc[ch * 32 + c + 3] = a1.y;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bars.tempty(b));
+        if ((gi & 3) == 3 || gi == p.ng - 1) mbar_arrive(bars.empty_S(cur));
+        ++gc;
+      }
+      if (!ok) break;
+      const int m = mt * BM + 32 * q + lane;
+      if (m < p.M) {
+        uint16_t *yrow = p.y + (size_t)m * p.ld;
+        const bool vec = (p.ld & 7) == 0;
+        if (GATEUP) {
+          // columns 32pp + r (gate) and 32pp + 16 + r (up) of this half are rows
+          // 16 * (8 nt + 4 hf + pp) + r of the gate and up weights
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            const int n0 = 16 * (8 * nt + 4 * hf + pp);
+            float hv[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              const float gv = acc[32 * pp + r], uv = acc[32 * pp + 16 + r];
+              hv[r] = gv / (1.0f + __expf(-gv)) * uv;
+            }
+            if (vec && n0 + 16 <= p.N) {
+              uint4 v0 = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]),
+                                    pack_bf16x2(hv[4], hv[5]), pack_bf16x2(hv[6], hv[7]));
+              uint4 v1 = make_uint4(pack_bf16x2(hv[8], hv[9]), pack_bf16x2(hv[10], hv[11]),
+                                    pack_bf16x2(hv[12], hv[13]), pack_bf16x2(hv[14], hv[15]));
+              *reinterpret_cast<uint4 *>(yrow + n0) = v0;
+              *reinterpret_cast<uint4 *>(yrow + n0 + 8) = v1;
+            } else {
+#pragma unroll
+              for (int r = 0; r < 16; ++r)
+                if (n0 + r < p.N) {
+                  __nv_bfloat16 bv = __float2bfloat16_rn(hv[r]);
+                  yrow[n0 + r] = *reinterpret_cast<uint16_t *>(&bv);
+                }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c8 = 0; c8 < 16; ++c8) {
+            const int n0 = nt * BN + hf * 128 + c8 * 8;
+            if (vec && n0 + 8 <= p.N) {
+              uint4 v = make_uint4(pack_bf16x2(acc[c8 * 8], acc[c8 * 8 + 1]),
+                                   pack_bf16x2(acc[c8 * 8 + 2], acc[c8 * 8 + 3]),
+                                   pack_bf16x2(acc[c8 * 8 + 4], acc[c8 * 8 + 5]),
+                                   pack_bf16x2(acc[c8 * 8 + 6], acc[c8 * 8 + 7]));
+              *reinterpret_cast<uint4 *>(yrow + n0) = v;
+            } else {
+#pragma unroll
+              for (int r = 0; r < 8; ++r)
+                if (n0 + r < p.N) {
+                  __nv_bfloat16 bv = __float2bfloat16_rn(acc[c8 * 8 + r]);
+                  yrow[n0 + r] = *reinterpret_cast<uint16_t *>(&bv);
+                }
+            }
+          }
+        }
+      }
+    }
+    if (!ok) give_up(abort_flag, p.err);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps and launch
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool SYM, bool GATEUP>
+cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
+                           const CUtensorMap &tz, const PromptParams &p, int grid, cudaStream_t s) {
+  auto kern = prompt_tc_kernel<SYM, GATEUP>;
+  static bool attr_set = false;  // per instantiation; attribute is per device function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<grid, kThreads, SMEM_ALLOC, s>>>(tx, tq, ts, tz, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
+  const int rows = packed_rows(c);
+  const Layout L = make_layout(rows, c.K, c.group, c.sym);
+  CUtensorMap tx, tq, ts, tz;
+  bool ok = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, (uint64_t)c.K, (uint64_t)c.M,
+                      (uint64_t)c.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.codes_off, (uint64_t)L.chunks * 128,
+                       (uint64_t)L.tiles, (uint64_t)L.chunks * kChunkBytes, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.scales_off, (uint64_t)L.gblocks * 32,
+                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, 16,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (c.sym) {
+    tz = ts;  // unused
+  } else {
+    ok = ok && encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.zeros_off, (uint64_t)L.gblocks * 8,
+                         (uint64_t)L.tiles, (uint64_t)L.gblocks * kZeroBlockBytes, 8, 16,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  PromptParams p;
+  p.y = c.y;
+  p.M = c.M;
+  p.N = c.N;
+  p.K = c.K;
+  p.ld = c.N;
+  p.mtiles = (c.M + BM - 1) / BM;
+  p.ntiles = (rows + BN - 1) / BN;
+  p.nk = c.K / BK;
+  p.ng = c.K / c.group;
+  p.spg = c.group / BK;
+  p.err = c.err;
+  const int ntot = p.mtiles * p.ntiles;
+  const int grid = ntot < sm_count ? ntot : sm_count;
+  if (c.sym) {
+    return c.gateup ? launch_variant<true, true>(tx, tq, ts, tz, p, grid, c.stream)
+                    : launch_variant<true, false>(tx, tq, ts, tz, p, grid, c.stream);
+  }
+  return c.gateup ? launch_variant<false, true>(tx, tq, ts, tz, p, grid, c.stream)
+                  : launch_variant<false, false>(tx, tq, ts, tz, p, grid, c.stream);
+}
+
+}  // namespace w4a16

@@ -1,0 +1,205 @@
+// Offline repack (canonical -> tiled layout) and the exact dequantisation
+// read-back used by the tests.
+//
+// The canonical packing (nibble j of word c holds k = 8c + j) and the exact
+// w = (q - z) * scale follow the INT4 kernels of the GRIMOIRE v1.7 release
+// notes ("What changed"); the tiled order is this library's own, described in
+// w4a16_common.cuh.
+#include "w4a16_internal.h"
+
+namespace w4a16 {
+namespace {
+
+struct RepackSrc {
+  const uint32_t *qw[2];
+  const uint16_t *sc[2];
+  const uint32_t *z[2];
+  int n_src;     // rows of each source weight
+  int gateup;    // 0: one weight, tile T = rows 16T..; 1: tiles alternate gate, up
+};
+
+// (source, row) of row r (0..15) of tile T; row < 0 for padding
+__device__ __forceinline__ int src_row(const RepackSrc &s, int T, int r, int &which) {
+  int row;
+  if (s.gateup) {
+    which = T & 1;
+    row = 16 * (T >> 1) + r;
+  } else {
+    which = 0;
+    row = 16 * T + r;
+  }
+  return row < s.n_src ? row : -1;
+}
+
+__device__ __forceinline__ uint32_t zero_code(const RepackSrc &s, int which, int row, int gi,
+                                              int groups) {
+  int zw = (groups + 7) / 8;
+  uint32_t word = s.z[which][(size_t)row * zw + gi / 8];
+  return (word >> (4 * (gi % 8))) & 0xFu;
+}
+
+__global__ void repack_codes_kernel(RepackSrc s, Layout L, uint32_t *out) {
+  const size_t total = (size_t)L.tiles * L.chunks * 128;
+  const int kw = L.K / 8;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int sidx = (int)(idx & 3);
+    const int lane = (int)((idx >> 2) & 31);
+    const size_t tc = idx >> 7;
+    const int c = (int)(tc % L.chunks);
+    const int T = (int)(tc / L.chunks);
+    const int g = lane >> 2, t = lane & 3;
+    const int k0 = 64 * c + 16 * t + 4 * sidx;  // k0 % 8 is 0 or 4
+    uint32_t src[2];
+    for (int h = 0; h < 2; ++h) {
+      int which;
+      int row = src_row(s, T, g + 8 * h, which);
+      src[h] = row < 0 ? 0u : (s.qw[which][(size_t)row * kw + k0 / 8] >> (4 * (k0 % 8)));
+    }
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int kofs = 2 * ((j >> 1) & 1) + (j >> 2);
+      const uint32_t code = (src[j & 1] >> (4 * kofs)) & 0xFu;
+      word |= code << (4 * j);
+    }
+    out[idx] = word;
+  }
+}
+
+__global__ void repack_scales_kernel(RepackSrc s, Layout L, uint16_t *out) {
+  const size_t total = (size_t)L.tiles * L.gblocks * 64;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int h = (int)(idx & 1);
+    const int j = (int)((idx >> 1) & 3);
+    const int g = (int)((idx >> 3) & 7);
+    const size_t tb = idx >> 6;
+    const int blk = (int)(tb % L.gblocks);
+    const int T = (int)(tb / L.gblocks);
+    const int gi = 4 * blk + j;
+    int which;
+    const int row = src_row(s, T, g + 8 * h, which);
+    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0
+                                           : s.sc[which][(size_t)row * L.groups + gi];
+  }
+}
+
+__global__ void repack_zeros_kernel(RepackSrc s, Layout L, uint8_t *out) {
+  const size_t total = (size_t)L.tiles * L.gblocks * 32;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int j = (int)(idx & 3);
+    const int g = (int)((idx >> 2) & 7);
+    const size_t tb = idx >> 5;
+    const int blk = (int)(tb % L.gblocks);
+    const int T = (int)(tb / L.gblocks);
+    const int gi = 4 * blk + j;
+    uint32_t v = 0;
+    if (gi < L.groups) {
+      for (int h = 0; h < 2; ++h) {
+        int which;
+        const int row = src_row(s, T, g + 8 * h, which);
+        if (row >= 0) v |= zero_code(s, which, row, gi, L.groups) << (4 * h);
+      }
+    }
+    out[idx] = (uint8_t)v;
+  }
+}
+
+// w[n][k] = (q - z) * scale through the same unpack as the GEMM kernels
+__global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float *w) {
+  const size_t total = (size_t)L.tiles * L.chunks * 32;
+  const uint4 *codes = reinterpret_cast<const uint4 *>(packed + L.codes_off);
+  const uint32_t *scales = reinterpret_cast<const uint32_t *>(packed + L.scales_off);
+  const uint8_t *zeros = packed + L.zeros_off;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int lane = (int)(idx & 31);
+    const size_t tc = idx >> 5;
+    const int c = (int)(tc % L.chunks);
+    const int T = (int)(tc / L.chunks);
+    const int g = lane >> 2, t = lane & 3;
+    const int gi = (64 * c) / L.group;
+    const size_t bi = ((size_t)T * L.gblocks + gi / 4) * 8 + g;
+    const uint32_t sw = scales[bi * 4 + (gi & 3)];
+    const float s_g = bf16lo_to_f32(sw), s_g8 = bf16hi_to_f32(sw);
+    uint32_t zg, zg8;
+    if (L.sym) {
+      zg = zg8 = zero_pair(8);
+    } else {
+      const uint32_t zb = zeros[bi * 4 + (gi & 3)];
+      zg = zero_pair(zb & 0xF);
+      zg8 = zero_pair(zb >> 4);
+    }
+    const uint4 q = codes[idx];
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+    const int n0 = 16 * T + g, n1 = n0 + 8;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t u[4];
+      unpack_word(words[s], zg, zg8, u);
+      const int k = 64 * c + 16 * t + 4 * s;
+      // u[0]: row g, k+0 / k+1; u[1]: row g+8, k+0 / k+1; u[2]: row g, k+2 / k+3; u[3]: row g+8
+      if (n0 < N) {
+        float *r = w + (size_t)n0 * L.K + k;
+        r[0] = bf16lo_to_f32(u[0]) * s_g;
+        r[1] = bf16hi_to_f32(u[0]) * s_g;
+        r[2] = bf16lo_to_f32(u[2]) * s_g;
+        r[3] = bf16hi_to_f32(u[2]) * s_g;
+      }
+      if (n1 < N) {
+        float *r = w + (size_t)n1 * L.K + k;
+        r[0] = bf16lo_to_f32(u[1]) * s_g8;
+        r[1] = bf16hi_to_f32(u[1]) * s_g8;
+        r[2] = bf16lo_to_f32(u[3]) * s_g8;
+        r[3] = bf16hi_to_f32(u[3]) * s_g8;
+      }
+    }
+  }
+}
+
+int grid_for(size_t work, int threads) {
+  size_t b = (work + threads - 1) / threads;
+  if (b > 65535u * 16u) b = 65535u * 16u;
+  return (int)(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0,
+                          const int32_t *qw1, const uint16_t *sc1, const int32_t *z1,
+                          int n_src, bool gateup, const Layout &L, uint8_t *packed,
+                          cudaStream_t stream) {
+  RepackSrc s;
+  s.qw[0] = reinterpret_cast<const uint32_t *>(qw0);
+  s.qw[1] = reinterpret_cast<const uint32_t *>(qw1 ? qw1 : qw0);
+  s.sc[0] = sc0;
+  s.sc[1] = sc1 ? sc1 : sc0;
+  s.z[0] = reinterpret_cast<const uint32_t *>(z0);
+  s.z[1] = reinterpret_cast<const uint32_t *>(z1 ? z1 : z0);
+  s.n_src = n_src;
+  s.gateup = gateup ? 1 : 0;
+  const int th = 256;
+  size_t nc = (size_t)L.tiles * L.chunks * 128;
+  repack_codes_kernel<<<grid_for(nc, th), th, 0, stream>>>(s, L,
+                                                          reinterpret_cast<uint32_t *>(packed + L.codes_off));
+  size_t ns = (size_t)L.tiles * L.gblocks * 64;
+  repack_scales_kernel<<<grid_for(ns, th), th, 0, stream>>>(
+      s, L, reinterpret_cast<uint16_t *>(packed + L.scales_off));
+  if (!L.sym) {
+    size_t nz = (size_t)L.tiles * L.gblocks * 32;
+    repack_zeros_kernel<<<grid_for(nz, th), th, 0, stream>>>(s, L, packed + L.zeros_off);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, float *w,
+                              cudaStream_t stream) {
+  const int th = 256;
+  size_t n = (size_t)L.tiles * L.chunks * 32;
+  dequantize_kernel<<<grid_for(n, th), th, 0, stream>>>(packed, L, N, w);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

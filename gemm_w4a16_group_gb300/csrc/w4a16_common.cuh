@@ -1,0 +1,262 @@
+// Device-side helpers shared by the W4A16 kernels: the repacked layout, the
+// exact nibble -> bf16 (q - z) rebuild, and thin wrappers over the sm_100-family
+// PTX used by the tcgen05 GEMM (mbarrier, TMA, tcgen05.*).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace w4a16 {
+
+// ---------------------------------------------------------------------------
+// Repacked layout (see w4a16_repack in w4a16.h)
+//
+//  Rows are tiled 16 at a time (tile T = rows 16T .. 16T+15) and K in chunks
+//  of 64. For tile T, chunk c and lane L = 4g + t (g = 0..7, t = 0..3) there is
+//  one 16-byte run of four 32-bit words s = 0..3. Word s holds the codes of
+//  rows 16T+g and 16T+g+8 at k = 64c + 16t + 4s + {0..3}:
+//
+//     nibble j of word s  ->  row 16T + g + 8*(j & 1),  k = 64c + 16t + 4s + kofs(j)
+//     kofs(j) = 2*((j >> 1) & 1) + (j >> 2)        (0,0,2,2,1,1,3,3)
+//
+//  so that ((word >> 4p) & 0x000F000F) puts the two codes of one mma.sync A
+//  register (row g or g+8, two consecutive k) into the two 16-bit halves, and
+//  the 16 values of k a lane owns are contiguous in x.
+//
+//  Scales: per tile, per block of four groups, [g 0..7][group j 0..3][h 0..1]
+//  bf16 = scale(row 16T + g + 8h, group 4*blk + j): 128 bytes per block.
+//  Zeros (asymmetric only): per tile and block, [g][j] bytes holding
+//  zero(row g) | zero(row g+8) << 4: 32 bytes per block.
+// ---------------------------------------------------------------------------
+constexpr int kTileRows = 16;
+constexpr int kChunkK = 64;
+constexpr int kChunkBytes = 512;      // 32 lanes x 16 bytes
+constexpr int kScaleBlockBytes = 128; // per tile, per 4 groups
+constexpr int kZeroBlockBytes = 32;
+
+struct Layout {
+  int N, K, group, sym;
+  int tiles;       // ceil(N / 16)
+  int chunks;      // K / 64
+  int groups;      // K / group
+  int gblocks;     // ceil(groups / 4)
+  size_t codes_off, scales_off, zeros_off, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int N, int K, int group, int sym) {
+  Layout L;
+  L.N = N; L.K = K; L.group = group; L.sym = sym;
+  L.tiles = (N + kTileRows - 1) / kTileRows;
+  L.chunks = K / kChunkK;
+  L.groups = K / group;
+  L.gblocks = (L.groups + 3) / 4;
+  L.codes_off = 0;
+  L.scales_off = align_up((size_t)L.tiles * L.chunks * kChunkBytes, 256);
+  L.zeros_off = align_up(L.scales_off + (size_t)L.tiles * L.gblocks * kScaleBlockBytes, 256);
+  size_t end = L.zeros_off + (sym ? 0 : (size_t)L.tiles * L.gblocks * kZeroBlockBytes);
+  L.total = align_up(end, 256);
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Exact unpack. bf16 0x4300 is 128.0 with a mantissa step of 1, so
+// (0x4300 | c) is exactly 128 + c for a 4-bit c, and subtracting the bf16
+// value 128 + z leaves the integer q - z (|q - z| <= 15) exactly. This is the
+// "(0x4300 | c) - 128" code rebuild of the TensorFold PR #859 lane GEMV, with
+// the zero point folded into the subtrahend.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kNibMask = 0x000F000Fu;
+constexpr uint32_t kBf16x2_128 = 0x43004300u;
+
+// bf16x2 (128 + z) in both halves
+__device__ __forceinline__ uint32_t zero_pair(uint32_t z) { return kBf16x2_128 | (z * 0x00010001u); }
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162 *>(&a),
+                             *reinterpret_cast<__nv_bfloat162 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Four bf16x2 registers of (q - z) from one packed word: out[p] holds nibble p
+// (low half) and nibble p + 4 (high half); out[0], out[2] are row g and use
+// zg = zero_pair(z of row g), out[1], out[3] are row g + 8 and use zg8.
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t zg, uint32_t zg8, uint32_t out[4]) {
+  out[0] = bf16x2_sub((w & kNibMask) | kBf16x2_128, zg);
+  out[1] = bf16x2_sub(((w >> 4) & kNibMask) | kBf16x2_128, zg8);
+  out[2] = bf16x2_sub(((w >> 8) & kNibMask) | kBf16x2_128, zg);
+  out[3] = bf16x2_sub(((w >> 12) & kNibMask) | kBf16x2_128, zg8);
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// Error word written by kernels (bounded waits that gave up).
+// ---------------------------------------------------------------------------
+constexpr int kErrTimeout = 1;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase completed, false after kWaitLimitNs or
+// when *abort became non-zero (another role gave up).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used after giving up, to let
+// asynchronous work this thread started finish before the CTA exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor) and proxy fences
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// generic-proxy shared-memory writes -> visible to the async proxy (tensor core)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, kind::f16, single CTA
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// mbarrier arrives once every tcgen05 op issued so far by this thread completed
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor for a K-major operand stored with the
+// 128-byte swizzle: rows of 64 bf16 (128 B), 8-row atoms of 1024 B stacked
+// along M/N (stride 1024 B), descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace w4a16

@@ -1,0 +1,40 @@
+// Internal launcher interface between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "w4a16_common.cuh"
+
+namespace w4a16 {
+
+// One matmul call as the kernels see it. For the fused gate/up form,
+// N is the rows of ONE of the two weights (N_each), `packed` the interleaved
+// buffer, and the output has N columns.
+struct GemmCall {
+  const uint16_t *x;
+  const uint8_t *packed;
+  uint16_t *y;
+  int M, N, K, group, sym;
+  bool gateup;
+  cudaStream_t stream;
+  int *err;  // device error word (bounded waits that gave up)
+};
+
+// Rows covered by the packed buffer of a call (padded; interleaved for gate/up).
+inline int packed_rows(const GemmCall &c) {
+  return c.gateup ? 2 * ((c.N + 127) / 128 * 128) : c.N;
+}
+
+cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0,
+                          const int32_t *qw1, const uint16_t *sc1, const int32_t *z1,
+                          int n_src, bool gateup, const Layout &L, uint8_t *packed,
+                          cudaStream_t stream);
+cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, float *w,
+                              cudaStream_t stream);
+
+cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count);  // 1 <= M <= 16
+cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count);     // M == 1, not gate/up
+cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count);   // any M
+
+}  // namespace w4a16

@@ -1,0 +1,157 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) group-quantized INT4-weight x
+ * bf16-activation matmul library.
+ *
+ *   y[M, N] = x[M, K] . dequant(W)[N, K]^T,   w[n][k] = (q[n][k] - z[n][k/G]) * scale[n][k/G]
+ *
+ * The dequantisation is the exact "(q - z) * scale" of the INT4 kernels in the
+ * GRIMOIRE v1.7 release notes ("What changed"): q a 4-bit code, one bf16 scale
+ * per (output row, K-group) with group G = 64 or 128, and z = 8 for the
+ * symmetric GPTQ-Int4 checkpoints or a packed 4-bit zero point for the
+ * asymmetric AutoRound W4A16 ones (same page, measurement table). The regimes
+ * are those the same pages measure: one-row decode, 2-16 rows of batched
+ * decode and speculative verify, the output-vocabulary head over all verify
+ * rows in one pass, and 4,096-row prompts with the feed-forward gate fused in
+ * (GRIMOIRE v1.8 release notes, "INT4 verify faster" and "INT4 prompt
+ * processing").
+ *
+ * Canonical (input) layout, row-major, little-endian:
+ *   qweight int32  [N][K/8]            nibble j (bits 4j..4j+3) of word c holds k = 8c + j
+ *   scales  bf16   [N][K/G]            bf16 values passed as uint16_t bit patterns
+ *   zeros   int32  [N][ceil(K/G/8)]    nibble j of word c holds the zero of group 8c + j
+ *                                      (asymmetric only; unused nibbles ignored)
+ *
+ * Conventions for every call:
+ *   - Pointers named x, y, h, qweight, scales, zeros, packed, w_out are DEVICE
+ *     pointers owned by the caller; the library allocates no device memory
+ *     and keeps no pointer after a call returns.
+ *   - Every compute call is asynchronous on `stream` (NULL = legacy default
+ *     stream) and launches kernels on the calling thread's current device.
+ *   - Return value: W4A16_OK (0) or a negative W4A16_ERR_* code. On any error
+ *     detected before launch nothing is launched and no memory is written.
+ *     W4A16_ERR_CUDA means a CUDA call failed; w4a16_last_cuda_error() gives
+ *     its cudaError_t value (thread-local).
+ *   - bf16 values are IEEE bfloat16 bit patterns in uint16_t; outputs are
+ *     rounded to nearest-even from float32.
+ *   - sym != 0 selects z = 8; then `zeros` is ignored and may be NULL.
+ *   - Supported sizes: 1 <= M, 1 <= N, 64 <= K, K % G == 0, G in {64, 128},
+ *     M, N, K below 2^31 / 16.
+ *   - Alignment: x, y, h 16 bytes; packed 256 bytes (cudaMalloc gives both).
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without the CUDA headers (same type as the runtime's). */
+typedef struct CUstream_st *w4a16_stream_t;
+
+#define W4A16_OK 0
+#define W4A16_ERR_INVALID_ARG (-1)  /* size, group, null pointer or reserved argument */
+#define W4A16_ERR_MISALIGNED (-2)   /* a pointer breaks the alignment rules above */
+#define W4A16_ERR_UNSUPPORTED (-3)  /* the current device is not an sm_103 GPU */
+#define W4A16_ERR_CUDA (-4)         /* a CUDA call failed; see w4a16_last_cuda_error() */
+#define W4A16_ERR_TIMEOUT (-5)      /* a bounded wait inside a kernel gave up */
+
+/*
+ * Size in bytes of the repacked weight that w4a16_repack writes for an
+ * N x K weight (codes, scales and, when !sym, zero points, each section
+ * 256-byte aligned; rows padded to a multiple of 16). Returns 0 when the
+ * sizes are not supported.
+ */
+size_t w4a16_repacked_bytes(int N, int K, int group, int sym);
+
+/*
+ * Offline repack of one canonical weight (qweight, scales, zeros as above)
+ * into the library's tiled layout in `packed` (w4a16_repacked_bytes bytes,
+ * caller-allocated device memory). Pure bit moves: no value is rounded, so
+ * every dequantised weight stays exactly (q - z) * scale. Rows are tiled 16 at
+ * a time; within a tile and a 64-wide K chunk each of 32 lanes owns one
+ * 16-byte run of codes for two rows and 16 consecutive k, the order in which
+ * the kernels consume them. Scales (and zeros) sit per tile in blocks of four
+ * groups. Padding rows get code 0, scale 0 and zero 0. Not timed on the hot
+ * path; asynchronous on `stream`.
+ */
+int w4a16_repack(const int32_t *qweight, const uint16_t *scales, const int32_t *zeros,
+                 int N, int K, int group, int sym, void *packed, w4a16_stream_t stream);
+
+/* Size of the repacked gate/up pair of w4a16_repack_gateup (N_each rows each). */
+size_t w4a16_gateup_repacked_bytes(int N_each, int K, int group, int sym);
+
+/*
+ * Offline repack of the feed-forward gate and up weights (two canonical
+ * weights of N_each rows each) into one buffer whose 16-row tiles alternate
+ * gate, up, gate, up, ... (N_each padded to a multiple of 128), so that one
+ * tile of the prompt GEMM holds 128 gate rows and the 128 matching up rows.
+ * The result is also a valid w4a16_repack buffer of 2 * round_up(N_each, 128)
+ * rows in that interleaved order.
+ */
+int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const int32_t *z_gate,
+                        const int32_t *qw_up, const uint16_t *sc_up, const int32_t *z_up,
+                        int N_each, int K, int group, int sym, void *packed,
+                        w4a16_stream_t stream);
+
+/*
+ * y[M][N] (bf16, row-major) = x[M][K] (bf16, row-major) . dequant(W)^T, with
+ * W given as the output of w4a16_repack for the same (N, K, group, sym).
+ * float32 accumulation; each group's partial sum is scaled in float32.
+ * `scales` and `zeros` are reserved: scales and zero points travel inside
+ * `packed`, and both must be NULL (else W4A16_ERR_INVALID_ARG).
+ * Kernel choice: M = 1 -> one-row GEMV; 2 <= M <= 16 -> small-M tensor-core
+ * kernel reading each weight once for all rows; M > 16 -> the tcgen05 GEMM.
+ * Results are bitwise reproducible run to run (no atomics in any sum).
+ */
+int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,
+               const int32_t *zeros, int M, int N, int K, int group, int sym, uint16_t *y,
+               w4a16_stream_t stream);
+
+/*
+ * Fused feed-forward gate (GRIMOIRE v1.8, "INT4 prompt processing"):
+ *   h[M][N_each] = SiLU(x Wg^T) * (x Wu^T),  SiLU(v) = v / (1 + e^-v),
+ * with both products accumulated in float32 and never rounded before the
+ * SiLU and the product; h is rounded once to bf16. `packed_gateup` comes from
+ * w4a16_repack_gateup. Any M >= 1.
+ */
+int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N_each, int K,
+                      int group, int sym, uint16_t *h, w4a16_stream_t stream);
+
+/*
+ * Test export: w_out[N][K] (float32, row-major) = (q - z) * scale read back
+ * from a repacked buffer through the kernels' own unpack. Exact.
+ */
+int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float *w_out,
+                     w4a16_stream_t stream);
+
+/*
+ * Waits for all work on the current device, then reads and clears the
+ * device error word that a kernel sets when one of its bounded waits gave up
+ * (W4A16_ERR_TIMEOUT; the kernel's outputs are then undefined). W4A16_OK
+ * when no kernel gave up since the last call.
+ */
+int w4a16_kernel_status(void);
+
+/* Static string for a status code. */
+const char *w4a16_strerror(int status);
+
+/* cudaError_t of the last W4A16_ERR_CUDA on this thread (0 if none). */
+int w4a16_last_cuda_error(void);
+
+/*
+ * Kernel selection override for A/B measurement: 0 = automatic (default),
+ * 1 = force the CUDA-core one-row GEMV for M = 1, 2 = force the small-M
+ * tensor-core kernel for M <= 16, 3 = force the tcgen05 GEMM for any M.
+ * Returns the previous value. Process-wide; not thread-safe against
+ * concurrent calls.
+ */
+int w4a16_set_kernel_override(int which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

@@ -27,19 +27,42 @@ __all__ = [
     "make_scales", "make_zeros", "make_x", "make_problem", "TENSOR_IDS",
 ]
 
-_GAMMA = np.uint64(0x9E3779B97F4A7C15)
-_M1 = np.uint64(0xBF58476D1CE4E5B9)
-_M2 = np.uint64(0x94D049BB133111EB)
+def _signed(c: int) -> np.int64:
+    return np.int64(c - (1 << 64) if c >= (1 << 63) else c)
+
+
+# multiplications run on int64 views: two's-complement wrap-around is the same
+# modulo-2^64 product, and numpy's int64 multiply is far faster than uint64's
+_GAMMA = _signed(0x9E3779B97F4A7C15)
+_M1 = _signed(0xBF58476D1CE4E5B9)
+_M2 = _signed(0x94D049BB133111EB)
 
 # stream id of every tensor a problem draws
 TENSOR_IDS = {"x": 1, "qweight": 2, "scales": 3, "zeros": 4,
               "qweight_up": 5, "scales_up": 6, "zeros_up": 7}
 
 
+_BLOCK = 1 << 20  # draws per in-place block (reused buffers keep page faults down)
+
+
+def _mix_inplace(z: np.ndarray, tmp: np.ndarray) -> None:
+    """SplitMix64 output function applied in place to a uint64 array."""
+    zi = z.view(np.int64)
+    np.right_shift(z, np.uint64(30), out=tmp)
+    np.bitwise_xor(z, tmp, out=z)
+    np.multiply(zi, _M1, out=zi)
+    np.right_shift(z, np.uint64(27), out=tmp)
+    np.bitwise_xor(z, tmp, out=z)
+    np.multiply(zi, _M2, out=zi)
+    np.right_shift(z, np.uint64(31), out=tmp)
+    np.bitwise_xor(z, tmp, out=z)
+
+
 def _mix(z: np.ndarray) -> np.ndarray:
-    z = (z ^ (z >> np.uint64(30))) * _M1
-    z = (z ^ (z >> np.uint64(27))) * _M2
-    return z ^ (z >> np.uint64(31))
+    """SplitMix64 output function on uint64 values (array in, uint64 array out)."""
+    z = np.array(z, dtype=np.uint64, copy=True)
+    _mix_inplace(z, np.empty_like(z))
+    return z
 
 
 def splitmix64_stream(state0: int, n: int, offset: int = 0) -> np.ndarray:
@@ -47,9 +70,21 @@ def splitmix64_stream(state0: int, n: int, offset: int = 0) -> np.ndarray:
 
     Output i (1-based) is mix(state0 + i * gamma) modulo 2^64.
     """
+    out = np.empty(n, dtype=np.uint64)
+    s0 = _signed(state0 & 0xFFFFFFFFFFFFFFFF)
+    step = min(n, _BLOCK) if n else 0
+    idx = np.empty(step, dtype=np.int64)
+    tmp = np.empty(step, dtype=np.uint64)
     with np.errstate(over="ignore"):
-        i = np.arange(offset + 1, offset + n + 1, dtype=np.uint64)
-        return _mix(np.uint64(state0 & 0xFFFFFFFFFFFFFFFF) + i * _GAMMA)
+        for b0 in range(0, n, _BLOCK):
+            b1 = min(n, b0 + _BLOCK)
+            m = b1 - b0
+            zi = out[b0:b1].view(np.int64)
+            np.copyto(idx[:m], np.arange(offset + 1 + b0, offset + 1 + b1, dtype=np.int64))
+            np.multiply(idx[:m], _GAMMA, out=zi)
+            np.add(zi, s0, out=zi)
+            _mix_inplace(out[b0:b1], tmp[:m])
+    return out
 
 
 def _stream_state(seed: int, tensor_id: int) -> int:
@@ -111,9 +146,25 @@ def make_codes(N: int, K: int, seed: int, tid: int) -> np.ndarray:
     return (bits >> np.uint64(60)).astype(np.uint8).reshape(N, K)
 
 
-def make_qweight(N: int, K: int, seed: int, tid: int = TENSOR_IDS["qweight"]) -> np.ndarray:
+def make_qweight(N: int, K: int, seed: int, tid: int = TENSOR_IDS["qweight"],
+                 block_rows: int = 1 << 14) -> np.ndarray:
+    """Packed uniform codes, int32 [N, K/8]: word w (row-major) is the low (w even)
+    or high (w odd) 32 bits of draw w // 2, i.e. 16 independent uniform 4-bit
+    codes per draw. Drawn in row blocks so full-size weights stay cheap."""
     assert K % 8 == 0
-    return pack_nibbles_rows(make_codes(N, K, seed, tid))
+    W = K // 8
+    state = _stream_state(seed, tid)
+    out = np.empty((N, W), dtype=np.uint32)
+    for r0 in range(0, N, block_rows):
+        r1 = min(N, r0 + block_rows)
+        w0, w1 = r0 * W, r1 * W                      # word range [w0, w1)
+        d0, d1 = w0 // 2, (w1 + 1) // 2              # draws covering it
+        bits = splitmix64_stream(state, d1 - d0, offset=d0)
+        words = np.empty(2 * (d1 - d0), dtype=np.uint32)
+        words[0::2] = (bits & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+        words[1::2] = (bits >> np.uint64(32)).astype(np.uint32)
+        out[r0:r1] = words[w0 - 2 * d0: w1 - 2 * d0].reshape(r1 - r0, W)
+    return out.view(np.int32)
 
 
 def make_scales(N: int, Kg: int, lo: float, hi: float, seed: int,

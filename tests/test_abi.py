@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every function include/w4a16.h
+declares; argument checks that need no GPU return their status codes without
+touching CUDA (no device is needed, so these run on CPU-only hosts too)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_w4a16_group_gb300 as w4
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "w4a16.h")
+
+OK, INVALID, MISALIGNED = 0, -1, -2
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return w4.lib()
+
+
+def test_exports_match_header(L):
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    assert sorted(w4.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_library_is_in_tree(L):
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    assert os.path.commonpath([w4.library_path(), root]) == root
+
+
+def test_repacked_bytes_layout(L):
+    # N=256, K=512, G=128: 16 tiles x 8 chunks x 512 B of codes, then one
+    # 4-group block of scales per tile (128 B), then (asym) 32 B of zeros per tile
+    assert w4.repacked_bytes(256, 512, 128, True) == 65536 + 2048
+    assert w4.repacked_bytes(256, 512, 128, False) == 65536 + 2048 + 512
+    # ragged N pads to 16 rows; every section is 256-byte aligned
+    n = w4.repacked_bytes(250, 5120, 64, False)
+    assert n % 256 == 0 and n == 16 * 80 * 512 + 16 * 20 * 128 + 16 * 20 * 32
+    # gate/up: N_each padded to 128, two weights
+    assert w4.gateup_repacked_bytes(100, 512, 128, True) == w4.repacked_bytes(256, 512, 128, True)
+    for bad in [(0, 512, 128), (16, 512, 96), (16, 100, 64), (16, 32, 64), (16, 192, 128)]:
+        assert w4.repacked_bytes(*bad, True) == 0
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced on these paths
+
+
+def _gemm(L, x=FAKE, packed=FAKE, scales=None, zeros=None, M=4, N=64, K=128, group=64, sym=1, y=FAKE):
+    P = ctypes.c_void_p
+    return L.w4a16_gemm(P(x), P(packed), P(scales), P(zeros), M, N, K, group, sym, P(y), None)
+
+
+def test_gemm_argument_checks(L):
+    assert _gemm(L, x=None) == INVALID
+    assert _gemm(L, y=None) == INVALID
+    assert _gemm(L, packed=None) == INVALID
+    assert _gemm(L, scales=FAKE) == INVALID       # reserved: must be NULL
+    assert _gemm(L, zeros=FAKE) == INVALID
+    assert _gemm(L, M=0) == INVALID
+    assert _gemm(L, N=0) == INVALID
+    assert _gemm(L, K=96, group=64) == INVALID    # K % G
+    assert _gemm(L, group=32) == INVALID
+    assert _gemm(L, K=0) == INVALID
+    assert _gemm(L, x=FAKE + 8) == MISALIGNED
+    assert _gemm(L, y=FAKE + 2) == MISALIGNED
+    assert _gemm(L, packed=FAKE + 128) == MISALIGNED
+
+
+def test_other_entry_points_argument_checks(L):
+    P = ctypes.c_void_p
+    assert L.w4a16_gateup_silu(P(FAKE), None, 4, 64, 128, 64, 1, P(FAKE), None) == INVALID
+    assert L.w4a16_gateup_silu(P(FAKE), P(FAKE), 4, 64, 100, 64, 1, P(FAKE), None) == INVALID
+    assert L.w4a16_gateup_silu(P(FAKE + 4), P(FAKE), 4, 64, 128, 64, 1, P(FAKE), None) == MISALIGNED
+    assert L.w4a16_repack(None, P(FAKE), None, 64, 128, 64, 1, P(FAKE), None) == INVALID
+    assert L.w4a16_repack(P(FAKE), P(FAKE), None, 64, 128, 64, 0, P(FAKE), None) == INVALID  # asym needs zeros
+    assert L.w4a16_repack(P(FAKE), P(FAKE), None, 64, 128, 64, 1, P(FAKE + 16), None) == MISALIGNED
+    assert L.w4a16_repack_gateup(P(FAKE), P(FAKE), None, None, P(FAKE), None, 64, 128, 64, 1,
+                                 P(FAKE), None) == INVALID
+    assert L.w4a16_dequantize(P(FAKE), 64, 128, 64, 1, None, None) == INVALID
+    assert L.w4a16_dequantize(P(FAKE), 64, 128, 48, 1, P(FAKE), None) == INVALID
+
+
+def test_strerror_and_override(L):
+    for rc in (0, -1, -2, -3, -4, -5):
+        assert len(w4.strerror(rc)) >= 2
+    assert w4.strerror(-99) == "unknown status"
+    prev = w4.set_kernel_override(w4.KERNEL_SMALLM)
+    assert w4.set_kernel_override(prev) == w4.KERNEL_SMALLM
+    assert w4.set_kernel_override(7) == -1

@@ -1,0 +1,150 @@
+"""CUDA path (through the C ABI) against the float64 oracle.
+
+Bounds: dequantisation is bit-exact; matmul outputs satisfy
+|y - ref| <= 2^-7 |ref| + 1e-5 sum_k |x_k w_nk|; the fused SiLU(gate) * up
+output satisfies the propagated bound in oracle.silu_bound. Sizes here are
+small enough for the oracle to compute every output, and span several tiles
+with ragged tails in N (not a multiple of 16 or of the 256-row GEMM tile) and
+in M (not a multiple of 8 or of the 128-row GEMM tile).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+import gemm_w4a16_group_gb300 as w4
+
+from gpu_helpers import (assert_within, bf16_f64, check_gemm_full, dev, host_bits, kernel,
+                         packed_gateup_of, packed_of, run_gateup, run_gemm, torch, upload)
+
+pytestmark = pytest.mark.gpu
+
+GEMV, SMALLM, TC = w4.KERNEL_GEMV, w4.KERNEL_SMALLM, w4.KERNEL_TC
+
+
+@pytest.mark.parametrize("sym,group", [(True, 128), (False, 64), (True, 64), (False, 128)])
+@pytest.mark.parametrize("N,K", [(250, 512), (64, 1024), (1, 128)])
+def test_dequantize_bit_exact(sym, group, N, K):
+    if K % group:
+        pytest.skip("K % G")
+    p = synth.make_problem(1, N, K, group, sym, seed=N + K)
+    d = upload(p)
+    w = w4.dequantize(packed_of(p, d), N, K, group, sym).cpu().numpy().astype(np.float64)
+    ref = oracle.dequant(p["qweight"], p["scales"], p["zeros"], N, K, group, sym)
+    np.testing.assert_array_equal(w, ref)
+
+
+CASES = [
+    # (kernel, M, N, K, group, sym)
+    (GEMV, 1, 250, 512, 128, True),
+    (GEMV, 1, 1040, 2048, 64, False),
+    (GEMV, 1, 16, 17408 // 8, 128, True),
+    (SMALLM, 1, 250, 512, 128, True),
+    (SMALLM, 2, 1040, 2048, 64, False),
+    (SMALLM, 5, 250, 1024, 128, False),
+    (SMALLM, 8, 520, 2048, 64, True),
+    (SMALLM, 13, 250, 512, 64, False),
+    (SMALLM, 16, 1040, 1024, 128, True),
+    (SMALLM, 16, 32, 5120, 64, False),
+    (TC, 1, 250, 512, 128, True),
+    (TC, 17, 520, 1024, 64, False),
+    (TC, 200, 520, 1024, 128, True),
+    (TC, 130, 300, 640, 64, False),
+    (TC, 256, 512, 512, 128, False),
+]
+
+
+@pytest.mark.parametrize("which,M,N,K,group,sym", CASES)
+def test_gemm_parity(which, M, N, K, group, sym):
+    p = synth.make_problem(M, N, K, group, sym, seed=M * 7 + N + K)
+    y = run_gemm(p, which)
+    check_gemm_full(p, y)
+
+
+@pytest.mark.parametrize("which,M", [(GEMV, 1), (SMALLM, 1), (SMALLM, 8), (SMALLM, 16), (TC, 40)])
+@pytest.mark.parametrize("sym", [True, False])
+def test_one_hot_x_gives_rounded_weight(which, M, sym):
+    """x = e_k: y[n] = (q - z) * scale exactly in float32, so y is its bf16 rounding."""
+    N, K, group = 272, 512, 64
+    p = synth.make_problem(M, N, K, group, sym, seed=3)
+    ks = (np.arange(M) * 97 + 5) % K
+    x = np.zeros((M, K), np.uint16)
+    x[np.arange(M), ks] = 0x3F80
+    p["x"] = x
+    y = run_gemm(p, which)
+    w = oracle.dequant(p["qweight"], p["scales"], p["zeros"], N, K, group, sym)
+    expect = synth.f32_to_bf16_bits(w[:, ks].T.astype(np.float32))
+    np.testing.assert_array_equal(y, expect)
+
+
+@pytest.mark.parametrize("which,M", [(GEMV, 1), (SMALLM, 5), (TC, 33)])
+def test_codes_equal_zero_give_exact_zero(which, M):
+    N, K, group = 96, 512, 128
+    p = synth.make_problem(M, N, K, group, False, seed=4)
+    zmat = synth.make_codes(N, K // group, 4, 9)
+    p["zeros"] = synth.pack_nibbles_rows(zmat)
+    p["qweight"] = synth.pack_nibbles_rows(np.repeat(zmat, group, axis=1))
+    y = run_gemm(p, which)
+    assert np.all((y & 0x7FFF) == 0)
+
+
+@pytest.mark.parametrize("which,M", [(SMALLM, 16), (SMALLM, 5), (TC, 150)])
+def test_rows_independent_and_deterministic(which, M):
+    """Runs are bitwise reproducible; permuting x rows permutes y rows bitwise."""
+    N, K, group = 520, 1024, 64
+    p = synth.make_problem(M, N, K, group, False, seed=5)
+    d = upload(p)
+    packed = packed_of(p, d)
+    y1 = run_gemm(p, which, d, packed)
+    y2 = run_gemm(p, which, d, packed)
+    np.testing.assert_array_equal(y1, y2)
+    perm = np.random.default_rng(0).permutation(M)
+    yp = run_gemm(p, which, d, packed, x=dev(p["x"][perm]))
+    np.testing.assert_array_equal(yp, y1[perm])
+
+
+def test_gemv_and_smallm_agree_within_bound():
+    p = synth.make_problem(1, 2080, 4096, 128, True, seed=6)
+    d = upload(p)
+    packed = packed_of(p, d)
+    a = run_gemm(p, GEMV, d, packed)
+    b = run_gemm(p, SMALLM, d, packed)
+    check_gemm_full(p, a)
+    check_gemm_full(p, b)
+
+
+GATEUP_CASES = [
+    (SMALLM, 1, 136, 512, 128, True),
+    (SMALLM, 5, 300, 1024, 64, False),
+    (SMALLM, 16, 128, 2048, 128, True),
+    (TC, 17, 136, 512, 64, False),
+    (TC, 200, 300, 1024, 128, True),
+]
+
+
+@pytest.mark.parametrize("which,M,N,K,group,sym", GATEUP_CASES)
+def test_gateup_silu_parity(which, M, N, K, group, sym):
+    p = synth.make_problem(M, N, K, group, sym, seed=M + N, gateup=True)
+    h = run_gateup(p, which)
+    mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)
+    ref, g, u, ga, ua = oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"],
+                                              p["qweight_up"], p["scales_up"], p["zeros_up"],
+                                              M, N, K, group, sym, mi, ni)
+    assert_within(h.reshape(-1), ref, oracle.silu_bound(ref, g, u, ga, ua), "gateup")
+
+
+def test_gateup_buffer_is_a_plain_repack_of_interleaved_rows():
+    """The gate/up buffer read as an ordinary weight gives gate and up rows
+    alternating in 16-row tiles."""
+    M, N, K, group = 3, 128, 512, 128
+    p = synth.make_problem(M, N, K, group, True, seed=8, gateup=True)
+    d = upload(p)
+    pg = packed_gateup_of(p, d)
+    y = host_bits(w4.gemm(d["x"], pg, 2 * N, K, group, True))
+    yg = run_gemm(p, SMALLM, d)
+    pu = dict(p, qweight=p["qweight_up"], scales=p["scales_up"], zeros=p["zeros_up"])
+    yu = run_gemm(pu, SMALLM)
+    inter = y.reshape(M, N // 16, 2, 16)
+    np.testing.assert_array_equal(inter[:, :, 0].reshape(M, N), yg)
+    np.testing.assert_array_equal(inter[:, :, 1].reshape(M, N), yu)

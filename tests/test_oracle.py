@@ -246,11 +246,11 @@ def test_gateup_closed_forms(sym):
     # stay exact in float64), and h = SiLU(g) * sum_k x_k
     qu1 = synth.pack_nibbles_rows(np.repeat(zmat + 1, G, axis=1))
     ones = np.full((N, Kg), 0x3F80, np.uint16)
-    h, g, u, _, _ = oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], z, qu1, ones, z,
-                                          M, N, K, G, sym, mi, ni)
+    codes_g = synth.make_codes(N, K, 13, 2)
+    h, g, u, _, _ = oracle.gateup_silu_at(p["x"], synth.pack_nibbles_rows(codes_g), p["scales"], z,
+                                          qu1, ones, z, M, N, K, G, sym, mi, ni)
     xs = [sum(Fraction(float(v)) for v in synth.bf16_bits_to_f32(p["x"][m])) for m in range(M)]
     np.testing.assert_array_equal(u, np.array([float(xs[m]) for m in mi]))
-    codes_g = synth.make_codes(N, K, 13, 2)
     ge, _ = _brute(codes_g, zmat, p["scales"], p["x"], G)
     for i, (m, n) in enumerate(zip(mi, ni)):
         gv = float(ge[m][n])

@@ -39,6 +39,11 @@ def test_distributions():
     assert c.min() == 0 and c.max() == 15
     counts = np.bincount(c.ravel(), minlength=16)
     assert counts.min() > 0.9 * c.size / 16
+    # whole-word draws: 16 codes per SplitMix64 output, every nibble uniform
+    w = synth.make_qweight(64, 1024, 0).view(np.uint32)
+    nib = (w[..., None] >> (4 * np.arange(8, dtype=np.uint32))) & np.uint32(15)
+    counts = np.bincount(nib.ravel(), minlength=16)
+    assert counts.min() > 0.9 * nib.size / 16
     s = synth.bf16_bits_to_f32(synth.make_scales(256, 40, 0.005, 0.02, 0))
     assert s.min() >= 0.005 * (1 - 2 ** -8) and s.max() <= 0.02 * (1 + 2 ** -8)
     x = synth.bf16_bits_to_f32(synth.make_x(4, 4096, 0)).astype(np.float64)
@@ -59,3 +64,14 @@ def test_workload_table():
     assert workloads.algorithmic_bytes(1, 34816, 5120, 128, True) == 91_994_112
     assert w["prompt_gateup_m4096_k5120_n17408"]["kind"] == "gateup"
     assert sum(1 for k in w if k.startswith("smallm_")) == 15
+
+
+def test_qweight_words_are_draw_halves_and_blocking_is_invisible():
+    w = synth.make_qweight(10, 64, 3).view(np.uint32).ravel()
+    d = synth.splitmix64_stream(synth._stream_state(3, synth.TENSOR_IDS["qweight"]), 40)
+    assert w[0] == int(d[0]) & 0xFFFFFFFF and w[1] == int(d[0]) >> 32
+    assert w[79] == int(d[39]) >> 32
+    np.testing.assert_array_equal(synth.make_qweight(37, 128, 5, block_rows=4),
+                                  synth.make_qweight(37, 128, 5))
+    np.testing.assert_array_equal(synth.splitmix64_stream(9, 10, offset=5),
+                                  synth.splitmix64_stream(9, 15)[5:])

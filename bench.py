@@ -40,8 +40,17 @@ L2_BYTES = 129 * 1024 * 1024
 DEFAULT = "decode_ffn_m1"  # gate+up GEMV followed by the down GEMV
 
 
+def parse_shape(spec: str) -> dict:
+    """'M,N,K,G,sym|asym' -> an ad-hoc workload (profiling cases)."""
+    m, n, k, g, s = spec.split(",")
+    return dict(kind="gemm", M=int(m), N=int(n), K=int(k), group=int(g), sym=(s == "sym"),
+                scale_range=(0.005, 0.02), x_scale=1.0)
+
+
 def step_parts(workload: str):
     """[(name, params)] of the calls one step makes."""
+    if workload.startswith("shape:"):
+        return [(workload, parse_shape(workload[len("shape:"):]))]
     if workload == DEFAULT:
         return [("decode_gateup_m1_k5120_n34816", WORKLOADS["decode_gateup_m1_k5120_n34816"]),
                 ("decode_down_m1_k17408_n5120", WORKLOADS["decode_down_m1_k17408_n5120"])]
@@ -127,6 +136,7 @@ def run_cuda(args, rank, world):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     w4.lib()
+    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3}[args.kernel])
     peaks = load_peaks()
 
     def up(a):
@@ -240,7 +250,7 @@ def run_cuda(args, rank, world):
         "n_gpus": world, "steps": nsteps, "warmup": nwarm, "ms_per_step": ms / nsteps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload table)",
-        "config": {"workload": args.workload, "calls_per_step": [pt["name"] for pt in parts],
+        "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
                    "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
                    "parallelism": f"replicas x{world}", "per_call_ms": [round(v, 5) for v in per_call_ms]},
@@ -324,9 +334,12 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default=DEFAULT, choices=[DEFAULT] + list(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT,
+                    help=f"{DEFAULT} (default), one of {sorted(WORKLOADS)}, or shape:M,N,K,G,sym|asym")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],
+                    help="kernel override for A/B measurement (default: automatic choice)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

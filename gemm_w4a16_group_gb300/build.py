@@ -18,8 +18,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(PKG, "_build")
+BUILD = os.environ.get("W4A16_BUILD_DIR") or os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libw4a16_gb300.so")
+# developer knob: extra nvcc flags (e.g. -D tuning macros) for A/B builds
+EXTRA = os.environ.get("W4A16_NVCC_FLAGS", "").split()
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -57,7 +59,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc] + ARCH + CFLAGS + ["-c", src, "-o", obj]
+        cmd = [cc] + ARCH + CFLAGS + EXTRA + ["-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

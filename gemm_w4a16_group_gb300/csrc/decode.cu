@@ -1,45 +1,59 @@
 // Decode-regime kernels, M <= 16 rows of x against the whole weight.
 //
-// Both kernels stream the repacked weight exactly once per call (HBM-bound),
-// each lane issuing one 16-byte load per 16-row tile and 64-wide K chunk, and
-// turn nibbles into exact (q - z) values in registers:
+// Both kernels stream the repacked weight exactly once per call (HBM-bound)
+// and are built around the integer-ALU cost of the nibble unpack, which is
+// what bounds them on GB300:
 //
-//  * smallm_mma_kernel (M = 1..16): the two rows x 16 k a lane holds are the
-//    A fragment of mma.sync m16n8k16 (bf16 in, f32 accumulate) after the
-//    bf16 rebuild; x rows are the B fragment (zero rows above M). One group's
-//    products sum in a fresh accumulator, then acc += scale * partial in
-//    float32. "2-16 rows ... INT4 weights and bf16 activations" is the DPAS
-//    verify GEMM of the GRIMOIRE v1.7 release notes ("What changed"), and the
-//    same pages' v1.8 notes ("INT4 verify faster") show it occupancy-bound:
-//    here the weight tile is read once for all rows and unpacked once.
-//  * gemv_m1_kernel (M = 1): CUDA-core form. Each nibble is rebuilt as a
-//    float32 2^23 + q * 16^p by OR-ing the magic exponent onto it in place
-//    (one LOP3, no shift for the low five nibbles), the constant 2^23 + z * 16^p
-//    is subtracted exactly, the product with x accumulates in float32 (packed
-//    f32x2 FMA), and the 16^-p factor is applied once per group. Lanes then
-//    meet by warp shuffles (the single-user ESIMD GEMV of the same v1.7 notes).
+//  * Every warp owns a ring of shared-memory slots that its lane 0 fills with
+//    bulk asynchronous copies (cp.async.bulk, completion counted on one
+//    mbarrier per slot). A slot is one 256-wide K unit of the warp's tiles:
+//    their packed codes plus the scale (and zero) block. The bytes in flight
+//    cost no registers, and the per-slot bookkeeping is spread over 32 to 64
+//    packed words per lane.
 //
-// Split-K: KW warps of a CTA take disjoint K slices of the same tiles and sum
+//  * smallm_mma_kernel (M = 1..16): a lane's two rows x 16 k are the A
+//    fragment of mma.sync m16n8k16 (bf16 in, f32 accumulate); x rows are the
+//    B fragment. Each packed word becomes four bf16x2 registers of exact
+//    q - z: three shifts and four LOP3s give 128 + q (bf16 0x4300 is 128 with
+//    a mantissa step of 1, the "(0x4300 | c) - 128" rebuild of TensorFold PR
+//    #859) and one bf16x2 subtraction of 128 + z per register leaves q - z.
+//    One group's products sum in a fresh accumulator, then acc += scale *
+//    partial in float32. "2-16 rows ... INT4 weights and bf16 activations" is
+//    the DPAS verify GEMM of the GRIMOIRE v1.7 release notes ("What changed");
+//    their v1.8 notes ("INT4 verify faster") show it occupancy-bound: here each
+//    weight tile is read and unpacked once for all rows and the tensor core
+//    does the multiply-adds.
+//  * gemv_m1_kernel (M = 1): CUDA-core form. Each nibble becomes the float32
+//    2^23 + q * 16^p by OR-ing the magic exponent onto it in place (no shift
+//    for the low five nibbles), 2^23 + z * 16^p is subtracted exactly, the
+//    product with x accumulates in float32 (packed f32x2 FMA), and the 16^-p
+//    factor is applied once per group. Lanes meet by warp shuffles (the
+//    single-user ESIMD GEMV of the same v1.7 notes).
+//
+// Split-K: the warps of a CTA take disjoint K slices of the same tiles and sum
 // through shared memory; for short N, KC CTAs of a cluster split K further and
 // rank 0 sums the others' partials through distributed shared memory, in rank
 // order (split-K by clusters on sm_90+, as in TensorFold PR #859, "What this
-// changes"). Sums never use atomics, so results are bitwise reproducible.
+// changes"). No sum uses atomics, so results are bitwise reproducible.
 #include "w4a16_internal.h"
 
 namespace w4a16 {
 namespace {
 
-constexpr int kMaxWarps = 8;
+constexpr int kWarps = 4;       // warps per CTA
+constexpr int kUnitChunks = 4;  // 64-wide K chunks per ring slot (256 k)
 
 struct DecodeParams {
   const uint16_t *x;
-  const uint4 *codes;
-  const uint32_t *scales;  // [tile][gblock][g][4 groups] words of (row g | row g+8 << 16)
-  const uint32_t *zeros;   // [tile][gblock][g] words of 4 bytes (row g | row g+8 << 4)
+  const uint8_t *codes;    // [tile][chunk][lane][16 B]
+  const uint8_t *scales;   // [tile][gblock][g][4 groups][2 rows] bf16
+  const uint8_t *zeros;    // [tile][gblock][g][4 groups] bytes (row g | row g+8 << 4)
   uint16_t *y;
   int M, N, K;             // N: output columns (N_each for gate/up)
-  int tiles, chunks, groups, gblocks;
+  int tiles, chunks, groups, gblocks, units;
   int ld;                  // y row stride in elements
+  int *err;
+  UnpackConsts uc;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -50,12 +64,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// same product, accumulator starting from zero
+__device__ __forceinline__ void mma_bf16_16816_zero(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                    uint32_t b1) {
+  const float z = 0.f;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
 }
 
 __device__ __forceinline__ uint4 ldg_keep(const uint4 *p) {
@@ -63,12 +79,6 @@ __device__ __forceinline__ uint4 ldg_keep(const uint4 *p) {
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t ldg_u32(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
@@ -83,25 +93,107 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
 
-// Slice [g0, g1) of the K groups for this warp.
-__device__ __forceinline__ void k_slice(int groups, int &g0, int &g1) {
-  const int kw = blockDim.x >> 5;
-  const int nsl = gridDim.y * kw;
-  const int sidx = blockIdx.y * kw + (threadIdx.x >> 5);
-  g0 = (int)((long long)groups * sidx / nsl);
-  g1 = (int)((long long)groups * (sidx + 1) / nsl);
+// 1-D bulk copy global -> shared, completion counted on `bar`; the weights are
+// read once, so they are marked first to leave L2.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 
-// Sum the per-warp partials red[w][e] (w < KW) into red[0][e]; with a cluster,
-// rank 0 then adds every other rank's red[0][e] in rank order. Returns true in
-// the CTA that must write the outputs.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Slice [u0, u1) of the K units for this warp.
+__device__ __forceinline__ void k_slice(int units, int &u0, int &u1) {
+  const int nsl = gridDim.y * kWarps;
+  const int sidx = blockIdx.y * kWarps + (threadIdx.x >> 5);
+  u0 = (int)((long long)units * sidx / nsl);
+  u1 = (int)((long long)units * (sidx + 1) / nsl);
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp ring of K-unit slots filled by bulk copies.
+//   slot layout: codes [TPW][4 chunks][32 lanes][16 B], then the scale block
+//   of each tile [TPW][128 B], then (asymmetric) its zero block [TPW][32 B].
+//   A unit u covers chunks 4u .. 4u+3 (fewer in a ragged last unit) and lies
+//   inside scale block u (group 64) or u/2 (group 128).
+// ---------------------------------------------------------------------------
+template <int TPW, bool SYM, int SLOTS>
+struct Ring {
+  static constexpr int kTileCode = kUnitChunks * kChunkBytes;  // 2048
+  static constexpr int kScaleOff = TPW * kTileCode;
+  static constexpr int kZeroOff = kScaleOff + TPW * kScaleBlockBytes;
+  static constexpr int kSlotBytes = kZeroOff + (SYM ? 0 : TPW * kZeroBlockBytes);
+  static constexpr int kWarpBytes = SLOTS * kSlotBytes;
+
+  uint8_t *base;   // this warp's slots (generic address)
+  uint32_t sbase;  // same, shared-window address
+  uint32_t bar0;   // SLOTS mbarriers, 8 bytes apart
+  const uint8_t *codes[TPW];
+  const uint8_t *scales[TPW];
+  const uint8_t *zeros[TPW];
+  uint64_t policy;
+  int chunks, upb;  // chunks per tile, units per scale block (1 or 2)
+
+  __device__ void setup(const DecodeParams &p, uint8_t *warp_base, uint64_t *warp_bars, int tile0, int cpg) {
+    base = warp_base;
+    sbase = smem_u32(warp_base);
+    bar0 = smem_u32(warp_bars);
+    chunks = p.chunks;
+    upb = cpg;  // a block of four groups spans 4 * cpg chunks = cpg units
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+      const int tile = min(tile0 + i, p.tiles - 1);
+      codes[i] = p.codes + (size_t)tile * p.chunks * kChunkBytes;
+      scales[i] = p.scales + (size_t)tile * p.gblocks * kScaleBlockBytes;
+      zeros[i] = p.zeros + (size_t)tile * p.gblocks * kZeroBlockBytes;
+    }
+    policy = 0;
+    if ((threadIdx.x & 31) == 0) {
+      for (int s = 0; s < SLOTS; ++s) mbar_init(bar0 + 8 * s, 1);
+      fence_mbar_init();
+      policy = evict_first_policy();
+    }
+    __syncwarp();
+  }
+
+  // lane 0: copy unit u into slot s
+  __device__ void issue(int s, int u) {
+    const uint32_t bar = bar0 + 8 * s;
+    const uint32_t dst = sbase + s * kSlotBytes;
+    const int nch = min(kUnitChunks, chunks - kUnitChunks * u);
+    const int blk = u / upb;
+    mbar_arrive_expect_tx(bar, TPW * (nch * kChunkBytes + kScaleBlockBytes + (SYM ? 0 : kZeroBlockBytes)));
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+      bulk_copy(dst + i * kTileCode, codes[i] + (size_t)u * kTileCode, nch * kChunkBytes, bar, policy);
+      bulk_copy(dst + kScaleOff + i * kScaleBlockBytes, scales[i] + (size_t)blk * kScaleBlockBytes,
+                kScaleBlockBytes, bar, policy);
+      if (!SYM)
+        bulk_copy(dst + kZeroOff + i * kZeroBlockBytes, zeros[i] + (size_t)blk * kZeroBlockBytes, kZeroBlockBytes,
+                  bar, policy);
+    }
+  }
+
+  __device__ const uint8_t *slot(int s) const { return base + s * kSlotBytes; }
+};
+
+// Sum the per-warp partials red[w][e] into red[0][e]; with a cluster, rank 0
+// then adds every other rank's red[0][e] in rank order. Returns true in the
+// CTA that writes the outputs.
 template <int E>
 __device__ __forceinline__ bool reduce_partials(float (*red)[E]) {
-  const int kw = blockDim.x >> 5;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float s = red[0][e];
-    for (int w = 1; w < kw; ++w) s += red[w][e];
+    for (int w = 1; w < kWarps; ++w) s += red[w][e];
     red[0][e] = s;
   }
   if (gridDim.y == 1) {
@@ -133,39 +225,73 @@ __device__ __forceinline__ bool reduce_partials(float (*red)[E]) {
   return rank == 0;
 }
 
+// Dynamic shared memory of a decode CTA: rings, their barriers, the partials
+// and the abort flag.
+template <int TPW, bool SYM, int SLOTS, int E>
+struct DecodeSmem {
+  using R = Ring<TPW, SYM, SLOTS>;
+  static constexpr int kRingOff = 0;
+  static constexpr int kBarOff = kWarps * R::kWarpBytes;
+  static constexpr int kRedOff = kBarOff + kWarps * SLOTS * 8;
+  static constexpr int kFlagOff = kRedOff + kWarps * E * 4;
+  static constexpr int kBytes = kFlagOff + 16;
+};
+
+// Wait for the slot of the it-th unit. The outcome is made warp-uniform (a
+// lane that gave up makes the whole warp give up, so no lane is left behind at
+// a later __syncwarp); on giving up, raise the CTA abort flag.
+template <int SLOTS>
+__device__ __forceinline__ bool wait_slot(uint32_t bar0, int it, volatile int *abort_flag, int *err) {
+  const int s = it % SLOTS;
+  const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * s, (it / SLOTS) & 1, abort_flag));
+  if (!ok && (threadIdx.x & 31) == 0) {
+    *abort_flag = 1;
+    atomicExch(err, kErrTimeout);
+  }
+  return ok;
+}
+
+// After giving up: let the copies this warp issued land before the CTA exits.
+template <int SLOTS>
+__device__ __forceinline__ void drain_ring(uint32_t bar0, int first_unwaited, int issued) {
+  for (int it = first_unwaited; it < issued; ++it) mbar_wait_drain(bar0 + 8 * (it % SLOTS), (it / SLOTS) & 1);
+}
+
 // ---------------------------------------------------------------------------
 // small-M tensor-core kernel
 // ---------------------------------------------------------------------------
-template <int MT, int TPW, bool SYM, int CPG, int PF, bool GATEUP>
-__global__ void __launch_bounds__(256) smallm_mma_kernel(DecodeParams p) {
+template <int MT, int TPW, bool SYM, int CPG, int SLOTS, bool GATEUP>
+__global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p) {
   constexpr int E = TPW * MT * 4 * 32;
-  __shared__ float red[kMaxWarps][E];
+  constexpr int GPU = kUnitChunks / CPG;  // groups per full unit
+  using SM = DecodeSmem<TPW, SYM, SLOTS, E>;
+  using R = Ring<TPW, SYM, SLOTS>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float(*red)[E] = reinterpret_cast<float(*)[E]>(smem + SM::kRedOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kFlagOff);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int tile0 = blockIdx.x * TPW;
-  int gb, ge;
-  k_slice(p.groups, gb, ge);
+  if (threadIdx.x == 0) *abort_flag = 0;
+  __syncthreads();
+  int ub, ue;
+  k_slice(p.units, ub, ue);
+  const int nu = ue - ub;
 
-  const uint4 *wp[TPW];
-  const uint32_t *sp[TPW];
-  const uint32_t *zp[TPW];
-#pragma unroll
-  for (int i = 0; i < TPW; ++i) {
-    const int tile = min(tile0 + i, p.tiles - 1);
-    wp[i] = p.codes + (size_t)tile * p.chunks * 32 + lane;
-    sp[i] = p.scales + ((size_t)tile * p.gblocks * 8 + g) * 4;
-    zp[i] = p.zeros + ((size_t)tile * p.gblocks * 8 + g);
-  }
-  // x rows g and g + 8 (B fragment columns); rows >= M stay zero
+  R ring;
+  ring.setup(p, smem + SM::kRingOff + warp * R::kWarpBytes,
+             reinterpret_cast<uint64_t *>(smem + SM::kBarOff) + warp * SLOTS, tile0, CPG);
+  int issued = 0;
+  if (lane == 0)
+    for (; issued < SLOTS && issued < nu; ++issued) ring.issue(issued, ub + issued);
+
+  // B fragment column g + 8 mt reads x row min(g + 8 mt, M - 1): columns past M
+  // compute duplicates that are never stored
   const uint4 *xp[MT];
-  bool xv[MT];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const int m = g + 8 * mt;
-    xv[mt] = m < p.M;
-    xp[mt] = reinterpret_cast<const uint4 *>(p.x + (size_t)(xv[mt] ? m : 0) * p.K + 16 * t);
-  }
+  for (int mt = 0; mt < MT; ++mt)
+    xp[mt] = reinterpret_cast<const uint4 *>(p.x + (size_t)min(g + 8 * mt, p.M - 1) * p.K + 16 * t);
 
   float acc[TPW][MT][4];
 #pragma unroll
@@ -175,107 +301,70 @@ __global__ void __launch_bounds__(256) smallm_mma_kernel(DecodeParams p) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[i][mt][r] = 0.f;
 
-  // prefetch ring: weights, x fragments and scale / zero words of PF groups
-  uint4 rw[PF][CPG][TPW];
-  uint4 rx[PF][CPG][MT][2];
-  uint32_t rs[PF][TPW], rz[PF][TPW];
-
-  auto load_group = [&](int gg, uint4 (&w)[CPG][TPW], uint4 (&xx)[CPG][MT][2], uint32_t (&s)[TPW],
-                        uint32_t (&z)[TPW]) {
+  int it = 0;
+  for (; it < nu; ++it) {
+    const int u = ub + it;
+    const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);  // groups in this unit
+    if (!wait_slot<SLOTS>(ring.bar0, it, abort_flag, p.err)) break;
+    const uint8_t *sl = ring.slot(it % SLOTS);
 #pragma unroll
-    for (int cc = 0; cc < CPG; ++cc) {
-      const int c = gg * CPG + cc;
-#pragma unroll
-      for (int i = 0; i < TPW; ++i) w[cc][i] = ldg_stream(wp[i] + (size_t)c * 32);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        if (xv[mt]) {
-          xx[cc][mt][0] = ldg_keep(xp[mt] + (size_t)c * 8);
-          xx[cc][mt][1] = ldg_keep(xp[mt] + (size_t)c * 8 + 1);
-        } else {
-          xx[cc][mt][0] = make_uint4(0, 0, 0, 0);
-          xx[cc][mt][1] = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      s[i] = ldg_u32(sp[i] + (size_t)(gg >> 2) * 32 + (gg & 3));
-      z[i] = SYM ? 0u : ldg_u32(zp[i] + (size_t)(gg >> 2) * 8);
-    }
-  };
-
-#pragma unroll
-  for (int d = 0; d < PF; ++d)
-    if (gb + d < ge) load_group(gb + d, rw[d], rx[d], rs[d], rz[d]);
-
-  for (int gi = gb; gi < ge; gi += PF) {
-#pragma unroll
-    for (int d = 0; d < PF; ++d) {
-      const int gg = gi + d;
-      if (gg < ge) {
-        uint4 w[CPG][TPW];
-        uint4 xx[CPG][MT][2];
-        uint32_t s[TPW], z[TPW];
-#pragma unroll
-        for (int cc = 0; cc < CPG; ++cc) {
-#pragma unroll
-          for (int i = 0; i < TPW; ++i) w[cc][i] = rw[d][cc][i];
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            xx[cc][mt][0] = rx[d][cc][mt][0];
-            xx[cc][mt][1] = rx[d][cc][mt][1];
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < TPW; ++i) {
-          s[i] = rs[d][i];
-          z[i] = rz[d][i];
-        }
-        if (gg + PF < ge) load_group(gg + PF, rw[d], rx[d], rs[d], rz[d]);
-
+    for (int j = 0; j < GPU; ++j) {
+      if (j < ngu) {
+        const int gg = u * GPU + j;  // global group index
         uint32_t zg[TPW], zg8[TPW];
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
           if (SYM) {
             zg[i] = zg8[i] = zero_pair(8);
           } else {
-            const uint32_t zb = (z[i] >> (8 * (gg & 3))) & 0xFFu;
+            const uint32_t zb = sl[R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3)];
             zg[i] = zero_pair(zb & 0xF);
             zg8[i] = zero_pair(zb >> 4);
           }
         }
         float part[TPW][MT][4];
 #pragma unroll
-        for (int i = 0; i < TPW; ++i)
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) part[i][mt][r] = 0.f;
-#pragma unroll
         for (int cc = 0; cc < CPG; ++cc) {
+          const int cl = j * CPG + cc;  // chunk within the unit
+          const int c = kUnitChunks * u + cl;
+          uint4 xx[MT][2];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            xx[mt][0] = ldg_keep(xp[mt] + (size_t)c * 8);
+            xx[mt][1] = ldg_keep(xp[mt] + (size_t)c * 8 + 1);
+          }
+          uint4 w[TPW];
+#pragma unroll
+          for (int i = 0; i < TPW; ++i)
+            w[i] = *reinterpret_cast<const uint4 *>(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
 #pragma unroll
           for (int st = 0; st < 4; ++st) {
             // B fragment: x words 2st (k+0, k+1) and 2st+1 (k+2, k+3) of this lane's 16 k
             uint32_t b0[MT], b1[MT];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              const uint4 &xh = xx[cc][mt][st >> 1];
-              b0[mt] = word_of(xh, 2 * (st & 1));
-              b1[mt] = word_of(xh, 2 * (st & 1) + 1);
+              b0[mt] = word_of(xx[mt][st >> 1], 2 * (st & 1));
+              b1[mt] = word_of(xx[mt][st >> 1], 2 * (st & 1) + 1);
             }
 #pragma unroll
             for (int i = 0; i < TPW; ++i) {
               uint32_t a[4];
-              unpack_word(word_of(w[cc][i], st), zg[i], zg8[i], a);
+              unpack_word(word_of(w[i], st), zg[i], zg8[i], p.uc, a);
 #pragma unroll
-              for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(part[i][mt], a, b0[mt], b1[mt]);
+              for (int mt = 0; mt < MT; ++mt) {
+                if (cc == 0 && st == 0)
+                  mma_bf16_16816_zero(part[i][mt], a, b0[mt], b1[mt]);
+                else
+                  mma_bf16_16816(part[i][mt], a, b0[mt], b1[mt]);
+              }
             }
           }
         }
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
-          const float sg = bf16lo_to_f32(s[i]), sg8 = bf16hi_to_f32(s[i]);
+          const uint32_t sw =
+              *reinterpret_cast<const uint32_t *>(sl + R::kScaleOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
+          const float sg = bf16lo_to_f32(sw), sg8 = bf16hi_to_f32(sw);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             acc[i][mt][0] = fmaf(sg, part[i][mt][0], acc[i][mt][0]);
@@ -286,7 +375,15 @@ __global__ void __launch_bounds__(256) smallm_mma_kernel(DecodeParams p) {
         }
       }
     }
+    // every lane has consumed the slot: refill it with the unit SLOTS ahead
+    __syncwarp();
+    if (lane == 0 && issued < nu) {
+      fence_proxy_async_smem();
+      ring.issue(it % SLOTS, ub + issued);
+      ++issued;
+    }
   }
+  if (it < nu && lane == 0) drain_ring<SLOTS>(ring.bar0, it, issued);
 
 #pragma unroll
   for (int i = 0; i < TPW; ++i)
@@ -299,15 +396,16 @@ __global__ void __launch_bounds__(256) smallm_mma_kernel(DecodeParams p) {
 
   // element e = ((i*MT + mt)*4 + r)*32 + lane:
   //   row n = 16*(tile0+i) + g + 8*(r>>1), column m = 8*mt + 2t + (r&1)
-  constexpr int EO = GATEUP ? E / 2 : E;  // gate/up: tile 0 gate, tile 1 up
-  for (int e = threadIdx.x; e < EO; e += blockDim.x) {
+  // gate/up: tiles alternate gate, up; the pair (i, i+1) gives 16 outputs
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int ln = e & 31, r = (e >> 5) & 3, im = e >> 7;
     const int mt = im % MT, i = im / MT;
     const int m = 8 * mt + 2 * (ln & 3) + (r & 1);
     const int nl = (ln >> 2) + 8 * (r >> 1);
     if (m >= p.M) continue;
     if (GATEUP) {
-      const int n = 16 * (tile0 >> 1) + nl;
+      if (i & 1) continue;
+      const int n = 16 * ((tile0 + i) >> 1) + nl;
       if (n < p.N) {
         const float gv = red[0][e], uv = red[0][e + MT * 4 * 32];
         p.y[(size_t)m * p.ld + n] = f32_to_bf16_bits(silu_f32(gv) * uv);
@@ -322,141 +420,127 @@ __global__ void __launch_bounds__(256) smallm_mma_kernel(DecodeParams p) {
 // ---------------------------------------------------------------------------
 // one-row CUDA-core GEMV
 // ---------------------------------------------------------------------------
-template <int TPW, bool SYM, int CPG, int PF>
-__global__ void __launch_bounds__(256) gemv_m1_kernel(DecodeParams p) {
+template <int TPW, bool SYM, int CPG, int SLOTS>
+__global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
   constexpr int E = TPW * 2 * 8;  // (tile, row half, g)
-  __shared__ float red[kMaxWarps][E];
+  constexpr int GPU = kUnitChunks / CPG;
+  using SM = DecodeSmem<TPW, SYM, SLOTS, E>;
+  using R = Ring<TPW, SYM, SLOTS>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float(*red)[E] = reinterpret_cast<float(*)[E]>(smem + SM::kRedOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kFlagOff);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int tile0 = blockIdx.x * TPW;
-  int gb, ge;
-  k_slice(p.groups, gb, ge);
+  if (threadIdx.x == 0) *abort_flag = 0;
+  __syncthreads();
+  int ub, ue;
+  k_slice(p.units, ub, ue);
+  const int nu = ue - ub;
 
-  const uint4 *wp[TPW];
-  const uint32_t *sp[TPW];
-  const uint32_t *zp[TPW];
-#pragma unroll
-  for (int i = 0; i < TPW; ++i) {
-    const int tile = min(tile0 + i, p.tiles - 1);
-    wp[i] = p.codes + (size_t)tile * p.chunks * 32 + lane;
-    sp[i] = p.scales + ((size_t)tile * p.gblocks * 8 + g) * 4;
-    zp[i] = p.zeros + ((size_t)tile * p.gblocks * 8 + g);
-  }
+  R ring;
+  ring.setup(p, smem + SM::kRingOff + warp * R::kWarpBytes,
+             reinterpret_cast<uint64_t *>(smem + SM::kBarOff) + warp * SLOTS, tile0, CPG);
+  int issued = 0;
+  if (lane == 0)
+    for (; issued < SLOTS && issued < nu; ++issued) ring.issue(issued, ub + issued);
   const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + 16 * t);
 
   float out[TPW][2];
 #pragma unroll
   for (int i = 0; i < TPW; ++i) out[i][0] = out[i][1] = 0.f;
 
-  uint4 rw[PF][CPG][TPW];
-  uint4 rx[PF][CPG][2];
-  uint32_t rs[PF][TPW], rz[PF][TPW];
-  auto load_group = [&](int gg, uint4 (&w)[CPG][TPW], uint4 (&xx)[CPG][2], uint32_t (&s)[TPW],
-                        uint32_t (&z)[TPW]) {
+  // the float32 magic 2^23 (mantissa step 1) and the nibble masks live in
+  // registers so each "nibble | magic" is one LOP3
+  const uint32_t magic = p.uc.magic ^ 0x43004300u ^ 0x4B000000u;
+  const uint32_t m0 = p.uc.mask & 0xFu, m1 = m0 << 4, m2 = m0 << 8, m3 = m0 << 12, m4 = m0 << 16;
+  constexpr uint32_t kMagic = 0x4B000000u, kNeg = 0x80000000u;
+  int it = 0;
+  for (; it < nu; ++it) {
+    const int u = ub + it;
+    const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);
+    if (!wait_slot<SLOTS>(ring.bar0, it, abort_flag, p.err)) break;
+    const uint8_t *sl = ring.slot(it % SLOTS);
 #pragma unroll
-    for (int cc = 0; cc < CPG; ++cc) {
-      const int c = gg * CPG + cc;
-#pragma unroll
-      for (int i = 0; i < TPW; ++i) w[cc][i] = ldg_stream(wp[i] + (size_t)c * 32);
-      xx[cc][0] = ldg_keep(xp + (size_t)c * 8);
-      xx[cc][1] = ldg_keep(xp + (size_t)c * 8 + 1);
-    }
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      s[i] = ldg_u32(sp[i] + (size_t)(gg >> 2) * 32 + (gg & 3));
-      z[i] = SYM ? 0u : ldg_u32(zp[i] + (size_t)(gg >> 2) * 8);
-    }
-  };
-#pragma unroll
-  for (int d = 0; d < PF; ++d)
-    if (gb + d < ge) load_group(gb + d, rw[d], rx[d], rs[d], rz[d]);
-
-  constexpr uint32_t kMagic = 0x4B000000u;  // float32 2^23: mantissa step 1
-  for (int gi = gb; gi < ge; gi += PF) {
-#pragma unroll
-    for (int d = 0; d < PF; ++d) {
-      const int gg = gi + d;
-      if (gg < ge) {
-        uint4 w[CPG][TPW];
+    for (int j = 0; j < GPU; ++j) {
+      if (j < ngu) {
+        const int gg = u * GPU + j;
         uint4 xx[CPG][2];
-        uint32_t s[TPW], z[TPW];
 #pragma unroll
         for (int cc = 0; cc < CPG; ++cc) {
-#pragma unroll
-          for (int i = 0; i < TPW; ++i) w[cc][i] = rw[d][cc][i];
-          xx[cc][0] = rx[d][cc][0];
-          xx[cc][1] = rx[d][cc][1];
+          const int c = kUnitChunks * u + j * CPG + cc;
+          xx[cc][0] = ldg_keep(xp + (size_t)c * 8);
+          xx[cc][1] = ldg_keep(xp + (size_t)c * 8 + 1);
         }
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
-          s[i] = rs[d][i];
-          z[i] = rz[d][i];
-        }
-        if (gg + PF < ge) load_group(gg + PF, rw[d], rx[d], rs[d], rz[d]);
-
-        // nibble j of a word: row g + 8*(j&1), class p(j) (its place 16^p), k offset kofs(j)
-        //   j : 0 1 2 3 4 5 6 7
-        //   p : 0 1 2 3 4 0 1 2      (j = 5..7 are read from the word shifted right by 20)
-        // -(2^23 + z * 16^p(j)) is added exactly (both operands are integers below 2^24).
-        float2 cz[4];
-        float2 part[TPW][4];  // pairs (j=0,1) (2,3) (4,5) (6,7)
-#pragma unroll
-        for (int i = 0; i < TPW; ++i)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) part[i][q] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < TPW; ++i) {
+          const uint32_t sw =
+              *reinterpret_cast<const uint32_t *>(sl + R::kScaleOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
           uint32_t za = 8, zb = 8;
           if (!SYM) {
-            const uint32_t zbyte = (z[i] >> (8 * (gg & 3))) & 0xFFu;
+            const uint32_t zbyte = sl[R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3)];
             za = zbyte & 0xF;
             zb = zbyte >> 4;
           }
-          constexpr uint32_t kNeg = 0x80000000u;
-          cz[0] = make_float2(__uint_as_float(kNeg | kMagic | za), __uint_as_float(kNeg | kMagic | (zb << 4)));
-          cz[1] = make_float2(__uint_as_float(kNeg | kMagic | (za << 8)),
-                              __uint_as_float(kNeg | kMagic | (zb << 12)));
-          cz[2] = make_float2(__uint_as_float(kNeg | kMagic | (za << 16)), __uint_as_float(kNeg | kMagic | zb));
-          cz[3] = make_float2(__uint_as_float(kNeg | kMagic | (za << 4)),
-                              __uint_as_float(kNeg | kMagic | (zb << 8)));
+          // nibble j of a word: row g + 8*(j&1), place 16^p(j), k offset kofs(j)
+          //   j : 0 1 2 3 4 5 6 7
+          //   p : 0 1 2 3 4 0 1 2      (j = 5..7 are read from the word shifted right by 20)
+          // -(2^23 + z * 16^p(j)) is added exactly (both operands are integers below 2^24).
+          const float2 cz0 = make_float2(__uint_as_float(kNeg | kMagic | za), __uint_as_float(kNeg | kMagic | (zb << 4)));
+          const float2 cz1 =
+              make_float2(__uint_as_float(kNeg | kMagic | (za << 8)), __uint_as_float(kNeg | kMagic | (zb << 12)));
+          const float2 cz2 =
+              make_float2(__uint_as_float(kNeg | kMagic | (za << 16)), __uint_as_float(kNeg | kMagic | zb));
+          const float2 cz3 =
+              make_float2(__uint_as_float(kNeg | kMagic | (za << 4)), __uint_as_float(kNeg | kMagic | (zb << 8)));
+          float2 part[4];  // pairs (j=0,1) (2,3) (4,5) (6,7)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) part[q] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int cc = 0; cc < CPG; ++cc) {
+            const int cl = j * CPG + cc;
+            const uint4 wv = *reinterpret_cast<const uint4 *>(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
 #pragma unroll
             for (int st = 0; st < 4; ++st) {
-              const uint32_t wd = word_of(w[cc][i], st);
+              const uint32_t wd = word_of(wv, st);
               const uint32_t w20 = wd >> 20;
               const uint32_t xa = word_of(xx[cc][st >> 1], 2 * (st & 1));      // k+0, k+1
               const uint32_t xb = word_of(xx[cc][st >> 1], 2 * (st & 1) + 1);  // k+2, k+3
               const float x0 = bf16lo_to_f32(xa), x1 = bf16hi_to_f32(xa);
               const float x2 = bf16lo_to_f32(xb), x3 = bf16hi_to_f32(xb);
-              const float2 v01 = make_float2(__uint_as_float(kMagic | (wd & 0xFu)),
-                                             __uint_as_float(kMagic | (wd & 0xF0u)));
-              const float2 v23 = make_float2(__uint_as_float(kMagic | (wd & 0xF00u)),
-                                             __uint_as_float(kMagic | (wd & 0xF000u)));
-              const float2 v45 = make_float2(__uint_as_float(kMagic | (wd & 0xF0000u)),
-                                             __uint_as_float(kMagic | (w20 & 0xFu)));
-              const float2 v67 = make_float2(__uint_as_float(kMagic | (w20 & 0xF0u)),
-                                             __uint_as_float(kMagic | (w20 & 0xF00u)));
+              const float2 v01 = make_float2(__uint_as_float(lop3_and_or(wd, m0, magic)),
+                                             __uint_as_float(lop3_and_or(wd, m1, magic)));
+              const float2 v23 = make_float2(__uint_as_float(lop3_and_or(wd, m2, magic)),
+                                             __uint_as_float(lop3_and_or(wd, m3, magic)));
+              const float2 v45 = make_float2(__uint_as_float(lop3_and_or(wd, m4, magic)),
+                                             __uint_as_float(lop3_and_or(w20, m0, magic)));
+              const float2 v67 = make_float2(__uint_as_float(lop3_and_or(w20, m1, magic)),
+                                             __uint_as_float(lop3_and_or(w20, m2, magic)));
               // j=0,1 at k+0; j=2,3 at k+2; j=4,5 at k+1; j=6,7 at k+3
-              part[i][0] = __ffma2_rn(make_float2(x0, x0), __fadd2_rn(v01, cz[0]), part[i][0]);
-              part[i][1] = __ffma2_rn(make_float2(x2, x2), __fadd2_rn(v23, cz[1]), part[i][1]);
-              part[i][2] = __ffma2_rn(make_float2(x1, x1), __fadd2_rn(v45, cz[2]), part[i][2]);
-              part[i][3] = __ffma2_rn(make_float2(x3, x3), __fadd2_rn(v67, cz[3]), part[i][3]);
+              part[0] = __ffma2_rn(make_float2(x0, x0), __fadd2_rn(v01, cz0), part[0]);
+              part[1] = __ffma2_rn(make_float2(x2, x2), __fadd2_rn(v23, cz1), part[1]);
+              part[2] = __ffma2_rn(make_float2(x1, x1), __fadd2_rn(v45, cz2), part[2]);
+              part[3] = __ffma2_rn(make_float2(x3, x3), __fadd2_rn(v67, cz3), part[3]);
             }
           }
           // undo the 16^p places: row g gets j = 0, 2, 4, 6 (p = 0, 2, 4, 1),
           // row g + 8 gets j = 1, 3, 5, 7 (p = 1, 3, 0, 2)
-          const float rg = part[i][0].x + part[i][1].x * 0x1p-8f + part[i][2].x * 0x1p-16f +
-                           part[i][3].x * 0x1p-4f;
-          const float rg8 = part[i][0].y * 0x1p-4f + part[i][1].y * 0x1p-12f + part[i][2].y +
-                            part[i][3].y * 0x1p-8f;
-          out[i][0] = fmaf(bf16lo_to_f32(s[i]), rg, out[i][0]);
-          out[i][1] = fmaf(bf16hi_to_f32(s[i]), rg8, out[i][1]);
+          const float rg = part[0].x + part[1].x * 0x1p-8f + part[2].x * 0x1p-16f + part[3].x * 0x1p-4f;
+          const float rg8 = part[0].y * 0x1p-4f + part[1].y * 0x1p-12f + part[2].y + part[3].y * 0x1p-8f;
+          out[i][0] = fmaf(bf16lo_to_f32(sw), rg, out[i][0]);
+          out[i][1] = fmaf(bf16hi_to_f32(sw), rg8, out[i][1]);
         }
       }
     }
+    __syncwarp();
+    if (lane == 0 && issued < nu) {
+      fence_proxy_async_smem();
+      ring.issue(it % SLOTS, ub + issued);
+      ++issued;
+    }
   }
+  if (it < nu && lane == 0) drain_ring<SLOTS>(ring.bar0, it, issued);
 
   // the four lanes t = 0..3 of each g hold disjoint k of the same two rows
 #pragma unroll
@@ -486,29 +570,35 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(DecodeParams p) {
 // launch configuration
 // ---------------------------------------------------------------------------
 struct DecodeCfg {
-  int tpw, kw, kc;
+  int tpw, kc, smem;
 };
 
-DecodeCfg pick_cfg(int tiles, int groups, int sm_count, int tpw) {
-  DecodeCfg c;
+// Split-K choice: the largest cluster split (<= 8) that still lets every CTA
+// of the grid be resident at once (one wave), with at least one K unit per
+// warp; grids that already fill the GPU stay unsplit.
+template <typename Kern>
+cudaError_t pick_cfg(Kern kern, int smem, int tiles, int units, int sm_count, int tpw, DecodeCfg &c) {
   c.tpw = tpw;
-  c.kw = 4;
+  c.smem = smem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   const int ctas = (tiles + tpw - 1) / tpw;
-  // aim for about 16 resident warps per SM so enough 16-byte loads are in flight
-  const long long target = (long long)sm_count * 16;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * kWarps, smem) != cudaSuccess || occ < 1)
+    occ = 1;
+  const long long resident = (long long)occ * sm_count;
   c.kc = 1;
-  while (c.kc < 8 && (long long)ctas * c.kw * c.kc < target && groups >= 4 * c.kw * c.kc) c.kc *= 2;
-  return c;
+  while (c.kc < 8 && (long long)ctas * c.kc * 2 <= resident && units >= kWarps * c.kc * 2) c.kc *= 2;
+  return cudaSuccess;
 }
 
 template <typename Kern>
-cudaError_t launch_decode(Kern kern, const DecodeParams &prm, const DecodeCfg &cfg,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(Kern kern, const DecodeParams &prm, const DecodeCfg &cfg, cudaStream_t stream) {
   const int ctas = (prm.tiles + cfg.tpw - 1) / cfg.tpw;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(ctas, cfg.kc, 1);
-  lc.blockDim = dim3(32 * cfg.kw, 1, 1);
-  lc.dynamicSmemBytes = 0;
+  lc.blockDim = dim3(32 * kWarps, 1, 1);
+  lc.dynamicSmemBytes = cfg.smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
   int na = 0;
@@ -527,9 +617,9 @@ cudaError_t launch_decode(Kern kern, const DecodeParams &prm, const DecodeCfg &c
 DecodeParams make_params(const GemmCall &c, const Layout &L) {
   DecodeParams p;
   p.x = c.x;
-  p.codes = reinterpret_cast<const uint4 *>(c.packed + L.codes_off);
-  p.scales = reinterpret_cast<const uint32_t *>(c.packed + L.scales_off);
-  p.zeros = reinterpret_cast<const uint32_t *>(c.packed + (c.sym ? L.scales_off : L.zeros_off));
+  p.codes = c.packed + L.codes_off;
+  p.scales = c.packed + L.scales_off;
+  p.zeros = c.packed + (c.sym ? L.scales_off : L.zeros_off);
   p.y = c.y;
   p.M = c.M;
   p.N = c.N;
@@ -538,28 +628,50 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
   p.chunks = L.chunks;
   p.groups = L.groups;
   p.gblocks = L.gblocks;
+  p.units = (L.chunks + kUnitChunks - 1) / kUnitChunks;
   p.ld = c.N;
+  p.err = c.err;
+  p.uc = host_unpack_consts();
   return p;
 }
 
-template <int MT, bool SYM, int CPG, bool GATEUP>
-cudaError_t run_mma(const DecodeParams &p, const DecodeCfg &cfg, cudaStream_t s) {
-  constexpr int PF = (MT == 1 ? 4 : 2) / CPG;
-  return launch_decode(smallm_mma_kernel<MT, 2, SYM, CPG, PF, GATEUP>, p, cfg, s);
+constexpr int slots_for(int tpw) { return tpw >= 4 ? 2 : 3; }
+
+template <int MT, int TPW, bool SYM, int CPG, bool GATEUP>
+cudaError_t run_mma(const DecodeParams &p, int sm_count, cudaStream_t s) {
+  constexpr int SLOTS = slots_for(TPW);
+  auto kern = smallm_mma_kernel<MT, TPW, SYM, CPG, SLOTS, GATEUP>;
+  DecodeCfg cfg;
+  cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * MT * 4 * 32>::kBytes, p.tiles, p.units,
+                           sm_count, TPW, cfg);
+  return e != cudaSuccess ? e : launch_decode(kern, p, cfg, s);
 }
 
+// Tiles per warp: four when the grid still fills the GPU several times over
+// (fewer per-slot overheads per packed word), else two.
 template <bool SYM, int CPG, bool GATEUP>
-cudaError_t run_mma_m(const DecodeParams &p, const DecodeCfg &cfg, cudaStream_t s) {
-  return p.M <= 8 ? run_mma<1, SYM, CPG, GATEUP>(p, cfg, s) : run_mma<2, SYM, CPG, GATEUP>(p, cfg, s);
+cudaError_t run_mma_m(const DecodeParams &p, int sm_count, cudaStream_t s) {
+  const bool wide = p.tiles >= 4 * 8 * sm_count;
+  if (p.M <= 8)
+    return wide ? run_mma<1, 4, SYM, CPG, GATEUP>(p, sm_count, s) : run_mma<1, 2, SYM, CPG, GATEUP>(p, sm_count, s);
+  return run_mma<2, 2, SYM, CPG, GATEUP>(p, sm_count, s);
 }
 
 template <bool GATEUP>
-cudaError_t run_mma_all(const DecodeParams &p, const DecodeCfg &cfg, int sym, int group,
-                        cudaStream_t s) {
-  if (sym) {
-    return group == 64 ? run_mma_m<true, 1, GATEUP>(p, cfg, s) : run_mma_m<true, 2, GATEUP>(p, cfg, s);
-  }
-  return group == 64 ? run_mma_m<false, 1, GATEUP>(p, cfg, s) : run_mma_m<false, 2, GATEUP>(p, cfg, s);
+cudaError_t run_mma_all(const DecodeParams &p, int sm_count, int sym, int group, cudaStream_t s) {
+  if (sym)
+    return group == 64 ? run_mma_m<true, 1, GATEUP>(p, sm_count, s) : run_mma_m<true, 2, GATEUP>(p, sm_count, s);
+  return group == 64 ? run_mma_m<false, 1, GATEUP>(p, sm_count, s) : run_mma_m<false, 2, GATEUP>(p, sm_count, s);
+}
+
+template <bool SYM, int CPG>
+cudaError_t run_gemv(const DecodeParams &p, int sm_count, cudaStream_t s) {
+  constexpr int TPW = 2, SLOTS = slots_for(TPW);
+  auto kern = gemv_m1_kernel<TPW, SYM, CPG, SLOTS>;
+  DecodeCfg cfg;
+  cudaError_t e =
+      pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * 16>::kBytes, p.tiles, p.units, sm_count, TPW, cfg);
+  return e != cudaSuccess ? e : launch_decode(kern, p, cfg, s);
 }
 
 }  // namespace
@@ -567,21 +679,15 @@ cudaError_t run_mma_all(const DecodeParams &p, const DecodeCfg &cfg, int sym, in
 cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(packed_rows(c), c.K, c.group, c.sym);
   DecodeParams p = make_params(c, L);
-  const DecodeCfg cfg = pick_cfg(L.tiles, L.groups, sm_count, 2);
-  if (c.gateup) return run_mma_all<true>(p, cfg, c.sym, c.group, c.stream);
-  return run_mma_all<false>(p, cfg, c.sym, c.group, c.stream);
+  if (c.gateup) return run_mma_all<true>(p, sm_count, c.sym, c.group, c.stream);
+  return run_mma_all<false>(p, sm_count, c.sym, c.group, c.stream);
 }
 
 cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(packed_rows(c), c.K, c.group, c.sym);
   DecodeParams p = make_params(c, L);
-  const DecodeCfg cfg = pick_cfg(L.tiles, L.groups, sm_count, 2);
-  if (c.sym) {
-    return c.group == 64 ? launch_decode(gemv_m1_kernel<2, true, 1, 4>, p, cfg, c.stream)
-                         : launch_decode(gemv_m1_kernel<2, true, 2, 2>, p, cfg, c.stream);
-  }
-  return c.group == 64 ? launch_decode(gemv_m1_kernel<2, false, 1, 4>, p, cfg, c.stream)
-                       : launch_decode(gemv_m1_kernel<2, false, 2, 2>, p, cfg, c.stream);
+  if (c.sym) return c.group == 64 ? run_gemv<true, 1>(p, sm_count, c.stream) : run_gemv<true, 2>(p, sm_count, c.stream);
+  return c.group == 64 ? run_gemv<false, 1>(p, sm_count, c.stream) : run_gemv<false, 2>(p, sm_count, c.stream);
 }
 
 }  // namespace w4a16

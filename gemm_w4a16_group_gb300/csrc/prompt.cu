@@ -74,6 +74,7 @@ struct PromptParams {
   int ng;          // K / group
   int spg;         // 64-wide stages per group (1 or 2)
   int *err;
+  UnpackConsts uc;
 };
 
 struct Bars {
@@ -279,10 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint4 q = *reinterpret_cast<const uint4 *>(qs + (i * 32 + lane) * 16);
           uint32_t u[4][4];
-          unpack_word(q.x, zg, zg8, u[0]);
-          unpack_word(q.y, zg, zg8, u[1]);
-          unpack_word(q.z, zg, zg8, u[2]);
-          unpack_word(q.w, zg, zg8, u[3]);
+          unpack_word(q.x, zg, zg8, p.uc, u[0]);
+          unpack_word(q.y, zg, zg8, p.uc, u[1]);
+          unpack_word(q.z, zg, zg8, p.uc, u[2]);
+          unpack_word(q.w, zg, zg8, p.uc, u[3]);
           // row 16i+g holds k = 16t + 4s + {0,1} in u[s][0] and {2,3} in u[s][2];
           // row 16i+g+8 likewise in u[s][1], u[s][3]
 #pragma unroll
@@ -490,6 +491,7 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   p.ng = c.K / c.group;
   p.spg = c.group / BK;
   p.err = c.err;
+  p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;
   const int grid = ntot < sm_count ? ntot : sm_count;
   if (c.sym) {

@@ -108,7 +108,7 @@ __global__ void repack_zeros_kernel(RepackSrc s, Layout L, uint8_t *out) {
 }
 
 // w[n][k] = (q - z) * scale through the same unpack as the GEMM kernels
-__global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float *w) {
+__global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float *w, UnpackConsts uc) {
   const size_t total = (size_t)L.tiles * L.chunks * 32;
   const uint4 *codes = reinterpret_cast<const uint4 *>(packed + L.codes_off);
   const uint32_t *scales = reinterpret_cast<const uint32_t *>(packed + L.scales_off);
@@ -138,7 +138,7 @@ __global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float 
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       uint32_t u[4];
-      unpack_word(words[s], zg, zg8, u);
+      unpack_word(words[s], zg, zg8, uc, u);
       const int k = 64 * c + 16 * t + 4 * s;
       // u[0]: row g, k+0 / k+1; u[1]: row g+8, k+0 / k+1; u[2]: row g, k+2 / k+3; u[3]: row g+8
       if (n0 < N) {
@@ -198,7 +198,7 @@ cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, flo
                               cudaStream_t stream) {
   const int th = 256;
   size_t n = (size_t)L.tiles * L.chunks * 32;
-  dequantize_kernel<<<grid_for(n, th), th, 0, stream>>>(packed, L, N, w);
+  dequantize_kernel<<<grid_for(n, th), th, 0, stream>>>(packed, L, N, w, host_unpack_consts());
   return cudaGetLastError();
 }
 

@@ -81,14 +81,41 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// Four bf16x2 registers of (q - z) from one packed word: out[p] holds nibble p
-// (low half) and nibble p + 4 (high half); out[0], out[2] are row g and use
-// zg = zero_pair(z of row g), out[1], out[3] are row g + 8 and use zg8.
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t zg, uint32_t zg8, uint32_t out[4]) {
-  out[0] = bf16x2_sub((w & kNibMask) | kBf16x2_128, zg);
-  out[1] = bf16x2_sub(((w >> 4) & kNibMask) | kBf16x2_128, zg8);
-  out[2] = bf16x2_sub(((w >> 8) & kNibMask) | kBf16x2_128, zg);
-  out[3] = bf16x2_sub(((w >> 12) & kNibMask) | kBf16x2_128, zg8);
+// (w & mask) | magic as ONE three-input LOP3. With both constants as
+// immediates the compiler splits it into two logic ops, and the integer ALU
+// pipe is what bounds the unpack rate, so the constants travel in registers
+// (UnpackConsts comes in as a kernel argument and is not constant-folded).
+struct UnpackConsts {
+  uint32_t mask;   // kNibMask
+  uint32_t magic;  // kBf16x2_128
+};
+inline UnpackConsts host_unpack_consts() { return UnpackConsts{kNibMask, kBf16x2_128}; }
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t w, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(w), "r"(mask), "r"(magic));  // (a & b) | c
+  return d;
+}
+
+// Four bf16x2 registers of 128 + q from one packed word: out[p] holds nibble
+// p (low half) and nibble p + 4 (high half); out[0], out[2] are row g,
+// out[1], out[3] row g + 8. Three shifts and four LOP3s, all exact.
+__device__ __forceinline__ void unpack_word_biased(uint32_t w, const UnpackConsts &uc, uint32_t out[4]) {
+  out[0] = lop3_and_or(w, uc.mask, uc.magic);
+  out[1] = lop3_and_or(w >> 4, uc.mask, uc.magic);
+  out[2] = lop3_and_or(w >> 8, uc.mask, uc.magic);
+  out[3] = lop3_and_or(w >> 12, uc.mask, uc.magic);
+}
+
+// Same registers holding q - z exactly: zg = zero_pair(z of row g) is
+// subtracted from out[0], out[2] and zg8 (row g + 8) from out[1], out[3].
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t zg, uint32_t zg8, const UnpackConsts &uc,
+                                            uint32_t out[4]) {
+  unpack_word_biased(w, uc, out);
+  out[0] = bf16x2_sub(out[0], zg);
+  out[1] = bf16x2_sub(out[1], zg8);
+  out[2] = bf16x2_sub(out[2], zg);
+  out[3] = bf16x2_sub(out[3], zg8);
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }

@@ -135,12 +135,11 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false,
              reinterpret_cast<cudaStream_t>(stream), d.err};
+  // M <= 16: the tensor-core decode kernel (measured faster than the CUDA-core
+  // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
   const int ov = g_override.load();
   if (M == 1 && ov == 1) return finish_launch(launch_gemv_m1(c, d.sm_count));
-  if (M <= 16 && ov != 3) {
-    if (M == 1 && ov == 0) return finish_launch(launch_gemv_m1(c, d.sm_count));
-    return finish_launch(launch_smallm_mma(c, d.sm_count));
-  }
+  if (M <= 16 && ov != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 

@@ -9,18 +9,24 @@
 // MMA, as the TensorFold PR #859 prompt GEMM does ("each weight rounded once to
 // bf16"), would cost up to 2^-9 per weight; this split keeps every weight
 // exact. The feed-forward gate is fused as in the GRIMOIRE v1.8 release notes
-// ("INT4 prompt processing"): the CTA's 256 columns are 128 gate rows and the
-// 128 matching up rows, so h = SiLU(g) * u is formed from the two float32
-// accumulators before a single bf16 rounding.
+// ("INT4 prompt processing"): the CTA's 128 weight rows are 64 gate rows and
+// the 64 matching up rows (16-row tiles alternate), so h = SiLU(g) * u is
+// formed from two float32 accumulators of the same thread before a single
+// bf16 rounding.
+//
+// A CTA tile is 256 rows of x by 128 weight rows: two M = 128 MMAs per K step
+// share one dequantised B tile, which halves the dequantisation work (the
+// pacing role) per multiply-add against a 128 x 256 tile.
 //
 // One persistent CTA per SM, 512 threads, warp-specialised:
-//   warp 0       TMA producer: x tile [128 x 64] (128-byte swizzle), packed codes of
-//                256 rows x 64 k, and per four groups the scale (+ zero) block
+//   warp 0       TMA producer: x tile [256 x 64] (128-byte swizzle), packed codes of
+//                128 rows x 64 k, and per four groups the scale (+ zero) block
 //   warp 1       TMEM allocator and the single MMA-issuing thread:
-//                D[b] (+)= A . B^T, M = 128, N = 256, K = 16, b = group parity
+//                D[b][h] (+)= A[h] . B^T, M = 128, N = 128, K = 16, h = x-row half,
+//                b = group parity
 //   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
 //                128-byte-swizzled K-major B tile; scale block -> float32
-//   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b];
+//   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b][h];
 //                per tile, the bf16 store (or SiLU(gate) * up)
 // Every wait is bounded; a wait that gives up sets the device error word and
 // every role leaves its loop, drains what it started and exits.
@@ -32,17 +38,19 @@
 namespace w4a16 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 256, BN = 128, BK = 64;
+constexpr int UM = 128;      // rows of one MMA (one x-row half)
+constexpr int NT16 = BN / 16;  // 16-row weight tiles per CTA tile
 constexpr int SL = 4;  // x + codes ring
-constexpr int SB = 3;  // dequantised B ring
+constexpr int SB = 4;  // dequantised B ring
 constexpr int SS = 2;  // scale-block ring (4 groups each)
 constexpr int kThreads = 512;
 
-constexpr int A_BYTES = BM * BK * 2;   // 16384
-constexpr int B_BYTES = BN * BK * 2;   // 32768
-constexpr int Q_BYTES = BN * BK / 2;   // 8192
-constexpr int RS_BYTES = 16 * kScaleBlockBytes;  // 2048
-constexpr int RZ_BYTES = 16 * kZeroBlockBytes;   // 512
+constexpr int A_BYTES = BM * BK * 2;   // 32768: x rows 0-127 then 128-255
+constexpr int B_BYTES = BN * BK * 2;   // 16384
+constexpr int Q_BYTES = BN * BK / 2;   // 4096
+constexpr int RS_BYTES = NT16 * kScaleBlockBytes;  // 1024
+constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256
 constexpr int SC_FLOATS = 4 * BN;                // float32 scales of one block
 
 constexpr int OFF_A = 0;
@@ -62,8 +70,8 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(OFF_B % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
-constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+constexpr uint32_t kIdesc = idesc_bf16_f32(UM, BN);
+constexpr uint32_t kTmemCols = 512;  // two buffers x two x-row halves x 128 fp32 columns
 
 struct PromptParams {
   uint16_t *y;
@@ -170,16 +178,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : RZ_BYTES));
             const int blk = kb / (4 * p.spg);
-            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, nt * 16, bars.full_S(slot));
+            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, nt * NT16, bars.full_S(slot));
             if (!SYM)
-              tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, nt * 16, bars.full_S(slot));
+              tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, nt * NT16, bars.full_S(slot));
             ++sc;
           }
           const int slot = ls % SL;
           if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(bars.full_L(slot), A_BYTES + Q_BYTES);
           tma_load_2d(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM, bars.full_L(slot));
-          tma_load_2d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, nt * 16, bars.full_L(slot));
+          tma_load_2d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, nt * NT16, bars.full_L(slot));
           ++ls;
         }
       }
@@ -206,18 +214,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = gc & 1;
           if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(b * 2 * BN);
           for (int ks = 0; ks < p.spg; ++ks) {
             const int sl = ls % SL, sb = bs % SB;
             if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
             if (!mbar_wait(bars.full_B(sb), (bs / SB) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t adesc = sw128_desc(sbase + OFF_A + sl * A_BYTES);
+            const uint64_t adesc0 = sw128_desc(sbase + OFF_A + sl * A_BYTES);
+            const uint64_t adesc1 = sw128_desc(sbase + OFF_A + sl * A_BYTES + UM * 128);
             const uint64_t bdesc = sw128_desc(sbase + OFF_B + sb * B_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
-              tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
+              tc_mma_f16(d_tmem, adesc0 + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
+              tc_mma_f16(d_tmem + BN, adesc1 + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
             }
             tc_commit(bars.empty_L(sl));
             tc_commit(bars.empty_B(sb));
@@ -249,15 +259,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb % (4 * p.spg) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
-          // scale block -> float32 columns: thread dt owns tile dt>>3, g = dt&7
-          const int ti = dt >> 3, tg = dt & 7;
-          const uint4 raw = *reinterpret_cast<const uint4 *>(smem + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
-          float *scf = reinterpret_cast<float *>(smem + OFF_SC) + cur * SC_FLOATS;
-          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          // scale block -> float32 columns: thread dt < 64 owns tile dt>>3, g = dt&7
+          if (dt < NT16 * 8) {
+            const int ti = dt >> 3, tg = dt & 7;
+            const uint4 raw =
+                *reinterpret_cast<const uint4 *>(smem + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
+            float *scf = reinterpret_cast<float *>(smem + OFF_SC) + cur * SC_FLOATS;
+            const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            scf[j * BN + 16 * ti + tg] = bf16lo_to_f32(rw[j]);
-            scf[j * BN + 16 * ti + tg + 8] = bf16hi_to_f32(rw[j]);
+            for (int j = 0; j < 4; ++j) {
+              scf[j * BN + 16 * ti + tg] = bf16lo_to_f32(rw[j]);
+              scf[j * BN + 16 * ti + tg + 8] = bf16hi_to_f32(rw[j]);
+            }
           }
           mbar_arrive(bars.conv_S(cur));
           ++sc;
@@ -268,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *qs = smem + OFF_Q + sl * Q_BYTES;
         uint8_t *bt = smem + OFF_B + sb * B_BYTES;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int i = dw + 4 * r;  // 16-row tile within the CTA's 256 rows
+        for (int r = 0; r < NT16 / 4; ++r) {
+          const int i = dw + 4 * r;  // 16-row tile within the CTA's 128 rows
           uint32_t zg, zg8;
           if (SYM) {
             zg = zg8 = zero_pair(8);
@@ -307,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31 = tile rows
-    const int hf = (warp - 8) >> 2;  // columns 128*hf .. +127
+    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31
+    const int hf = (warp - 8) >> 2;  // x-row half: D columns 128*hf .. +127 of a buffer
     float acc[128];
     uint32_t gc = 0, sc = 0;
     int cur = 0;
@@ -326,11 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = gc & 1;
         if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const float *scp = reinterpret_cast<const float *>(smem + OFF_SC) + cur * SC_FLOATS + (gi & 3) * BN + hf * 128;
+        const float *scp = reinterpret_cast<const float *>(smem + OFF_SC) + cur * SC_FLOATS + (gi & 3) * BN;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float d[32];
-          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + hf * 128 + ch * 32), d);
+          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + hf * BN + ch * 32), d);
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 s4 = *reinterpret_cast<const float4 *>(scp + ch * 32 + c);
@@ -350,16 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gc;
       }
       if (!ok) break;
-      const int m = mt * BM + 32 * q + lane;
+      const int m = mt * BM + hf * UM + 32 * q + lane;
       if (m < p.M) {
         uint16_t *yrow = p.y + (size_t)m * p.ld;
         const bool vec = (p.ld & 7) == 0;
         if (GATEUP) {
-          // columns 32pp + r (gate) and 32pp + 16 + r (up) of this half are rows
-          // 16 * (8 nt + 4 hf + pp) + r of the gate and up weights
+          // columns 32pp + r (gate) and 32pp + 16 + r (up) are rows
+          // 16 * (4 nt + pp) + r of the gate and up weights
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
-            const int n0 = 16 * (8 * nt + 4 * hf + pp);
+            const int n0 = 16 * (4 * nt + pp);
             float hv[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
@@ -385,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int c8 = 0; c8 < 16; ++c8) {
-            const int n0 = nt * BN + hf * 128 + c8 * 8;
+            const int n0 = nt * BN + c8 * 8;
             if (vec && n0 + 8 <= p.N) {
               uint4 v = make_uint4(pack_bf16x2(acc[c8 * 8], acc[c8 * 8 + 1]),
                                    pack_bf16x2(acc[c8 * 8 + 2], acc[c8 * 8 + 3]),
@@ -467,15 +480,15 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   bool ok = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, (uint64_t)c.K, (uint64_t)c.M,
                       (uint64_t)c.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.codes_off, (uint64_t)L.chunks * 128,
-                       (uint64_t)L.tiles, (uint64_t)L.chunks * kChunkBytes, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+                       (uint64_t)L.tiles, (uint64_t)L.chunks * kChunkBytes, 128, NT16, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.scales_off, (uint64_t)L.gblocks * 32,
-                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, 16,
+                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, NT16,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (c.sym) {
     tz = ts;  // unused
   } else {
     ok = ok && encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.zeros_off, (uint64_t)L.gblocks * 8,
-                         (uint64_t)L.tiles, (uint64_t)L.gblocks * kZeroBlockBytes, 8, 16,
+                         (uint64_t)L.tiles, (uint64_t)L.gblocks * kZeroBlockBytes, 8, NT16,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return cudaErrorInvalidValue;

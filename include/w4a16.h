@@ -102,8 +102,9 @@ int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const i
  * float32 accumulation; each group's partial sum is scaled in float32.
  * `scales` and `zeros` are reserved: scales and zero points travel inside
  * `packed`, and both must be NULL (else W4A16_ERR_INVALID_ARG).
- * Kernel choice: M = 1 -> one-row GEMV; 2 <= M <= 16 -> small-M tensor-core
- * kernel reading each weight once for all rows; M > 16 -> the tcgen05 GEMM.
+ * Kernel choice: M <= 16 -> the decode kernel (each weight read and unpacked
+ * once for all rows, multiply-adds on the tensor core); M > 16 -> the tcgen05
+ * GEMM. A CUDA-core one-row GEMV is selectable (w4a16_set_kernel_override).
  * Results are bitwise reproducible run to run (no atomics in any sum).
  */
 int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,

@@ -41,6 +41,10 @@ namespace w4a16 {
 namespace {
 
 constexpr int kWarps = 4;       // warps per CTA
+// ring depth (K units in flight per warp) for two tiles per warp
+#ifndef W4A16_DECODE_SLOTS2
+#define W4A16_DECODE_SLOTS2 2
+#endif
 constexpr int kUnitChunks = 4;  // 64-wide K chunks per ring slot (256 k)
 
 struct DecodeParams {
@@ -182,7 +186,7 @@ struct Ring {
     }
   }
 
-  __device__ const uint8_t *slot(int s) const { return base + s * kSlotBytes; }
+  __device__ uint32_t slot(int s) const { return sbase + s * kSlotBytes; }
 };
 
 // Sum the per-warp partials red[w][e] into red[0][e]; with a cluster, rank 0
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
     const int u = ub + it;
     const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);  // groups in this unit
     if (!wait_slot<SLOTS>(ring.bar0, it, abort_flag, p.err)) break;
-    const uint8_t *sl = ring.slot(it % SLOTS);
+    const uint32_t sl = ring.slot(it % SLOTS);
 #pragma unroll
     for (int j = 0; j < GPU; ++j) {
       if (j < ngu) {
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
           if (SYM) {
             zg[i] = zg8[i] = zero_pair(8);
           } else {
-            const uint32_t zb = sl[R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3)];
+            const uint32_t zb = lds8(sl + R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3));
             zg[i] = zero_pair(zb & 0xF);
             zg8[i] = zero_pair(zb >> 4);
           }
@@ -336,7 +340,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
           uint4 w[TPW];
 #pragma unroll
           for (int i = 0; i < TPW; ++i)
-            w[i] = *reinterpret_cast<const uint4 *>(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
+            w[i] = lds128(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
 #pragma unroll
           for (int st = 0; st < 4; ++st) {
             // B fragment: x words 2st (k+0, k+1) and 2st+1 (k+2, k+3) of this lane's 16 k
@@ -362,8 +366,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
         }
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
-          const uint32_t sw =
-              *reinterpret_cast<const uint32_t *>(sl + R::kScaleOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
+          const uint32_t sw = lds32(sl + R::kScaleOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
           const float sg = bf16lo_to_f32(sw), sg8 = bf16hi_to_f32(sw);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
     const int u = ub + it;
     const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);
     if (!wait_slot<SLOTS>(ring.bar0, it, abort_flag, p.err)) break;
-    const uint8_t *sl = ring.slot(it % SLOTS);
+    const uint32_t sl = ring.slot(it % SLOTS);
 #pragma unroll
     for (int j = 0; j < GPU; ++j) {
       if (j < ngu) {
@@ -475,11 +478,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
         }
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
-          const uint32_t sw =
-              *reinterpret_cast<const uint32_t *>(sl + R::kScaleOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
+          const uint32_t sw = lds32(sl + R::kScaleOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
           uint32_t za = 8, zb = 8;
           if (!SYM) {
-            const uint32_t zbyte = sl[R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3)];
+            const uint32_t zbyte = lds8(sl + R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3));
             za = zbyte & 0xF;
             zb = zbyte >> 4;
           }
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
 #pragma unroll
           for (int cc = 0; cc < CPG; ++cc) {
             const int cl = j * CPG + cc;
-            const uint4 wv = *reinterpret_cast<const uint4 *>(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
+            const uint4 wv = lds128(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
 #pragma unroll
             for (int st = 0; st < 4; ++st) {
               const uint32_t wd = word_of(wv, st);
@@ -573,22 +575,24 @@ struct DecodeCfg {
   int tpw, kc, smem;
 };
 
-// Split-K choice: the largest cluster split (<= 8) that still lets every CTA
-// of the grid be resident at once (one wave), with at least one K unit per
-// warp; grids that already fill the GPU stay unsplit.
+// Split-K choice: grids that already fill the GPU stay unsplit (each warp
+// then streams long K slices and its ring stays full); smaller grids take the
+// largest cluster split (<= 8) that keeps them within one wave, with at least
+// two K units per warp. Measured: splitting a 1.2-wave grid four ways to even
+// out the waves made it slower (each warp's first slot latency dominates).
 template <typename Kern>
 cudaError_t pick_cfg(Kern kern, int smem, int tiles, int units, int sm_count, int tpw, DecodeCfg &c) {
   c.tpw = tpw;
   c.smem = smem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int ctas = (tiles + tpw - 1) / tpw;
+  const long long ctas = (tiles + tpw - 1) / tpw;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * kWarps, smem) != cudaSuccess || occ < 1)
     occ = 1;
   const long long resident = (long long)occ * sm_count;
   c.kc = 1;
-  while (c.kc < 8 && (long long)ctas * c.kc * 2 <= resident && units >= kWarps * c.kc * 2) c.kc *= 2;
+  while (c.kc < 8 && ctas * c.kc * 2 <= resident && units >= kWarps * c.kc * 4) c.kc *= 2;
   return cudaSuccess;
 }
 
@@ -635,7 +639,7 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
   return p;
 }
 
-constexpr int slots_for(int tpw) { return tpw >= 4 ? 2 : 3; }
+constexpr int slots_for(int tpw) { return tpw >= 4 ? 2 : W4A16_DECODE_SLOTS2; }
 
 template <int MT, int TPW, bool SYM, int CPG, bool GATEUP>
 cudaError_t run_mma(const DecodeParams &p, int sm_count, cudaStream_t s) {

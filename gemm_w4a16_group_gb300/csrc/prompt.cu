@@ -262,14 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // scale block -> float32 columns: thread dt < 64 owns tile dt>>3, g = dt&7
           if (dt < NT16 * 8) {
             const int ti = dt >> 3, tg = dt & 7;
-            const uint4 raw =
-                *reinterpret_cast<const uint4 *>(smem + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
-            float *scf = reinterpret_cast<float *>(smem + OFF_SC) + cur * SC_FLOATS;
+            const uint4 raw = lds128(sbase + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
+            const uint32_t scf = sbase + OFF_SC + cur * SC_FLOATS * 4;
             const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              scf[j * BN + 16 * ti + tg] = bf16lo_to_f32(rw[j]);
-              scf[j * BN + 16 * ti + tg + 8] = bf16hi_to_f32(rw[j]);
+              sts32f(scf + (j * BN + 16 * ti + tg) * 4, bf16lo_to_f32(rw[j]));
+              sts32f(scf + (j * BN + 16 * ti + tg + 8) * 4, bf16hi_to_f32(rw[j]));
             }
           }
           mbar_arrive(bars.conv_S(cur));
@@ -278,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sl = ls % SL, sb = bs % SB;
         if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
         if (!mbar_wait(bars.empty_B(sb), ((bs / SB) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        const uint8_t *qs = smem + OFF_Q + sl * Q_BYTES;
-        uint8_t *bt = smem + OFF_B + sb * B_BYTES;
+        const uint32_t qs = sbase + OFF_Q + sl * Q_BYTES;
+        const uint32_t bt = sbase + OFF_B + sb * B_BYTES;
 #pragma unroll
         for (int r = 0; r < NT16 / 4; ++r) {
           const int i = dw + 4 * r;  // 16-row tile within the CTA's 128 rows
@@ -287,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SYM) {
             zg = zg8 = zero_pair(8);
           } else {
-            const uint32_t zb = smem[OFF_RZ + cur * RZ_BYTES + (i * 8 + g) * 4 + (gi & 3)];
+            const uint32_t zb = lds8(sbase + OFF_RZ + cur * RZ_BYTES + (i * 8 + g) * 4 + (gi & 3));
             zg = zero_pair(zb & 0xF);
             zg8 = zero_pair(zb >> 4);
           }
-          const uint4 q = *reinterpret_cast<const uint4 *>(qs + (i * 32 + lane) * 16);
+          const uint4 q = lds128(qs + (i * 32 + lane) * 16);
           uint32_t u[4][4];
           unpack_word(q.x, zg, zg8, p.uc, u[0]);
           unpack_word(q.y, zg, zg8, p.uc, u[1]);
@@ -302,11 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int n = 16 * i + g + 8 * h;
-            uint8_t *row = bt + (n >> 3) * 1024 + (n & 7) * 128;
+            const uint32_t row = bt + (n >> 3) * 1024 + (n & 7) * 128;
             const uint4 lo = make_uint4(u[0][h], u[0][2 + h], u[1][h], u[1][2 + h]);
             const uint4 hi = make_uint4(u[2][h], u[2][2 + h], u[3][h], u[3][2 + h]);
-            *reinterpret_cast<uint4 *>(row + (((2 * t) ^ (n & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4 *>(row + (((2 * t + 1) ^ (n & 7)) << 4)) = hi;
+            sts128(row + (((2 * t) ^ (n & 7)) << 4), lo);
+            sts128(row + (((2 * t + 1) ^ (n & 7)) << 4), hi);
           }
         }
         fence_proxy_async_smem();
@@ -339,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = gc & 1;
         if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const float *scp = reinterpret_cast<const float *>(smem + OFF_SC) + cur * SC_FLOATS + (gi & 3) * BN;
+        const uint32_t scp = sbase + OFF_SC + (cur * SC_FLOATS + (gi & 3) * BN) * 4;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float d[32];
           tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + hf * BN + ch * 32), d);
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
-            const float4 s4 = *reinterpret_cast<const float4 *>(scp + ch * 32 + c);
+            const float4 s4 = lds128f(scp + (ch * 32 + c) * 4);
             float2 a0 = make_float2(acc[ch * 32 + c], acc[ch * 32 + c + 1]);
             float2 a1 = make_float2(acc[ch * 32 + c + 2], acc[ch * 32 + c + 3]);
             a0 = __ffma2_rn(make_float2(s4.x, s4.y), make_float2(d[c], d[c + 1]), a0);

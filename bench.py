@@ -37,6 +37,33 @@ import synth  # noqa: E402
 from synth.workloads import WORKLOADS, algorithmic_bytes, gemm_flops  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: a stored ncu traffic figure is only reported
+    while the kernels it was measured on are unchanged."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_w4a16_group_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(f, "rb") as fh:
+                h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(name: str):
+    """DRAM bytes (read + write) per launch measured by ncu for `name`, or None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch", {}).get(name)
 DEFAULT = "decode_ffn_m1"  # gate+up GEMV followed by the down GEMV
 
 
@@ -256,7 +283,7 @@ def run_cuda(args, rank, world):
                    "parallelism": f"replicas x{world}", "per_call_ms": [round(v, 5) for v in per_call_ms]},
         "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
                      "achieved": round(achieved, 2), "peak": peak, "unit": d["unit"],
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": stored_traffic(d["name"]),
                      "peak_src": peaks["src"] + (" bf16 burst" if is_flops else " copy")},
         "e2e": {"value": round(e2e, 2), "unit": parts[0]["unit"], "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -338,9 +365,13 @@ def main():
                     help=f"{DEFAULT} (default), one of {sorted(WORKLOADS)}, or shape:M,N,K,G,sym|asym")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],
                     help="kernel override for A/B measurement (default: automatic choice)")
     args = ap.parse_args()
+    if args.print_source_hash:
+        print(kernel_source_hash())
+        return
     args.warmup = max(3, args.warmup)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

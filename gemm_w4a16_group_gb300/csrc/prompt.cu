@@ -127,20 +127,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < SL; ++i) {
       mbar_init(bars.full_L(i), 1);
-      mbar_init(bars.empty_L(i), 128 + 1);  // 128 dequant threads + one MMA commit
+      mbar_init(bars.empty_L(i), 4 + 1);  // one arrive per dequant warp + one MMA commit
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(bars.full_B(i), 128);
+      mbar_init(bars.full_B(i), 4);
       mbar_init(bars.empty_B(i), 1);
     }
     for (int i = 0; i < SS; ++i) {
       mbar_init(bars.full_S(i), 1);
-      mbar_init(bars.conv_S(i), 128);
-      mbar_init(bars.empty_S(i), 256);
+      mbar_init(bars.conv_S(i), 4);
+      mbar_init(bars.empty_S(i), 8);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.tfull(i), 1);
-      mbar_init(bars.tempty(i), 256);
+      mbar_init(bars.tempty(i), 8);
     }
     mbar_init(bars.mma_done(), 1);
     *abort_flag = 0;
@@ -164,6 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
+      // x is re-read by every weight-column tile: keep it in L2; each codes
+      // tile is read by the 16 row tiles in flight at once, then not again
+      uint64_t pol_keep, pol_stream;
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_stream));
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_s);
@@ -186,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = ls % SL;
           if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(bars.full_L(slot), A_BYTES + Q_BYTES);
-          tma_load_2d(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM, bars.full_L(slot));
-          tma_load_2d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, nt * NT16, bars.full_L(slot));
+          tma_load_2d_hint(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM, bars.full_L(slot), pol_keep);
+          tma_load_2d_hint(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, nt * NT16, bars.full_L(slot), pol_stream);
           ++ls;
         }
       }
@@ -271,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               sts32f(scf + (j * BN + 16 * ti + tg + 8) * 4, bf16hi_to_f32(rw[j]));
             }
           }
-          mbar_arrive(bars.conv_S(cur));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.conv_S(cur));
           ++sc;
         }
         const int sl = ls % SL, sb = bs % SB;
@@ -308,9 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             sts128(row + (((2 * t + 1) ^ (n & 7)) << 4), hi);
           }
         }
+        // each lane makes its stores visible to the tensor core, then one lane per
+        // warp signals the MMA thread and releases the codes stage
         fence_proxy_async_smem();
-        mbar_arrive(bars.full_B(sb));
-        mbar_arrive(bars.empty_L(sl));
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bars.full_B(sb));
+          mbar_arrive(bars.empty_L(sl));
+        }
         ++ls;
         ++bs;
       }
@@ -357,8 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(bars.tempty(b));
-        if ((gi & 3) == 3 || gi == p.ng - 1) mbar_arrive(bars.empty_S(cur));
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bars.tempty(b));
+          if ((gi & 3) == 3 || gi == p.ng - 1) mbar_arrive(bars.empty_S(cur));
+        }
         ++gc;
       }
       if (!ok) break;

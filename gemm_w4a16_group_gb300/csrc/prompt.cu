@@ -9,27 +9,35 @@
 // MMA, as the TensorFold PR #859 prompt GEMM does ("each weight rounded once to
 // bf16"), would cost up to 2^-9 per weight; this split keeps every weight
 // exact. The feed-forward gate is fused as in the GRIMOIRE v1.8 release notes
-// ("INT4 prompt processing"): the CTA's 128 weight rows are 64 gate rows and
-// the 64 matching up rows (16-row tiles alternate), so h = SiLU(g) * u is
+// ("INT4 prompt processing"): each 128 weight rows of a tile are 64 gate rows
+// and the 64 matching up rows (16-row tiles alternate), so h = SiLU(g) * u is
 // formed from two float32 accumulators of the same thread before a single
 // bf16 rounding.
 //
-// A CTA tile is 256 rows of x by 128 weight rows: two M = 128 MMAs per K step
-// share one dequantised B tile, which halves the dequantisation work (the
-// pacing role) per multiply-add against a 128 x 256 tile.
+// A tile is 256 rows of x by 256 weight rows, computed by a pair of CTAs on
+// two SMs with the pair form of the MMA (cta_group::2, M = 256, N = 256,
+// K = 16): each CTA stages its own 128 x rows and dequantises its own 128
+// weight rows, and the tensor cores of both SMs share the two weight halves.
+// Per multiply-add this halves the shared-memory operand traffic of an SM and
+// the x bytes it pulls from L2 against a one-SM 256 x 128 tile, with the same
+// dequantisation work per SM.
 //
-// One persistent CTA per SM, 512 threads, warp-specialised:
-//   warp 0       TMA producer: x tile [256 x 64] (128-byte swizzle), packed codes of
-//                128 rows x 64 k, and per four groups the scale (+ zero) block
-//   warp 1       TMEM allocator and the single MMA-issuing thread:
-//                D[b][h] (+)= A[h] . B^T, M = 128, N = 128, K = 16, h = x-row half,
-//                b = group parity
+// One persistent CTA pair per two SMs, 512 threads per CTA, warp-specialised:
+//   warp 0       TMA producer: the CTA's x rows [128 x 64] (128-byte swizzle), the
+//                packed codes of its 128 weight rows x 64 k, and per four groups
+//                the scale block of all 256 weight rows (+ the zero block of its own)
+//   warp 1       TMEM allocation (both CTAs); in the even CTA the single thread
+//                issuing D[b] (+)= A . B^T for the pair, b = group parity
 //   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
-//                128-byte-swizzled K-major B tile; scale block -> float32
-//   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b][h];
+//                128-byte-swizzled K-major B half; scale block -> float32
+//   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b];
 //                per tile, the bf16 store (or SiLU(gate) * up)
-// Every wait is bounded; a wait that gives up sets the device error word and
-// every role leaves its loop, drains what it started and exits.
+// The odd CTA signals the even CTA's barriers with remote arrivals (B half
+// written, TMEM buffer drained); the MMA thread's commits arrive on the
+// barriers of both CTAs. Every wait is bounded; a wait that gives up sets the
+// device error word and both CTAs' abort flags, every role leaves its loop,
+// drains what it started, and the pair meets at a cluster barrier before the
+// TMEM is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,20 +46,25 @@
 namespace w4a16 {
 namespace {
 
-constexpr int BM = 256, BN = 128, BK = 64;
-constexpr int UM = 128;      // rows of one MMA (one x-row half)
-constexpr int NT16 = BN / 16;  // 16-row weight tiles per CTA tile
-constexpr int SL = 4;  // x + codes ring
-constexpr int SB = 4;  // dequantised B ring
-constexpr int SS = 2;  // scale-block ring (4 groups each)
+constexpr int BM = 256, BN = 256, BK = 64;  // pair tile
+constexpr int HM = BM / 2, HN = BN / 2;     // x rows and weight rows of one CTA
+constexpr int NT16 = HN / 16;               // 16-row weight tiles of one CTA
+constexpr int PT16 = BN / 16;               // ... of the pair
+#ifndef W4A16_PROMPT_SL
+#define W4A16_PROMPT_SL 6
+#endif
+constexpr int SL = W4A16_PROMPT_SL;  // x + codes ring
+constexpr int SB = 4;                // dequantised B ring
+constexpr int SS = 2;                // scale-block ring (4 groups each)
 constexpr int kThreads = 512;
+constexpr uint16_t kPairMask = 0x3;
 
-constexpr int A_BYTES = BM * BK * 2;   // 32768: x rows 0-127 then 128-255
-constexpr int B_BYTES = BN * BK * 2;   // 16384
-constexpr int Q_BYTES = BN * BK / 2;   // 4096
-constexpr int RS_BYTES = NT16 * kScaleBlockBytes;  // 1024
-constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256
-constexpr int SC_FLOATS = 4 * BN;                // float32 scales of one block
+constexpr int A_BYTES = HM * BK * 2;  // 16384
+constexpr int B_BYTES = HN * BK * 2;  // 16384
+constexpr int Q_BYTES = HN * BK / 2;  // 4096
+constexpr int RS_BYTES = PT16 * kScaleBlockBytes;  // 2048: scales of the pair's 256 rows
+constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256: zeros of the CTA's 128 rows
+constexpr int SC_FLOATS = 4 * BN;                  // float32 scales of one block
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + SL * A_BYTES;
@@ -70,8 +83,8 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(OFF_B % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-constexpr uint32_t kIdesc = idesc_bf16_f32(UM, BN);
-constexpr uint32_t kTmemCols = 512;  // two buffers x two x-row halves x 128 fp32 columns
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+constexpr uint32_t kTmemCols = 512;  // two buffers x 256 fp32 columns
 
 struct PromptParams {
   uint16_t *y;
@@ -99,9 +112,19 @@ struct Bars {
   __device__ uint32_t mma_done() const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + 4); }
 };
 
-__device__ __forceinline__ void give_up(volatile int *abort_flag, int *err) {
+// this CTA's abort flag and the peer's (remote store), then the error word
+__device__ __forceinline__ void give_up(volatile int *abort_flag, uint32_t peer_abort, int *err) {
   *abort_flag = 1;
+  st_cluster_u32(peer_abort, 1u);
   atomicExch(err, kErrTimeout);
+}
+
+// arrive on the even CTA's copy of a barrier: locally there, remotely from the odd CTA
+__device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t rank) {
+  if (rank == 0)
+    mbar_arrive(bar);
+  else
+    mbar_arrive_remote(mapa_shared(bar, 0));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -122,15 +145,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd
+  const uint32_t peer_abort = mapa_shared(smem_u32(smem + OFF_MISC + 4), rank ^ 1u);
+  const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
   const int ntot = p.mtiles * p.ntiles;
 
   if (tid == 0) {
     for (int i = 0; i < SL; ++i) {
       mbar_init(bars.full_L(i), 1);
-      mbar_init(bars.empty_L(i), 4 + 1);  // one arrive per dequant warp + one MMA commit
+      mbar_init(bars.empty_L(i), 1);  // the MMA commit (multicast to both CTAs)
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(bars.full_B(i), 4);
+      mbar_init(bars.full_B(i), 8);  // even CTA: 4 local + 4 remote dequant warps
       mbar_init(bars.empty_B(i), 1);
     }
     for (int i = 0; i < SS; ++i) {
@@ -140,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.tfull(i), 1);
-      mbar_init(bars.tempty(i), 8);
+      mbar_init(bars.tempty(i), 16);  // even CTA: 8 local + 8 remote epilogue warps
     }
     mbar_init(bars.mma_done(), 1);
     *abort_flag = 0;
@@ -148,11 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc2(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish2();
   }
+  // barriers of both CTAs initialised before any remote arrival or commit
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -165,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       // x is re-read by every weight-column tile: keep it in L2; each codes
-      // tile is read by the 16 row tiles in flight at once, then not again
+      // tile is read by the row tiles in flight at once, then not again
       uint64_t pol_keep, pol_stream;
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_stream));
@@ -175,29 +202,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!SYM) tma_prefetch_desc(&tm_z);
       uint32_t ls = 0, sc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < ntot; tile += npairs) {
         const int mt = tile % p.mtiles, nt = tile / p.mtiles;
+        const int qt = nt * PT16 + (int)rank * NT16;  // first 16-row tile of this CTA's half
         for (int kb = 0; kb < p.nk; ++kb) {
           if (kb % (4 * p.spg) == 0) {
             const int slot = sc % SS;
             if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : RZ_BYTES));
             const int blk = kb / (4 * p.spg);
-            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, nt * NT16, bars.full_S(slot));
-            if (!SYM)
-              tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, nt * NT16, bars.full_S(slot));
+            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, nt * PT16, bars.full_S(slot));
+            if (!SYM) tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, qt, bars.full_S(slot));
             ++sc;
           }
           const int slot = ls % SL;
           if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(bars.full_L(slot), A_BYTES + Q_BYTES);
-          tma_load_2d_hint(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM, bars.full_L(slot), pol_keep);
-          tma_load_2d_hint(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, nt * NT16, bars.full_L(slot), pol_stream);
+          tma_load_2d_hint(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM + (int)rank * HM,
+                           bars.full_L(slot), pol_keep);
+          tma_load_2d_hint(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, qt, bars.full_L(slot), pol_stream);
           ++ls;
         }
       }
       if (!ok) {
-        give_up(abort_flag, p.err);
+        give_up(abort_flag, peer_abort, p.err);
         // let every copy already issued land before the CTA can exit
         for (uint32_t i = 0; i < SL && i < ls; ++i) {
           const uint32_t u = ls - 1 - i;
@@ -210,43 +238,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
       uint32_t ls = 0, bs = 0, gc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < ntot; tile += npairs) {
         for (int gi = 0; ok && gi < p.ng; ++gi) {
           const int b = gc & 1;
           if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(b * 2 * BN);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
           for (int ks = 0; ks < p.spg; ++ks) {
             const int sl = ls % SL, sb = bs % SB;
             if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
+            // the odd CTA's dequantisers arrive only after its own x and codes landed
             if (!mbar_wait(bars.full_B(sb), (bs / SB) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t adesc0 = sw128_desc(sbase + OFF_A + sl * A_BYTES);
-            const uint64_t adesc1 = sw128_desc(sbase + OFF_A + sl * A_BYTES + UM * 128);
+            const uint64_t adesc = sw128_desc(sbase + OFF_A + sl * A_BYTES);
             const uint64_t bdesc = sw128_desc(sbase + OFF_B + sb * B_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
-              tc_mma_f16(d_tmem, adesc0 + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
-              tc_mma_f16(d_tmem + BN, adesc1 + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
+              tc_mma2_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
             }
-            tc_commit(bars.empty_L(sl));
-            tc_commit(bars.empty_B(sb));
+            tc_commit2_mc(bars.empty_L(sl), kPairMask);
+            tc_commit2_mc(bars.empty_B(sb), kPairMask);
             ++ls;
             ++bs;
           }
           if (!ok) break;
-          tc_commit(bars.tfull(b));
+          tc_commit2_mc(bars.tfull(b), kPairMask);
           ++gc;
         }
       }
-      if (!ok) give_up(abort_flag, p.err);
-      // every MMA issued by this thread completes before TMEM can be freed
-      tc_commit(bars.mma_done());
+      if (!ok) give_up(abort_flag, peer_abort, p.err);
+      // every MMA issued by this thread completes before the pair's TMEM can be freed
+      tc_commit2(bars.mma_done());
       mbar_wait_drain(bars.mma_done(), 0);
     }
     }
@@ -258,14 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ls = 0, bs = 0, sc = 0;
     int cur = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+    for (int tile = pair; ok && tile < ntot; tile += npairs) {
       for (int kb = 0; kb < p.nk; ++kb) {
         const int gi = kb / p.spg;
         if (kb % (4 * p.spg) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
-          // scale block -> float32 columns: thread dt < 64 owns tile dt>>3, g = dt&7
-          if (dt < NT16 * 8) {
+          // scale block of the pair's 16 tiles -> float32 columns: thread dt owns
+          // tile dt>>3, g = dt&7
+          {
             const int ti = dt >> 3, tg = dt & 7;
             const uint4 raw = lds128(sbase + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
             const uint32_t scf = sbase + OFF_SC + cur * SC_FLOATS * 4;
@@ -314,29 +342,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             sts128(row + (((2 * t + 1) ^ (n & 7)) << 4), hi);
           }
         }
-        // each lane makes its stores visible to the tensor core, then one lane per
-        // warp signals the MMA thread and releases the codes stage
+        // each lane makes its stores visible to the tensor cores, then one lane
+        // per warp signals the MMA thread of the pair (the codes stage is
+        // released by the MMA commit, which follows this arrival)
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bars.full_B(sb));
-          mbar_arrive(bars.empty_L(sl));
-        }
+        if (lane == 0) arrive_even(bars.full_B(sb), rank);
         ++ls;
         ++bs;
       }
     }
-    if (!ok) give_up(abort_flag, p.err);
+    if (!ok) give_up(abort_flag, peer_abort, p.err);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31
-    const int hf = (warp - 8) >> 2;  // x-row half: D columns 128*hf .. +127 of a buffer
+    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31: x rows of this CTA
+    const int ch2 = (warp - 8) >> 2;  // D columns 128*ch2 .. +127: weight rows of CTA ch2
     float acc[128];
     uint32_t gc = 0, sc = 0;
     int cur = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < ntot; tile += gridDim.x) {
+    for (int tile = pair; ok && tile < ntot; tile += npairs) {
       const int mt = tile % p.mtiles, nt = tile / p.mtiles;
 #pragma unroll
       for (int c = 0; c < 128; ++c) acc[c] = 0.f;
@@ -349,11 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = gc & 1;
         if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t scp = sbase + OFF_SC + (cur * SC_FLOATS + (gi & 3) * BN) * 4;
+        const uint32_t scp = sbase + OFF_SC + (cur * SC_FLOATS + (gi & 3) * BN + ch2 * HN) * 4;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float d[32];
-          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 2 * BN + hf * BN + ch * 32), d);
+          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + ch2 * HN + ch * 32), d);
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 s4 = lds128f(scp + (ch * 32 + c) * 4);
@@ -370,22 +396,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bars.tempty(b));
+          arrive_even(bars.tempty(b), rank);
           if ((gi & 3) == 3 || gi == p.ng - 1) mbar_arrive(bars.empty_S(cur));
         }
         ++gc;
       }
       if (!ok) break;
-      const int m = mt * BM + hf * UM + 32 * q + lane;
+      const int m = mt * BM + (int)rank * HM + 32 * q + lane;
       if (m < p.M) {
         uint16_t *yrow = p.y + (size_t)m * p.ld;
         const bool vec = (p.ld & 7) == 0;
         if (GATEUP) {
-          // columns 32pp + r (gate) and 32pp + 16 + r (up) are rows
-          // 16 * (4 nt + pp) + r of the gate and up weights
+          // columns 32pp + r (gate) and 32pp + 16 + r (up) of this half are rows
+          // 16 * (8 nt + 4 ch2 + pp) + r of the gate and up weights
 #pragma unroll
           for (int pp = 0; pp < 4; ++pp) {
-            const int n0 = 16 * (4 * nt + pp);
+            const int n0 = 16 * (8 * nt + 4 * ch2 + pp);
             float hv[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
@@ -411,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int c8 = 0; c8 < 16; ++c8) {
-            const int n0 = nt * BN + c8 * 8;
+            const int n0 = nt * BN + ch2 * HN + c8 * 8;
             if (vec && n0 + 8 <= p.N) {
               uint4 v = make_uint4(pack_bf16x2(acc[c8 * 8], acc[c8 * 8 + 1]),
                                    pack_bf16x2(acc[c8 * 8 + 2], acc[c8 * 8 + 3]),
@@ -430,14 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok) give_up(abort_flag, p.err);
+    if (!ok) give_up(abort_flag, peer_abort, p.err);
   }
 
+  // both CTAs done with every barrier, smem operand and TMEM column of the pair
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc2(tmem_base, kTmemCols);
   }
 }
 
@@ -470,32 +497,52 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
   return r == CUDA_SUCCESS;
 }
 
+// Launch as clusters of two CTAs: one pair per tile, as many pairs as fit at
+// once (found once per instantiation), each walking the tiles with a stride.
 template <bool SYM, bool GATEUP>
 cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
-                           const CUtensorMap &tz, const PromptParams &p, int grid, cudaStream_t s) {
+                           const CUtensorMap &tz, const PromptParams &p, int ntot, cudaStream_t s) {
   auto kern = prompt_tc_kernel<SYM, GATEUP>;
-  static bool attr_set = false;  // per instantiation; attribute is per device function
-  if (!attr_set) {
+  cudaLaunchConfig_t lc = {};
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = SMEM_ALLOC;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  static int max_pairs = 0;  // per instantiation (one device type: sm_103a)
+  if (max_pairs == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    lc.gridDim = dim3(2, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &lc);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs = n;
   }
-  kern<<<grid, kThreads, SMEM_ALLOC, s>>>(tx, tq, ts, tz, p);
-  return cudaGetLastError();
+  const int pairs = ntot < max_pairs ? ntot : max_pairs;
+  lc.gridDim = dim3(2 * pairs, 1, 1);
+  return cudaLaunchKernelEx(&lc, kern, tx, tq, ts, tz, p);
 }
 
 }  // namespace
 
 cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
+  (void)sm_count;  // the pair count comes from the cluster occupancy query
   const int rows = packed_rows(c);
   const Layout L = make_layout(rows, c.K, c.group, c.sym);
   CUtensorMap tx, tq, ts, tz;
   bool ok = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, (uint64_t)c.K, (uint64_t)c.M,
-                      (uint64_t)c.K * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+                      (uint64_t)c.K * 2, BK, HM, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.codes_off, (uint64_t)L.chunks * 128,
                        (uint64_t)L.tiles, (uint64_t)L.chunks * kChunkBytes, 128, NT16, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.scales_off, (uint64_t)L.gblocks * 32,
-                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, NT16,
+                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, PT16,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (c.sym) {
     tz = ts;  // unused
@@ -519,13 +566,12 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   p.err = c.err;
   p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;
-  const int grid = ntot < sm_count ? ntot : sm_count;
   if (c.sym) {
-    return c.gateup ? launch_variant<true, true>(tx, tq, ts, tz, p, grid, c.stream)
-                    : launch_variant<true, false>(tx, tq, ts, tz, p, grid, c.stream);
+    return c.gateup ? launch_variant<true, true>(tx, tq, ts, tz, p, ntot, c.stream)
+                    : launch_variant<true, false>(tx, tq, ts, tz, p, ntot, c.stream);
   }
-  return c.gateup ? launch_variant<false, true>(tx, tq, ts, tz, p, grid, c.stream)
-                  : launch_variant<false, false>(tx, tq, ts, tz, p, grid, c.stream);
+  return c.gateup ? launch_variant<false, true>(tx, tq, ts, tz, p, ntot, c.stream)
+                  : launch_variant<false, false>(tx, tq, ts, tz, p, ntot, c.stream);
 }
 
 }  // namespace w4a16

@@ -14,25 +14,27 @@
 // formed from two float32 accumulators of the same thread before a single
 // bf16 rounding.
 //
-// A tile is 256 rows of x by 256 weight rows, computed by a pair of CTAs on
+// A tile is 256 weight rows by 256 rows of x, computed by a pair of CTAs on
 // two SMs with the pair form of the MMA (cta_group::2, M = 256, N = 256,
-// K = 16): each CTA stages its own 128 x rows and dequantises its own 128
-// weight rows, and the tensor cores of both SMs share the two weight halves.
-// Per multiply-add this halves the shared-memory operand traffic of an SM and
-// the x bytes it pulls from L2 against a one-SM 256 x 128 tile, with the same
-// dequantisation work per SM.
+// K = 16): each CTA dequantises its own 128 weight rows (the A operand) and
+// stages its own 128 x rows (its half of the B operand). Per multiply-add
+// this halves the shared-memory operand traffic of an SM and the x bytes it
+// pulls from L2 against a one-SM tile of 256 x rows by 128 weight rows, with
+// the same dequantisation work per SM. With the weights on the M side, a TMEM
+// lane is one weight row, so an epilogue thread folds each group with a single
+// scale held in a register.
 //
 // One persistent CTA pair per two SMs, 512 threads per CTA, warp-specialised:
 //   warp 0       TMA producer: the CTA's x rows [128 x 64] (128-byte swizzle), the
 //                packed codes of its 128 weight rows x 64 k, and per four groups
-//                the scale block of all 256 weight rows (+ the zero block of its own)
+//                their scale (+ zero) block
 //   warp 1       TMEM allocation (both CTAs); in the even CTA the single thread
-//                issuing D[b] (+)= A . B^T for the pair, b = group parity
+//                issuing D[b] (+)= W . X^T for the pair, b = group parity
 //   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
-//                128-byte-swizzled K-major B half; scale block -> float32
+//                128-byte-swizzled K-major W tile
 //   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b];
 //                per tile, the bf16 store (or SiLU(gate) * up)
-// The odd CTA signals the even CTA's barriers with remote arrivals (B half
+// The odd CTA signals the even CTA's barriers with remote arrivals (W half
 // written, TMEM buffer drained); the MMA thread's commits arrive on the
 // barriers of both CTAs. Every wait is bounded; a wait that gives up sets the
 // device error word and both CTAs' abort flags, every role leaves its loop,
@@ -46,51 +48,48 @@
 namespace w4a16 {
 namespace {
 
-constexpr int BM = 256, BN = 256, BK = 64;  // pair tile
-constexpr int HM = BM / 2, HN = BN / 2;     // x rows and weight rows of one CTA
-constexpr int NT16 = HN / 16;               // 16-row weight tiles of one CTA
-constexpr int PT16 = BN / 16;               // ... of the pair
+constexpr int BW = 256, BX = 256, BK = 64;  // pair tile: weight rows, x rows, k per stage
+constexpr int HW = BW / 2, HX = BX / 2;     // weight rows and x rows of one CTA
+constexpr int NT16 = HW / 16;               // 16-row weight tiles of one CTA
 #ifndef W4A16_PROMPT_SL
 #define W4A16_PROMPT_SL 6
 #endif
 constexpr int SL = W4A16_PROMPT_SL;  // x + codes ring
-constexpr int SB = 4;                // dequantised B ring
+constexpr int SW = 4;                // dequantised W ring
 constexpr int SS = 2;                // scale-block ring (4 groups each)
 constexpr int kThreads = 512;
 constexpr uint16_t kPairMask = 0x3;
 
-constexpr int A_BYTES = HM * BK * 2;  // 16384
-constexpr int B_BYTES = HN * BK * 2;  // 16384
-constexpr int Q_BYTES = HN * BK / 2;  // 4096
-constexpr int RS_BYTES = PT16 * kScaleBlockBytes;  // 2048: scales of the pair's 256 rows
-constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256: zeros of the CTA's 128 rows
-constexpr int SC_FLOATS = 4 * BN;                  // float32 scales of one block
+constexpr int X_BYTES = HX * BK * 2;  // 16384
+constexpr int W_BYTES = HW * BK * 2;  // 16384
+constexpr int Q_BYTES = HW * BK / 2;  // 4096
+constexpr int RS_BYTES = NT16 * kScaleBlockBytes;  // 1024
+constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + SL * A_BYTES;
-constexpr int OFF_Q = OFF_B + SB * B_BYTES;
+constexpr int OFF_X = 0;
+constexpr int OFF_W = OFF_X + SL * X_BYTES;
+constexpr int OFF_Q = OFF_W + SW * W_BYTES;
 constexpr int OFF_RS = OFF_Q + SL * Q_BYTES;
 constexpr int OFF_RZ = OFF_RS + SS * RS_BYTES;
-constexpr int OFF_SC = OFF_RZ + SS * RZ_BYTES;
-constexpr int OFF_BAR = OFF_SC + SS * SC_FLOATS * 4;
-// barriers: full_L, empty_L [SL]; full_B, empty_B [SB]; full_S, conv_S, empty_S [SS];
+constexpr int OFF_BAR = OFF_RZ + SS * RZ_BYTES;
+// barriers: full_L, empty_L [SL]; full_W, empty_W [SW]; full_S, empty_S [SS];
 // tfull, tempty [2]; mma_done [1]
-constexpr int NBARS = 2 * SL + 2 * SB + 3 * SS + 2 * 2 + 1;
+constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * 2 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 
-static_assert(OFF_B % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(OFF_W % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+constexpr uint32_t kIdesc = idesc_bf16_f32(BW, BX);
 constexpr uint32_t kTmemCols = 512;  // two buffers x 256 fp32 columns
 
 struct PromptParams {
   uint16_t *y;
   int M, N, K;     // N: output columns (N_each for gate/up)
   int ld;          // y row stride (elements)
-  int mtiles, ntiles;
+  int mtiles, ntiles;  // tiles of 256 x rows, of 256 weight rows
   int nk;          // K / 64
   int ng;          // K / group
   int spg;         // 64-wide stages per group (1 or 2)
@@ -102,14 +101,13 @@ struct Bars {
   uint32_t base;
   __device__ uint32_t full_L(int i) const { return base + 8 * i; }
   __device__ uint32_t empty_L(int i) const { return base + 8 * (SL + i); }
-  __device__ uint32_t full_B(int i) const { return base + 8 * (2 * SL + i); }
-  __device__ uint32_t empty_B(int i) const { return base + 8 * (2 * SL + SB + i); }
-  __device__ uint32_t full_S(int i) const { return base + 8 * (2 * SL + 2 * SB + i); }
-  __device__ uint32_t conv_S(int i) const { return base + 8 * (2 * SL + 2 * SB + SS + i); }
-  __device__ uint32_t empty_S(int i) const { return base + 8 * (2 * SL + 2 * SB + 2 * SS + i); }
-  __device__ uint32_t tfull(int i) const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + i); }
-  __device__ uint32_t tempty(int i) const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + 2 + i); }
-  __device__ uint32_t mma_done() const { return base + 8 * (2 * SL + 2 * SB + 3 * SS + 4); }
+  __device__ uint32_t full_W(int i) const { return base + 8 * (2 * SL + i); }
+  __device__ uint32_t empty_W(int i) const { return base + 8 * (2 * SL + SW + i); }
+  __device__ uint32_t full_S(int i) const { return base + 8 * (2 * SL + 2 * SW + i); }
+  __device__ uint32_t empty_S(int i) const { return base + 8 * (2 * SL + 2 * SW + SS + i); }
+  __device__ uint32_t tfull(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + i); }
+  __device__ uint32_t tempty(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + 2 + i); }
+  __device__ uint32_t mma_done() const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + 4); }
 };
 
 // this CTA's abort flag and the peer's (remote store), then the error word
@@ -127,9 +125,9 @@ __device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t rank) {
     mbar_arrive_remote(mapa_shared(bar, 0));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t *>(&b);
 }
 
 template <bool SYM, bool GATEUP>
@@ -155,14 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.full_L(i), 1);
       mbar_init(bars.empty_L(i), 1);  // the MMA commit (multicast to both CTAs)
     }
-    for (int i = 0; i < SB; ++i) {
-      mbar_init(bars.full_B(i), 8);  // even CTA: 4 local + 4 remote dequant warps
-      mbar_init(bars.empty_B(i), 1);
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(bars.full_W(i), 8);  // even CTA: 4 local + 4 remote dequant warps
+      mbar_init(bars.empty_W(i), 1);
     }
     for (int i = 0; i < SS; ++i) {
       mbar_init(bars.full_S(i), 1);
-      mbar_init(bars.conv_S(i), 4);
-      mbar_init(bars.empty_S(i), 8);
+      mbar_init(bars.empty_S(i), SYM ? 8 : 8 + 4);  // epilogue warps (+ dequantisers reading zeros)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.tfull(i), 1);
@@ -191,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      // x is re-read by every weight-column tile: keep it in L2; each codes
-      // tile is read by the row tiles in flight at once, then not again
+      // x is re-read by every weight tile: keep it in L2; each codes tile is
+      // read by the x tiles in flight at once, then not again
       uint64_t pol_keep, pol_stream;
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_stream));
@@ -204,21 +201,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
         const int mt = tile % p.mtiles, nt = tile / p.mtiles;
-        const int qt = nt * PT16 + (int)rank * NT16;  // first 16-row tile of this CTA's half
+        const int qt = nt * (BW / 16) + (int)rank * NT16;  // first 16-row tile of this CTA's weights
         for (int kb = 0; kb < p.nk; ++kb) {
           if (kb % (4 * p.spg) == 0) {
             const int slot = sc % SS;
             if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : RZ_BYTES));
             const int blk = kb / (4 * p.spg);
-            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, nt * PT16, bars.full_S(slot));
+            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, qt, bars.full_S(slot));
             if (!SYM) tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, qt, bars.full_S(slot));
             ++sc;
           }
           const int slot = ls % SL;
           if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(bars.full_L(slot), A_BYTES + Q_BYTES);
-          tma_load_2d_hint(sbase + OFF_A + slot * A_BYTES, &tm_x, kb * BK, mt * BM + (int)rank * HM,
+          mbar_arrive_expect_tx(bars.full_L(slot), X_BYTES + Q_BYTES);
+          tma_load_2d_hint(sbase + OFF_X + slot * X_BYTES, &tm_x, kb * BK, mt * BX + (int)rank * HX,
                            bars.full_L(slot), pol_keep);
           tma_load_2d_hint(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, qt, bars.full_L(slot), pol_stream);
           ++ls;
@@ -240,31 +237,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
-      uint32_t ls = 0, bs = 0, gc = 0;
+      uint32_t ls = 0, ws = 0, gc = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
         for (int gi = 0; ok && gi < p.ng; ++gi) {
           const int b = gc & 1;
           if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(b * BX);
           for (int ks = 0; ks < p.spg; ++ks) {
-            const int sl = ls % SL, sb = bs % SB;
+            const int sl = ls % SL, sw = ws % SW;
             if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
             // the odd CTA's dequantisers arrive only after its own x and codes landed
-            if (!mbar_wait(bars.full_B(sb), (bs / SB) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(bars.full_W(sw), (ws / SW) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t adesc = sw128_desc(sbase + OFF_A + sl * A_BYTES);
-            const uint64_t bdesc = sw128_desc(sbase + OFF_B + sb * B_BYTES);
+            const uint64_t wdesc = sw128_desc(sbase + OFF_W + sw * W_BYTES);
+            const uint64_t xdesc = sw128_desc(sbase + OFF_X + sl * X_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
-              tc_mma2_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (ks | kk) != 0);
+              tc_mma2_f16(d_tmem, wdesc + 2 * kk, xdesc + 2 * kk, kIdesc, (ks | kk) != 0);
             }
             tc_commit2_mc(bars.empty_L(sl), kPairMask);
-            tc_commit2_mc(bars.empty_B(sb), kPairMask);
+            tc_commit2_mc(bars.empty_W(sw), kPairMask);
             ++ls;
-            ++bs;
+            ++ws;
           }
           if (!ok) break;
           tc_commit2_mc(bars.tfull(b), kPairMask);
@@ -280,39 +277,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
     // ------------------------------------------------------------------ dequantisers
-    const int dw = warp - 4, dt = tid - 128;
+    const int dw = warp - 4;
     const int g = lane >> 2, t = lane & 3;
-    uint32_t ls = 0, bs = 0, sc = 0;
+    uint32_t ls = 0, ws = 0, sc = 0;
     int cur = 0;
     bool ok = true;
     for (int tile = pair; ok && tile < ntot; tile += npairs) {
       for (int kb = 0; kb < p.nk; ++kb) {
         const int gi = kb / p.spg;
-        if (kb % (4 * p.spg) == 0) {
+        if (!SYM && kb % (4 * p.spg) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
-          // scale block of the pair's 16 tiles -> float32 columns: thread dt owns
-          // tile dt>>3, g = dt&7
-          {
-            const int ti = dt >> 3, tg = dt & 7;
-            const uint4 raw = lds128(sbase + OFF_RS + cur * RS_BYTES + (ti * 8 + tg) * 16);
-            const uint32_t scf = sbase + OFF_SC + cur * SC_FLOATS * 4;
-            const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              sts32f(scf + (j * BN + 16 * ti + tg) * 4, bf16lo_to_f32(rw[j]));
-              sts32f(scf + (j * BN + 16 * ti + tg + 8) * 4, bf16hi_to_f32(rw[j]));
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.conv_S(cur));
           ++sc;
         }
-        const int sl = ls % SL, sb = bs % SB;
+        const int sl = ls % SL, sw = ws % SW;
         if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(bars.empty_B(sb), ((bs / SB) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(bars.empty_W(sw), ((ws / SW) & 1) ^ 1, abort_flag)) { ok = false; break; }
         const uint32_t qs = sbase + OFF_Q + sl * Q_BYTES;
-        const uint32_t bt = sbase + OFF_B + sb * B_BYTES;
+        const uint32_t wt = sbase + OFF_W + sw * W_BYTES;
 #pragma unroll
         for (int r = 0; r < NT16 / 4; ++r) {
           const int i = dw + 4 * r;  // 16-row tile within the CTA's 128 rows
@@ -335,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int n = 16 * i + g + 8 * h;
-            const uint32_t row = bt + (n >> 3) * 1024 + (n & 7) * 128;
+            const uint32_t row = wt + (n >> 3) * 1024 + (n & 7) * 128;
             const uint4 lo = make_uint4(u[0][h], u[0][2 + h], u[1][h], u[1][2 + h]);
             const uint4 hi = make_uint4(u[2][h], u[2][2 + h], u[3][h], u[3][2 + h]);
             sts128(row + (((2 * t) ^ (n & 7)) << 4), lo);
@@ -347,17 +329,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // released by the MMA commit, which follows this arrival)
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) arrive_even(bars.full_B(sb), rank);
+        if (lane == 0) {
+          arrive_even(bars.full_W(sw), rank);
+          if (!SYM && ((kb + 1) % (4 * p.spg) == 0 || kb + 1 == p.nk)) mbar_arrive(bars.empty_S(cur));
+        }
         ++ls;
-        ++bs;
+        ++ws;
       }
     }
     if (!ok) give_up(abort_flag, peer_abort, p.err);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;          // TMEM lanes 32q .. 32q+31: x rows of this CTA
-    const int ch2 = (warp - 8) >> 2;  // D columns 128*ch2 .. +127: weight rows of CTA ch2
+    const int q = warp & 3;           // TMEM lanes 32q .. 32q+31: this CTA's weight rows
+    const int ch2 = (warp - 8) >> 2;  // D columns 128*ch2 .. +127: x rows of CTA ch2
+    const int wr = 32 * q + lane;     // weight row within the CTA's 128
+    // this row's scale in a scale block: tile wr/16, g = wr%8, half (wr/8)%2
+    const uint32_t soff = (uint32_t)((wr >> 4) * kScaleBlockBytes + (wr & 7) * 16 + ((wr >> 3) & 1) * 2);
     float acc[128];
     uint32_t gc = 0, sc = 0;
     int cur = 0;
@@ -369,28 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int gi = 0; gi < p.ng; ++gi) {
         if ((gi & 3) == 0) {
           cur = sc % SS;
-          if (!mbar_wait(bars.conv_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
           ++sc;
         }
+        const float s = __uint_as_float(lds16(sbase + OFF_RS + cur * RS_BYTES + soff + (gi & 3) * 4) << 16);
         const int b = gc & 1;
         if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t scp = sbase + OFF_SC + (cur * SC_FLOATS + (gi & 3) * BN + ch2 * HN) * 4;
+        const float2 s2 = make_float2(s, s);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float d[32];
-          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BN + ch2 * HN + ch * 32), d);
+          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BX + ch2 * HX + ch * 32), d);
 #pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const float4 s4 = lds128f(scp + (ch * 32 + c) * 4);
-            float2 a0 = make_float2(acc[ch * 32 + c], acc[ch * 32 + c + 1]);
-            float2 a1 = make_float2(acc[ch * 32 + c + 2], acc[ch * 32 + c + 3]);
-            a0 = __ffma2_rn(make_float2(s4.x, s4.y), make_float2(d[c], d[c + 1]), a0);
-            a1 = __ffma2_rn(make_float2(s4.z, s4.w), make_float2(d[c + 2], d[c + 3]), a1);
-            acc[ch * 32 + c] = a0.x;
-            acc[ch * 32 + c + 1] = a0.y;
-            acc[ch * 32 + c + 2] = a1.x;
-            acc[ch * 32 + c + 3] = a1.y;
+          for (int c = 0; c < 32; c += 2) {
+            float2 a = make_float2(acc[ch * 32 + c], acc[ch * 32 + c + 1]);
+            a = __ffma2_rn(s2, make_float2(d[c], d[c + 1]), a);
+            acc[ch * 32 + c] = a.x;
+            acc[ch * 32 + c + 1] = a.y;
           }
         }
         tc_fence_before();
@@ -402,57 +386,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gc;
       }
       if (!ok) break;
-      const int m = mt * BM + (int)rank * HM + 32 * q + lane;
-      if (m < p.M) {
-        uint16_t *yrow = p.y + (size_t)m * p.ld;
-        const bool vec = (p.ld & 7) == 0;
-        if (GATEUP) {
-          // columns 32pp + r (gate) and 32pp + 16 + r (up) of this half are rows
-          // 16 * (8 nt + 4 ch2 + pp) + r of the gate and up weights
+      // thread = one weight row, 128 x rows m0 + c
+      const int m0 = mt * BX + ch2 * HX;
+      if (GATEUP) {
+        // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows (16-row
+        // tiles alternate); lanes 0-15 form h for x rows c < 64, lanes 16-31
+        // for c >= 64, each taking the other operand from its partner lane
+        const bool gate = lane < 16;
+        const int n = 16 * (nt * (BW / 32) + (int)rank * (NT16 / 2) + q) + (lane & 15);
 #pragma unroll
-          for (int pp = 0; pp < 4; ++pp) {
-            const int n0 = 16 * (8 * nt + 4 * ch2 + pp);
-            float hv[16];
+        for (int c = 0; c < 64; ++c) {
+          const float mine = gate ? acc[c] : acc[c + 64];
+          const float other = __shfl_xor_sync(0xffffffffu, gate ? acc[c + 64] : acc[c], 16);
+          const float gv = gate ? mine : other, uv = gate ? other : mine;
+          const int m = m0 + c + (gate ? 0 : 64);
+          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
+        }
+      } else {
+        const int n = nt * BW + (int)rank * HW + wr;
+        if (n < p.N) {
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-              const float gv = acc[32 * pp + r], uv = acc[32 * pp + 16 + r];
-              hv[r] = gv / (1.0f + __expf(-gv)) * uv;
-            }
-            if (vec && n0 + 16 <= p.N) {
-              uint4 v0 = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]),
-                                    pack_bf16x2(hv[4], hv[5]), pack_bf16x2(hv[6], hv[7]));
-              uint4 v1 = make_uint4(pack_bf16x2(hv[8], hv[9]), pack_bf16x2(hv[10], hv[11]),
-                                    pack_bf16x2(hv[12], hv[13]), pack_bf16x2(hv[14], hv[15]));
-              *reinterpret_cast<uint4 *>(yrow + n0) = v0;
-              *reinterpret_cast<uint4 *>(yrow + n0 + 8) = v1;
-            } else {
-#pragma unroll
-              for (int r = 0; r < 16; ++r)
-                if (n0 + r < p.N) {
-                  __nv_bfloat16 bv = __float2bfloat16_rn(hv[r]);
-                  yrow[n0 + r] = *reinterpret_cast<uint16_t *>(&bv);
-                }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int c8 = 0; c8 < 16; ++c8) {
-            const int n0 = nt * BN + ch2 * HN + c8 * 8;
-            if (vec && n0 + 8 <= p.N) {
-              uint4 v = make_uint4(pack_bf16x2(acc[c8 * 8], acc[c8 * 8 + 1]),
-                                   pack_bf16x2(acc[c8 * 8 + 2], acc[c8 * 8 + 3]),
-                                   pack_bf16x2(acc[c8 * 8 + 4], acc[c8 * 8 + 5]),
-                                   pack_bf16x2(acc[c8 * 8 + 6], acc[c8 * 8 + 7]));
-              *reinterpret_cast<uint4 *>(yrow + n0) = v;
-            } else {
-#pragma unroll
-              for (int r = 0; r < 8; ++r)
-                if (n0 + r < p.N) {
-                  __nv_bfloat16 bv = __float2bfloat16_rn(acc[c8 * 8 + r]);
-                  yrow[n0 + r] = *reinterpret_cast<uint16_t *>(&bv);
-                }
-            }
-          }
+          for (int c = 0; c < 128; ++c)
+            if (m0 + c < p.M) p.y[(size_t)(m0 + c) * p.ld + n] = bf16_bits(acc[c]);
         }
       }
     }
@@ -538,11 +493,11 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(rows, c.K, c.group, c.sym);
   CUtensorMap tx, tq, ts, tz;
   bool ok = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, (uint64_t)c.K, (uint64_t)c.M,
-                      (uint64_t)c.K * 2, BK, HM, CU_TENSOR_MAP_SWIZZLE_128B);
+                      (uint64_t)c.K * 2, BK, HX, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.codes_off, (uint64_t)L.chunks * 128,
                        (uint64_t)L.tiles, (uint64_t)L.chunks * kChunkBytes, 128, NT16, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.scales_off, (uint64_t)L.gblocks * 32,
-                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, PT16,
+                       (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, NT16,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (c.sym) {
     tz = ts;  // unused
@@ -558,8 +513,8 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   p.N = c.N;
   p.K = c.K;
   p.ld = c.N;
-  p.mtiles = (c.M + BM - 1) / BM;
-  p.ntiles = (rows + BN - 1) / BN;
+  p.mtiles = (c.M + BX - 1) / BX;
+  p.ntiles = (rows + BW - 1) / BW;
   p.nk = c.K / BK;
   p.ng = c.K / c.group;
   p.spg = c.group / BK;

@@ -95,7 +95,6 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return *reinterpret_cast<uint16_t *>(&b);
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
 
 // 1-D bulk copy global -> shared, completion counted on `bar`; the weights are
 // read once, so they are marked first to leave L2.

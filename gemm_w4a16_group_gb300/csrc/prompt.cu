@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float other = __shfl_xor_sync(0xffffffffu, gate ? acc[c + 64] : acc[c], 16);
           const float gv = gate ? mine : other, uv = gate ? other : mine;
           const int m = m0 + c + (gate ? 0 : 64);
-          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
+          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(silu_f32(gv) * uv);
         }
       } else {
         const int n = nt * BW + (int)rank * HW + wr;

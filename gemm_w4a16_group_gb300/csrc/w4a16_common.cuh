@@ -158,6 +158,13 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
+// SiLU(g) = g / (1 + e^-g) with the fast exponential and division: a few
+// float32 ulps, far inside the output's bf16 rounding (the IEEE division is a
+// long instruction sequence that stalled the prompt GEMM's per-tile output
+// phase for ~12 us). When e^-g overflows (g < -88) the quotient is 0, the
+// function's limit.
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 __device__ __forceinline__ uint32_t lds16(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));

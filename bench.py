@@ -197,59 +197,87 @@ def run_cuda(args, rank, world):
         del pt["p"]
     torch.cuda.synchronize()
 
+    # Device time comes from CUDA-graph replays: a decode server launches its
+    # steps from graphs, and an eager Python loop would time the host's launch
+    # path instead of the kernels (a decode call is ~10-30 us of device work).
+    s = torch.cuda.Stream(device=dev) if not args.eager else stream
+
     def call(pt, c, x=None, y=None):
         w = pt["w"]
         fn = w4.gateup_silu if w["kind"] == "gateup" else w4.gemm
         fn(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"],
-           out=pt["y"] if y is None else y, stream=stream)
+           out=pt["y"] if y is None else y, stream=s)
+
+    def steps(first, n, only=None):
+        for i in range(n):
+            for j, pt in enumerate(parts):
+                if only is None or j == only:
+                    call(pt, (first + i) % copies)
+
+    def capture(first, n, only=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            steps(first, n, only)
+        return g
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        a.record(s)
+        fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return a.elapsed_time(b)
 
     nsteps, nwarm = args.steps, args.warmup
-    # events around every call: per-launch durations of the dominant call
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in parts] for _ in range(nsteps)]
-    for i in range(nwarm):
-        for pt in parts:
-            call(pt, i % copies)
+    with torch.cuda.stream(s):
+        steps(0, nwarm)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    if args.eager:
+        run_all = lambda: steps(nwarm, nsteps)  # noqa: E731
+        run_part = [lambda j=j: steps(nwarm, nsteps, j) for j in range(len(parts))]
+    else:
+        g_all = capture(nwarm, nsteps)
+        g_part = [capture(nwarm, nsteps, j) for j in range(len(parts))]
+        for g in [g_all] + g_part:  # upload and run each graph once, untimed
+            with torch.cuda.stream(s):
+                g.replay()
+        run_all = g_all.replay
+        run_part = [g.replay for g in g_part]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)
     t_begin = time.time()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    start.record(stream)
-    for i in range(nsteps):
-        for j, pt in enumerate(parts):
-            ev[i][j][0].record(stream)
-            call(pt, (nwarm + i) % copies)
-            ev[i][j][1].record(stream)
-    stop.record(stream)
-    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        ms = timed(run_all)
+        # per-launch duration of each call: the same launches of that call alone
+        per_call_ms = [timed(run_part[j]) / nsteps for j in range(len(parts))]
     t_end = time.time()
     if w4.kernel_status() != 0:
         raise RuntimeError("a kernel's bounded wait gave up during the timed region")
-    ms = start.elapsed_time(stop)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
         torch.distributed.barrier()
-    per_call_ms = [float(np.mean([ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(nsteps)]))
-                   for j in range(len(parts))]
 
-    # end to end: pinned host x -> device, the calls, device y -> pinned host, every step
+    # end to end, eager through the public API: pinned host x -> device, the
+    # calls, device y -> pinned host, every step
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     xd = [torch.empty_like(pt["x"]) for pt in parts]
     torch.cuda.synchronize()
-    e_start.record(stream)
-    for i in range(nsteps):
-        for j, pt in enumerate(parts):
-            xd[j].copy_(pt["x_host"].view(pt["x"].dtype), non_blocking=True)
-            call(pt, (nwarm + nsteps + i) % copies, x=xd[j])
-            pt["y_host"].copy_(pt["y"].view(torch.int16), non_blocking=True)
-    e_stop.record(stream)
+    with torch.cuda.stream(s):
+        e_start.record(s)
+        for i in range(nsteps):
+            for j, pt in enumerate(parts):
+                xd[j].copy_(pt["x_host"].view(pt["x"].dtype), non_blocking=True)
+                call(pt, (nwarm + nsteps + i) % copies, x=xd[j])
+                pt["y_host"].copy_(pt["y"].view(torch.int16), non_blocking=True)
+        e_stop.record(s)
     torch.cuda.synchronize()
     sampler.stop()
     e2e_ms = e_start.elapsed_time(e_stop)
@@ -280,7 +308,8 @@ def run_cuda(args, rank, world):
         "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
                    "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
-                   "parallelism": f"replicas x{world}", "per_call_ms": [round(v, 5) for v in per_call_ms]},
+                   "parallelism": f"replicas x{world}", "launch": "eager" if args.eager else "cuda graph",
+                   "per_call_ms": [round(v, 5) for v in per_call_ms]},
         "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
                      "achieved": round(achieved, 2), "peak": peak, "unit": d["unit"],
                      "frac": round(achieved / peak, 4), "traffic": stored_traffic(d["name"]),
@@ -364,6 +393,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT,
                     help=f"{DEFAULT} (default), one of {sorted(WORKLOADS)}, or shape:M,N,K,G,sym|asym")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the timed steps from Python instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],

@@ -19,8 +19,8 @@ std::atomic<int> g_override{0};
 // Device error word set by kernels whose bounded waits gave up.
 __device__ int g_kernel_error;
 
-constexpr int kMaxDevices = 64;
 struct DeviceInfo {
+  int device = 0;
   bool ready = false;
   int status = W4A16_OK;
   int sm_count = 0;
@@ -57,6 +57,7 @@ int current_device(DeviceInfo &out) {
       d.sm_count = sms;
       d.status = W4A16_OK;
     }
+    d.device = dev;
     d.ready = true;
   }
   out = d;
@@ -134,7 +135,7 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
   int st = current_device(d);
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false,
-             reinterpret_cast<cudaStream_t>(stream), d.err};
+             reinterpret_cast<cudaStream_t>(stream), d.err, d.device};
   // M <= 16: the tensor-core decode kernel (measured faster than the CUDA-core
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
   const int ov = g_override.load();
@@ -153,7 +154,7 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
   int st = current_device(d);
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym ? 1 : 0, true,
-             reinterpret_cast<cudaStream_t>(stream), d.err};
+             reinterpret_cast<cudaStream_t>(stream), d.err, d.device};
   if (M <= 16 && g_override.load() != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }

@@ -57,6 +57,7 @@ struct DecodeParams {
   int tiles, chunks, groups, gblocks, units;
   int ld;                  // y row stride in elements
   int *err;
+  int device;              // host side only: ordinal for the per-device caches
   UnpackConsts uc;
 };
 
@@ -304,6 +305,17 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[i][mt][r] = 0.f;
 
+  // x is loaded one 64-wide chunk ahead of its use (xn), so the load latency
+  // overlaps the previous chunk's unpack and MMAs
+  uint4 xn[MT][2];
+  {
+    const int c0 = min(kUnitChunks * ub, p.chunks - 1);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      xn[mt][0] = ldg_keep(xp[mt] + (size_t)c0 * 8);
+      xn[mt][1] = ldg_keep(xp[mt] + (size_t)c0 * 8 + 1);
+    }
+  }
   int it = 0;
   for (; it < nu; ++it) {
     const int u = ub + it;
@@ -331,10 +343,13 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
           const int cl = j * CPG + cc;  // chunk within the unit
           const int c = kUnitChunks * u + cl;
           uint4 xx[MT][2];
+          const int cn = min(c + 1, p.chunks - 1);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            xx[mt][0] = ldg_keep(xp[mt] + (size_t)c * 8);
-            xx[mt][1] = ldg_keep(xp[mt] + (size_t)c * 8 + 1);
+            xx[mt][0] = xn[mt][0];
+            xx[mt][1] = xn[mt][1];
+            xn[mt][0] = ldg_keep(xp[mt] + (size_t)cn * 8);
+            xn[mt][1] = ldg_keep(xp[mt] + (size_t)cn * 8 + 1);
           }
           uint4 w[TPW];
 #pragma unroll
@@ -580,15 +595,19 @@ struct DecodeCfg {
 // two K units per warp. Measured: splitting a 1.2-wave grid four ways to even
 // out the waves made it slower (each warp's first slot latency dominates).
 template <typename Kern>
-cudaError_t pick_cfg(Kern kern, int smem, int tiles, int units, int sm_count, int tpw, DecodeCfg &c) {
+cudaError_t pick_cfg(Kern kern, int smem, int tiles, int units, int sm_count, int tpw, int device,
+                     PerDevice &occ_cache, DecodeCfg &c) {
   c.tpw = tpw;
   c.smem = smem;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   const long long ctas = (tiles + tpw - 1) / tpw;
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * kWarps, smem) != cudaSuccess || occ < 1)
-    occ = 1;
+  int occ = occ_cache.v[device].load(std::memory_order_relaxed);
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * kWarps, smem) != cudaSuccess || occ < 1)
+      occ = 1;
+    occ_cache.v[device].store(occ, std::memory_order_relaxed);
+  }
   const long long resident = (long long)occ * sm_count;
   c.kc = 1;
   while (c.kc < 8 && ctas * c.kc * 2 <= resident && units >= kWarps * c.kc * 4) c.kc *= 2;
@@ -634,6 +653,7 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
   p.units = (L.chunks + kUnitChunks - 1) / kUnitChunks;
   p.ld = c.N;
   p.err = c.err;
+  p.device = c.device;
   p.uc = host_unpack_consts();
   return p;
 }
@@ -644,19 +664,18 @@ template <int MT, int TPW, bool SYM, int CPG, bool GATEUP>
 cudaError_t run_mma(const DecodeParams &p, int sm_count, cudaStream_t s) {
   constexpr int SLOTS = slots_for(TPW);
   auto kern = smallm_mma_kernel<MT, TPW, SYM, CPG, SLOTS, GATEUP>;
+  static PerDevice occ;
   DecodeCfg cfg;
   cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * MT * 4 * 32>::kBytes, p.tiles, p.units,
-                           sm_count, TPW, cfg);
+                           sm_count, TPW, p.device, occ, cfg);
   return e != cudaSuccess ? e : launch_decode(kern, p, cfg, s);
 }
 
-// Tiles per warp: four when the grid still fills the GPU several times over
-// (fewer per-slot overheads per packed word), else two.
+// Two 16-row tiles per warp at every N (measured faster than four at the
+// 248,320-row head: more resident warps per SM).
 template <bool SYM, int CPG, bool GATEUP>
 cudaError_t run_mma_m(const DecodeParams &p, int sm_count, cudaStream_t s) {
-  const bool wide = p.tiles >= 4 * 8 * sm_count;
-  if (p.M <= 8)
-    return wide ? run_mma<1, 4, SYM, CPG, GATEUP>(p, sm_count, s) : run_mma<1, 2, SYM, CPG, GATEUP>(p, sm_count, s);
+  if (p.M <= 8) return run_mma<1, 2, SYM, CPG, GATEUP>(p, sm_count, s);
   return run_mma<2, 2, SYM, CPG, GATEUP>(p, sm_count, s);
 }
 
@@ -671,9 +690,10 @@ template <bool SYM, int CPG>
 cudaError_t run_gemv(const DecodeParams &p, int sm_count, cudaStream_t s) {
   constexpr int TPW = 2, SLOTS = slots_for(TPW);
   auto kern = gemv_m1_kernel<TPW, SYM, CPG, SLOTS>;
+  static PerDevice occ;
   DecodeCfg cfg;
-  cudaError_t e =
-      pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * 16>::kBytes, p.tiles, p.units, sm_count, TPW, cfg);
+  cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * 16>::kBytes, p.tiles, p.units, sm_count, TPW,
+                           p.device, occ, cfg);
   return e != cudaSuccess ? e : launch_decode(kern, p, cfg, s);
 }
 

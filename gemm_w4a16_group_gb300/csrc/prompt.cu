@@ -456,7 +456,8 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 // once (found once per instantiation), each walking the tiles with a stride.
 template <bool SYM, bool GATEUP>
 cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
-                           const CUtensorMap &tz, const PromptParams &p, int ntot, cudaStream_t s) {
+                           const CUtensorMap &tz, const PromptParams &p, int ntot, int device,
+                           cudaStream_t s) {
   auto kern = prompt_tc_kernel<SYM, GATEUP>;
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(kThreads, 1, 1);
@@ -469,18 +470,18 @@ cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const C
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  static int max_pairs = 0;  // per instantiation (one device type: sm_103a)
-  if (max_pairs == 0) {
+  static PerDevice max_pairs;  // clusters of this kernel that fit at once, per device
+  int np = max_pairs.v[device].load(std::memory_order_relaxed);
+  if (np == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     lc.gridDim = dim3(2, 1, 1);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &lc);
+    e = cudaOccupancyMaxActiveClusters(&np, kern, &lc);
     if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_pairs = n;
+    if (np < 1) return cudaErrorInvalidConfiguration;
+    max_pairs.v[device].store(np, std::memory_order_relaxed);
   }
-  const int pairs = ntot < max_pairs ? ntot : max_pairs;
+  const int pairs = ntot < np ? ntot : np;
   lc.gridDim = dim3(2 * pairs, 1, 1);
   return cudaLaunchKernelEx(&lc, kern, tx, tq, ts, tz, p);
 }
@@ -522,11 +523,11 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;
   if (c.sym) {
-    return c.gateup ? launch_variant<true, true>(tx, tq, ts, tz, p, ntot, c.stream)
-                    : launch_variant<true, false>(tx, tq, ts, tz, p, ntot, c.stream);
+    return c.gateup ? launch_variant<true, true>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
+                    : launch_variant<true, false>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
   }
-  return c.gateup ? launch_variant<false, true>(tx, tq, ts, tz, p, ntot, c.stream)
-                  : launch_variant<false, false>(tx, tq, ts, tz, p, ntot, c.stream);
+  return c.gateup ? launch_variant<false, true>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
+                  : launch_variant<false, false>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
 }
 
 }  // namespace w4a16

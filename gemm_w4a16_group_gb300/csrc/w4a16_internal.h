@@ -1,12 +1,23 @@
 // Internal launcher interface between the C-ABI layer and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "w4a16_common.cuh"
 
 namespace w4a16 {
+
+constexpr int kMaxDevices = 64;
+
+// A per-device fact about one kernel that is found once and then reused on
+// every call (the dynamic shared-memory opt-in is a per-device function
+// attribute; the occupancy query is slow next to a decode launch). 0 = not
+// found yet on that device; racing first calls store the same value.
+struct PerDevice {
+  std::atomic<int> v[kMaxDevices];
+};
 
 // One matmul call as the kernels see it. For the fused gate/up form,
 // N is the rows of ONE of the two weights (N_each), `packed` the interleaved
@@ -18,7 +29,8 @@ struct GemmCall {
   int M, N, K, group, sym;
   bool gateup;
   cudaStream_t stream;
-  int *err;  // device error word (bounded waits that gave up)
+  int *err;    // device error word (bounded waits that gave up)
+  int device;  // current device ordinal, < kMaxDevices
 };
 
 // Rows covered by the packed buffer of a call (padded; interleaved for gate/up).

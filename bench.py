@@ -164,6 +164,9 @@ def run_cuda(args, rank, world):
     stream = torch.cuda.current_stream()
     w4.lib()
     w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3}[args.kernel])
+    # decode calls stream their (read-only, already complete) weights while
+    # the previous kernel finishes; x and y wait for it
+    w4.set_programmatic_overlap(not args.no_overlap)
     peaks = load_peaks()
 
     def up(a):
@@ -308,7 +311,8 @@ def run_cuda(args, rank, world):
         "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
                    "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
-                   "parallelism": f"replicas x{world}", "launch": "eager" if args.eager else "cuda graph",
+                   "parallelism": f"replicas x{world}", "launch": ("eager" if args.eager else "cuda graph")
+                   + ("" if args.no_overlap else ", programmatic overlap"),
                    "per_call_ms": [round(v, 5) for v in per_call_ms]},
         "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
                      "achieved": round(achieved, 2), "peak": peak, "unit": d["unit"],
@@ -394,6 +398,7 @@ def main():
                     help=f"{DEFAULT} (default), one of {sorted(WORKLOADS)}, or shape:M,N,K,G,sym|asym")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps from Python instead of a CUDA graph")
+    ap.add_argument("--no-overlap", action="store_true", help="no programmatic overlap between decode calls")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],

@@ -20,7 +20,7 @@ from . import build as _build
 __all__ = [
     "EXPORTS", "W4A16Error", "lib", "library_path", "repacked_bytes", "gateup_repacked_bytes",
     "repack", "repack_gateup", "gemm", "gateup_silu", "dequantize", "kernel_status",
-    "set_kernel_override", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
+    "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
 ]
 
 # symbols declared in include/w4a16.h
@@ -28,6 +28,7 @@ EXPORTS = (
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_gateup_repacked_bytes", "w4a16_repack_gateup",
     "w4a16_gemm", "w4a16_gateup_silu", "w4a16_dequantize", "w4a16_kernel_status",
     "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
+    "w4a16_set_programmatic_overlap",
 )
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC = 0, 1, 2, 3
 
@@ -80,6 +81,8 @@ def lib(auto_build: bool = True) -> ctypes.CDLL:
     L.w4a16_last_cuda_error.restype = i32
     L.w4a16_set_kernel_override.argtypes = [i32]
     L.w4a16_set_kernel_override.restype = i32
+    L.w4a16_set_programmatic_overlap.argtypes = [i32]
+    L.w4a16_set_programmatic_overlap.restype = i32
     _lib = L
     return L
 
@@ -209,3 +212,14 @@ def kernel_status() -> int:
 
 def set_kernel_override(which: int) -> int:
     return int(lib().w4a16_set_kernel_override(which))
+
+
+def set_programmatic_overlap(on: bool) -> bool:
+    """Let each M <= 16 call start streaming its weights while the previous
+    kernel on the stream finishes (x and y are touched only after it has).
+    Only while packed weights are read-only and complete; returns the previous
+    setting."""
+    prev = int(lib().w4a16_set_programmatic_overlap(int(bool(on))))
+    if prev < 0:
+        raise W4A16Error("w4a16_set_programmatic_overlap: bad value")
+    return bool(prev)

@@ -15,6 +15,7 @@ namespace {
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_override{0};
+std::atomic<int> g_overlap{0};
 
 // Device error word set by kernels whose bounded waits gave up.
 __device__ int g_kernel_error;
@@ -135,7 +136,7 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
   int st = current_device(d);
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false,
-             reinterpret_cast<cudaStream_t>(stream), d.err, d.device};
+             reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
   // M <= 16: the tensor-core decode kernel (measured faster than the CUDA-core
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
   const int ov = g_override.load();
@@ -154,7 +155,7 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
   int st = current_device(d);
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym ? 1 : 0, true,
-             reinterpret_cast<cudaStream_t>(stream), d.err, d.device};
+             reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
   if (M <= 16 && g_override.load() != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
@@ -205,6 +206,11 @@ int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
 int w4a16_set_kernel_override(int which) {
   if (which < 0 || which > 3) return -1;
   return g_override.exchange(which);
+}
+
+int w4a16_set_programmatic_overlap(int on) {
+  if (on != 0 && on != 1) return -1;
+  return g_overlap.exchange(on);
 }
 
 }  // extern "C"

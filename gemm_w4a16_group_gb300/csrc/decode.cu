@@ -45,7 +45,11 @@ constexpr int kWarps = 4;       // warps per CTA
 #ifndef W4A16_DECODE_SLOTS2
 #define W4A16_DECODE_SLOTS2 2
 #endif
-constexpr int kUnitChunks = 4;  // 64-wide K chunks per ring slot (256 k)
+#ifndef W4A16_UNIT_CHUNKS
+#define W4A16_UNIT_CHUNKS 4
+#endif
+constexpr int kUnitChunks = W4A16_UNIT_CHUNKS;  // 64-wide K chunks per ring slot
+static_assert(kUnitChunks == 2 || kUnitChunks == 4, "a unit is 128 or 256 k");
 
 struct DecodeParams {
   const uint16_t *x;
@@ -58,6 +62,7 @@ struct DecodeParams {
   int ld;                  // y row stride in elements
   int *err;
   int device;              // host side only: ordinal for the per-device caches
+  bool overlap;            // host side only: launch with programmatic stream serialization
   UnpackConsts uc;
 };
 
@@ -131,58 +136,68 @@ __device__ __forceinline__ void k_slice(int units, int &u0, int &u1) {
 // ---------------------------------------------------------------------------
 template <int TPW, bool SYM, int SLOTS>
 struct Ring {
-  static constexpr int kTileCode = kUnitChunks * kChunkBytes;  // 2048
+  static constexpr int kTileCode = kUnitChunks * kChunkBytes;
   static constexpr int kScaleOff = TPW * kTileCode;
   static constexpr int kZeroOff = kScaleOff + TPW * kScaleBlockBytes;
   static constexpr int kSlotBytes = kZeroOff + (SYM ? 0 : TPW * kZeroBlockBytes);
   static constexpr int kWarpBytes = SLOTS * kSlotBytes;
+  // one bulk copy per lane: codes of each tile, then its scale block, then its
+  // zero block (asymmetric)
+  static constexpr int kCopies = TPW * (SYM ? 2 : 3);
 
-  uint8_t *base;   // this warp's slots (generic address)
-  uint32_t sbase;  // same, shared-window address
+  uint32_t sbase;  // this warp's slots, shared-window address
   uint32_t bar0;   // SLOTS mbarriers, 8 bytes apart
-  const uint8_t *codes[TPW];
-  const uint8_t *scales[TPW];
-  const uint8_t *zeros[TPW];
+  // this lane's copy (lanes >= kCopies issue none)
+  const uint8_t *src;  // source of the copy for unit 0 / scale block 0
+  uint32_t stride;     // source step per unit (codes) or per scale block
+  uint32_t dst_off;    // offset inside a slot
+  bool is_code;
   uint64_t policy;
-  int chunks, upb;  // chunks per tile, units per scale block (1 or 2)
+  int chunks, upb;  // chunks per tile, units per scale block
 
   __device__ void setup(const DecodeParams &p, uint8_t *warp_base, uint64_t *warp_bars, int tile0, int cpg) {
-    base = warp_base;
+    const int lane = threadIdx.x & 31;
     sbase = smem_u32(warp_base);
     bar0 = smem_u32(warp_bars);
     chunks = p.chunks;
-    upb = cpg;  // a block of four groups spans 4 * cpg chunks = cpg units
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      const int tile = min(tile0 + i, p.tiles - 1);
-      codes[i] = p.codes + (size_t)tile * p.chunks * kChunkBytes;
-      scales[i] = p.scales + (size_t)tile * p.gblocks * kScaleBlockBytes;
-      zeros[i] = p.zeros + (size_t)tile * p.gblocks * kZeroBlockBytes;
+    upb = 4 * cpg / kUnitChunks;  // a block of four groups spans 4 * cpg chunks
+    const int kind = lane / TPW, i = lane % TPW;
+    const size_t tile = (size_t)min(tile0 + i, p.tiles - 1);
+    is_code = kind == 0;
+    if (kind == 0) {
+      src = p.codes + tile * p.chunks * kChunkBytes;
+      stride = kTileCode;
+      dst_off = i * kTileCode;
+    } else if (kind == 1) {
+      src = p.scales + tile * p.gblocks * kScaleBlockBytes;
+      stride = kScaleBlockBytes;
+      dst_off = kScaleOff + i * kScaleBlockBytes;
+    } else {
+      src = p.zeros + tile * p.gblocks * kZeroBlockBytes;
+      stride = kZeroBlockBytes;
+      dst_off = kZeroOff + i * kZeroBlockBytes;
     }
-    policy = 0;
-    if ((threadIdx.x & 31) == 0) {
+    policy = evict_first_policy();
+    if (lane == 0) {
       for (int s = 0; s < SLOTS; ++s) mbar_init(bar0 + 8 * s, 1);
       fence_mbar_init();
-      policy = evict_first_policy();
     }
     __syncwarp();
   }
 
-  // lane 0: copy unit u into slot s
+  // The whole warp: copy unit u into slot s. Lane q < kCopies issues copy q
+  // and lane 0 posts the expected bytes with the slot's one arrival, so a copy
+  // that lands before that arrival cannot complete the phase.
   __device__ void issue(int s, int u) {
+    const int lane = threadIdx.x & 31;
     const uint32_t bar = bar0 + 8 * s;
-    const uint32_t dst = sbase + s * kSlotBytes;
     const int nch = min(kUnitChunks, chunks - kUnitChunks * u);
-    const int blk = u / upb;
-    mbar_arrive_expect_tx(bar, TPW * (nch * kChunkBytes + kScaleBlockBytes + (SYM ? 0 : kZeroBlockBytes)));
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      bulk_copy(dst + i * kTileCode, codes[i] + (size_t)u * kTileCode, nch * kChunkBytes, bar, policy);
-      bulk_copy(dst + kScaleOff + i * kScaleBlockBytes, scales[i] + (size_t)blk * kScaleBlockBytes,
-                kScaleBlockBytes, bar, policy);
-      if (!SYM)
-        bulk_copy(dst + kZeroOff + i * kZeroBlockBytes, zeros[i] + (size_t)blk * kZeroBlockBytes, kZeroBlockBytes,
-                  bar, policy);
+    if (lane == 0)
+      mbar_arrive_expect_tx(bar, TPW * (nch * kChunkBytes + kScaleBlockBytes + (SYM ? 0 : kZeroBlockBytes)));
+    if (lane < kCopies) {
+      const uint32_t bytes = is_code ? (uint32_t)(nch * kChunkBytes) : stride;
+      const size_t step = is_code ? (size_t)u : (size_t)(u / upb);
+      bulk_copy(sbase + s * kSlotBytes + dst_off, src + step * stride, bytes, bar, policy);
     }
   }
 
@@ -286,9 +301,12 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
   R ring;
   ring.setup(p, smem + SM::kRingOff + warp * R::kWarpBytes,
              reinterpret_cast<uint64_t *>(smem + SM::kBarOff) + warp * SLOTS, tile0, CPG);
-  int issued = 0;
-  if (lane == 0)
-    for (; issued < SLOTS && issued < nu; ++issued) ring.issue(issued, ub + issued);
+  int issued = 0;  // warp-uniform
+  for (; issued < SLOTS && issued < nu; ++issued) ring.issue(issued, ub + issued);
+  // the weights are in flight; x and y belong to the previous kernel until it
+  // has finished (programmatic overlap), and the next call may be scheduled
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   // B fragment column g + 8 mt reads x row min(g + 8 mt, M - 1): columns past M
   // compute duplicates that are never stored
@@ -394,7 +412,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
     }
     // every lane has consumed the slot: refill it with the unit SLOTS ahead
     __syncwarp();
-    if (lane == 0 && issued < nu) {
+    if (issued < nu) {
       fence_proxy_async_smem();
       ring.issue(it % SLOTS, ub + issued);
       ++issued;
@@ -459,9 +477,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
   R ring;
   ring.setup(p, smem + SM::kRingOff + warp * R::kWarpBytes,
              reinterpret_cast<uint64_t *>(smem + SM::kBarOff) + warp * SLOTS, tile0, CPG);
-  int issued = 0;
-  if (lane == 0)
-    for (; issued < SLOTS && issued < nu; ++issued) ring.issue(issued, ub + issued);
+  int issued = 0;  // warp-uniform
+  for (; issued < SLOTS && issued < nu; ++issued) ring.issue(issued, ub + issued);
+  grid_launch_dependents();
+  grid_dependency_wait();
   const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + 16 * t);
 
   float out[TPW][2];
@@ -550,7 +569,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
       }
     }
     __syncwarp();
-    if (lane == 0 && issued < nu) {
+    if (issued < nu) {
       fence_proxy_async_smem();
       ring.issue(it % SLOTS, ub + issued);
       ++issued;
@@ -622,14 +641,19 @@ cudaError_t launch_decode(Kern kern, const DecodeParams &prm, const DecodeCfg &c
   lc.blockDim = dim3(32 * kWarps, 1, 1);
   lc.dynamicSmemBytes = cfg.smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int na = 0;
   if (cfg.kc > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = cfg.kc;
-    attr[0].val.clusterDim.z = 1;
-    na = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = cfg.kc;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (prm.overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
   lc.attrs = attr;
   lc.numAttrs = na;
@@ -654,6 +678,7 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
   p.ld = c.N;
   p.err = c.err;
   p.device = c.device;
+  p.overlap = c.overlap;
   p.uc = host_unpack_consts();
   return p;
 }

@@ -134,6 +134,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. wait: block until the grids this one depends
+// on (the previous kernel on the stream, when launched with programmatic
+// stream serialization) have completed and their writes are visible; returns
+// at once otherwise. launch_dependents: the next such kernel may be scheduled
+// once every CTA of this grid has executed it (or exited).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

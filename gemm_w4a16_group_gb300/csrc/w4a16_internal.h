@@ -31,6 +31,7 @@ struct GemmCall {
   cudaStream_t stream;
   int *err;    // device error word (bounded waits that gave up)
   int device;  // current device ordinal, < kMaxDevices
+  bool overlap;  // programmatic overlap with the previous kernel (M <= 16 kernels)
 };
 
 // Rows covered by the packed buffer of a call (padded; interleaved for gate/up).

@@ -151,6 +151,25 @@ int w4a16_last_cuda_error(void);
  */
 int w4a16_set_kernel_override(int which);
 
+/*
+ * Programmatic overlap of consecutive decode calls (M <= 16), off by default.
+ * When on, the M <= 16 kernels are launched with programmatic stream
+ * serialization: a call may start while the previous kernel on its stream is
+ * still running, begin streaming its packed weights (and scales and zeros)
+ * at once, and wait for that kernel to finish (and its writes to become
+ * visible) before it reads x or writes y / h. This hides each call's launch
+ * and weight-fetch ramp behind the tail of the call before it, the common
+ * case of decode layers run back to back (also inside CUDA graphs).
+ * Turn it on only while the packed buffers are read-only: written once (at
+ * load time, e.g. by w4a16_repack), then made complete by a synchronization
+ * (cudaStreamSynchronize or an event the stream waits on) before the first
+ * call that uses them, because the weight reads of a call are not ordered
+ * after kernels still in flight on its stream. Process-wide; the setting is
+ * read when a call is launched. Returns the previous setting (0 or 1), or -1
+ * for a value other than 0 or 1.
+ */
+int w4a16_set_programmatic_overlap(int on);
+
 #ifdef __cplusplus
 }
 #endif

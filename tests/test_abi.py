@@ -97,3 +97,12 @@ def test_strerror_and_override(L):
     prev = w4.set_kernel_override(w4.KERNEL_SMALLM)
     assert w4.set_kernel_override(prev) == w4.KERNEL_SMALLM
     assert w4.set_kernel_override(7) == -1
+
+
+def test_programmatic_overlap_switch(L):
+    assert L.w4a16_set_programmatic_overlap(2) == -1
+    prev = L.w4a16_set_programmatic_overlap(1)
+    assert prev in (0, 1)
+    assert L.w4a16_set_programmatic_overlap(prev) == 1
+    assert w4.set_programmatic_overlap(False) == bool(prev)
+    assert w4.set_programmatic_overlap(prev) is False

@@ -178,6 +178,8 @@ def run_cuda(args, rank, world):
         p = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
                                x_scale=w["x_scale"], seed=0, gateup=w["kind"] == "gateup")
         units, unit, is_flops = part_units(w)
+        if args.argmax and not is_flops:
+            units -= 2 * w["M"] * w["N"]  # no logits written
         wbytes = algorithmic_bytes(1, w["N"], w["K"], w["group"], w["sym"]) * (2 if w["kind"] == "gateup" else 1)
         parts.append(dict(name=name, w=w, p=p, units=units, unit=unit, is_flops=is_flops, wbytes=wbytes))
     # weight copies to rotate through so that L2 never holds the next call's weights
@@ -195,6 +197,8 @@ def run_cuda(args, rank, world):
         pt["packed"] = [packed] + [packed.clone() for _ in range(copies - 1)]
         pt["x"] = up(p["x"])
         pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+        pt["idx"] = torch.empty(w["M"], dtype=torch.int64, device=dev)
+        pt["idx_host"] = torch.empty(w["M"], dtype=torch.int64).pin_memory()
         pt["x_host"] = torch.from_numpy(p["x"].view(np.int16)).pin_memory()
         pt["y_host"] = torch.empty((w["M"], w["N"]), dtype=torch.int16).pin_memory()
         del pt["p"]
@@ -207,6 +211,11 @@ def run_cuda(args, rank, world):
 
     def call(pt, c, x=None, y=None):
         w = pt["w"]
+        if args.argmax and w["kind"] != "gateup":
+            # the greedy pick only: the logits are not stored
+            idx, _ = w4.gemm_argmax(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"],
+                                    w["sym"], stream=s, index_out=pt["idx"])
+            return
         fn = w4.gateup_silu if w["kind"] == "gateup" else w4.gemm
         fn(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"],
            out=pt["y"] if y is None else y, stream=s)
@@ -279,7 +288,10 @@ def run_cuda(args, rank, world):
             for j, pt in enumerate(parts):
                 xd[j].copy_(pt["x_host"].view(pt["x"].dtype), non_blocking=True)
                 call(pt, (nwarm + nsteps + i) % copies, x=xd[j])
-                pt["y_host"].copy_(pt["y"].view(torch.int16), non_blocking=True)
+                if args.argmax and pt["w"]["kind"] != "gateup":
+                    pt["idx_host"].copy_(pt["idx"], non_blocking=True)
+                else:
+                    pt["y_host"].copy_(pt["y"].view(torch.int16), non_blocking=True)
         e_stop.record(s)
     torch.cuda.synchronize()
     sampler.stop()
@@ -302,7 +314,8 @@ def run_cuda(args, rank, world):
     peak = peaks["bf16_tflops"] if is_flops else peaks["hbm_gbs"]
     clocks = sampler.summary(t_begin, t_end)
     h2d = sum(pt["x"].numel() * 2 for pt in parts)
-    d2h = sum(pt["y"].numel() * 2 for pt in parts)
+    d2h = sum(pt["idx"].numel() * 8 if args.argmax and pt["w"]["kind"] != "gateup" else pt["y"].numel() * 2
+              for pt in parts)
     line = {
         "metric": metric_name(args.workload), "value": round(value, 2), "unit": parts[0]["unit"],
         "n_gpus": world, "steps": nsteps, "warmup": nwarm, "ms_per_step": ms / nsteps,
@@ -311,7 +324,7 @@ def run_cuda(args, rank, world):
         "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
                    "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
-                   "parallelism": f"replicas x{world}", "launch": ("eager" if args.eager else "cuda graph")
+                   "parallelism": f"replicas x{world}", "output": "argmax" if args.argmax else "y", "launch": ("eager" if args.eager else "cuda graph")
                    + ("" if args.no_overlap else ", programmatic overlap"),
                    "per_call_ms": [round(v, 5) for v in per_call_ms]},
         "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
@@ -399,6 +412,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps from Python instead of a CUDA graph")
     ap.add_argument("--no-overlap", action="store_true", help="no programmatic overlap between decode calls")
+    ap.add_argument("--argmax", action="store_true",
+                    help="time the fused argmax (w4a16_gemm_argmax, no logits stored) instead of the GEMM")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],

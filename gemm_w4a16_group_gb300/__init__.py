@@ -19,14 +19,14 @@ from . import build as _build
 
 __all__ = [
     "EXPORTS", "W4A16Error", "lib", "library_path", "repacked_bytes", "gateup_repacked_bytes",
-    "repack", "repack_gateup", "gemm", "gateup_silu", "dequantize", "kernel_status",
+    "repack", "repack_gateup", "gemm", "gemm_argmax", "gateup_silu", "dequantize", "kernel_status",
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
 ]
 
 # symbols declared in include/w4a16.h
 EXPORTS = (
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_gateup_repacked_bytes", "w4a16_repack_gateup",
-    "w4a16_gemm", "w4a16_gateup_silu", "w4a16_dequantize", "w4a16_kernel_status",
+    "w4a16_gemm", "w4a16_gemm_argmax", "w4a16_gateup_silu", "w4a16_dequantize", "w4a16_kernel_status",
     "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
     "w4a16_set_programmatic_overlap",
 )
@@ -69,6 +69,8 @@ def lib(auto_build: bool = True) -> ctypes.CDLL:
     L.w4a16_repack_gateup.restype = i32
     L.w4a16_gemm.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P]
     L.w4a16_gemm.restype = i32
+    L.w4a16_gemm_argmax.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P]
+    L.w4a16_gemm_argmax.restype = i32
     L.w4a16_gateup_silu.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
     L.w4a16_gateup_silu.restype = i32
     L.w4a16_dequantize.argtypes = [P, i32, i32, i32, i32, P, P]
@@ -178,6 +180,25 @@ def gemm(x, packed, N, K, group, sym, out=None, stream=None):
                           M, N, K, group, int(sym), _ptr(out, _bf16_types(), "out"), _stream(stream))
     _check(rc, "w4a16_gemm")
     return out
+
+
+def gemm_argmax(x, packed, N, K, group, sym, out=None, logits=False, stream=None, index_out=None):
+    """int64 [M]: the first column of each row of y = x . dequant(W)^T (bf16)
+    at which y is largest (torch.argmax over the bf16 row). For M <= 16 the
+    logits are stored only when `logits` is true or `out` is given; returns
+    (argmax, y or None)."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    if out is None and (logits or M > 16):
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    idx = index_out if index_out is not None else torch.empty(M, dtype=torch.int64, device=x.device)
+    rc = lib().w4a16_gemm_argmax(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), M, N, K,
+                                 group, int(sym), _ptr(out, _bf16_types(), "out"),
+                                 ctypes.c_void_p(idx.data_ptr()), _stream(stream))
+    _check(rc, "w4a16_gemm_argmax")
+    return idx, out
 
 
 def gateup_silu(x, packed_gateup, N_each, K, group, sym, out=None, stream=None):

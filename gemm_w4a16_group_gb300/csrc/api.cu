@@ -160,6 +160,32 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
+int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym,
+                      uint16_t *y, int64_t *argmax, w4a16_stream_t stream) {
+  if (!x || !packed || !argmax) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group) || (M > 16 && !y)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(argmax, 8))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool overlap = g_overlap.load() != 0;
+  cudaError_t e = launch_argmax_init(argmax, M, overlap, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false, s, d.err, d.device,
+             overlap};
+  if (M <= 16 && g_override.load() != 3) {
+    c.amax = argmax;  // keys from the decode kernel's epilogue; y may be NULL
+    e = launch_smallm_mma(c, d.sm_count);
+  } else {
+    e = launch_prompt_tc(c, d.sm_count);
+    if (e == cudaSuccess) e = launch_row_argmax(y, M, N, argmax, s);
+  }
+  if (e == cudaSuccess) e = launch_argmax_finalize(argmax, M, overlap, s);
+  return finish_launch(e);
+}
+
 int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float *w_out,
                      w4a16_stream_t stream) {
   if (!packed || !w_out) return W4A16_ERR_INVALID_ARG;

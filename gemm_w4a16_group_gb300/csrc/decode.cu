@@ -61,6 +61,7 @@ struct DecodeParams {
   int tiles, chunks, groups, gblocks, units;
   int ld;                  // y row stride in elements
   int *err;
+  unsigned long long *amax;  // per x row, the running argmax key of y (or null)
   int device;              // host side only: ordinal for the per-device caches
   bool overlap;            // host side only: launch with programmatic stream serialization
   UnpackConsts uc;
@@ -252,7 +253,8 @@ struct DecodeSmem {
   static constexpr int kRingOff = 0;
   static constexpr int kBarOff = kWarps * R::kWarpBytes;
   static constexpr int kRedOff = kBarOff + kWarps * SLOTS * 8;
-  static constexpr int kFlagOff = kRedOff + kWarps * E * 4;
+  static constexpr int kBestOff = kRedOff + kWarps * E * 4;  // 16 argmax keys, one per x row
+  static constexpr int kFlagOff = kBestOff + 16 * 8;
   static constexpr int kBytes = kFlagOff + 16;
 };
 
@@ -292,7 +294,9 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int tile0 = blockIdx.x * TPW;
+  unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + SM::kBestOff);
   if (threadIdx.x == 0) *abort_flag = 0;
+  if (threadIdx.x < 16) best[threadIdx.x] = 0;
   __syncthreads();
   int ub, ue;
   k_slice(p.units, ub, ue);
@@ -447,8 +451,17 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
       }
     } else {
       const int n = 16 * (tile0 + i) + nl;
-      if (n < p.N) p.y[(size_t)m * p.ld + n] = f32_to_bf16_bits(red[0][e]);
+      if (n < p.N) {
+        const uint16_t v = f32_to_bf16_bits(red[0][e]);
+        if (p.y) p.y[(size_t)m * p.ld + n] = v;
+        if (p.amax) atomicMax(best + m, argmax_key(v, n));
+      }
     }
+  }
+  if (!GATEUP && p.amax) {
+    // one global arrival per x row and CTA: the largest key of this CTA's outputs
+    __syncthreads();
+    if (threadIdx.x < p.M && best[threadIdx.x] != 0) atomicMax(p.amax + threadIdx.x, best[threadIdx.x]);
   }
 }
 
@@ -611,8 +624,9 @@ struct DecodeCfg {
 // Split-K choice: grids that already fill the GPU stay unsplit (each warp
 // then streams long K slices and its ring stays full); smaller grids take the
 // largest cluster split (<= 8) that keeps them within one wave, with at least
-// two K units per warp. Measured: splitting a 1.2-wave grid four ways to even
-// out the waves made it slower (each warp's first slot latency dominates).
+// one K unit per warp (graph-timed: 5120 x 5120 at M = 5 takes 8.7 us split
+// 4 ways against 10.3 us split 2 ways). Splitting a grid of more than half a
+// wave (e.g. 1.4 waves at N = 34816) was measured slower at every factor.
 template <typename Kern>
 cudaError_t pick_cfg(Kern kern, int smem, int tiles, int units, int sm_count, int tpw, int device,
                      PerDevice &occ_cache, DecodeCfg &c) {
@@ -629,7 +643,7 @@ cudaError_t pick_cfg(Kern kern, int smem, int tiles, int units, int sm_count, in
   }
   const long long resident = (long long)occ * sm_count;
   c.kc = 1;
-  while (c.kc < 8 && ctas * c.kc * 2 <= resident && units >= kWarps * c.kc * 4) c.kc *= 2;
+  while (c.kc < 8 && ctas * c.kc * 2 <= resident && units >= kWarps * c.kc * 2) c.kc *= 2;
   return cudaSuccess;
 }
 
@@ -679,6 +693,7 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
   p.err = c.err;
   p.device = c.device;
   p.overlap = c.overlap;
+  p.amax = reinterpret_cast<unsigned long long *>(c.amax);
   p.uc = host_unpack_consts();
   return p;
 }

@@ -118,6 +118,19 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t zg, uint32_t zg
   out[3] = bf16x2_sub(out[3], zg8);
 }
 
+// Argmax over bf16 outputs as one unsigned 64-bit key, so that atomicMax
+// finds the maximum and, among equal values, the lowest index (the first
+// occurrence). High half: the bf16 bits mapped to an order-preserving
+// unsigned code, -0 as +0, every NaN above +inf (a NaN is the maximum).
+// Low half: 0xFFFFFFFF - n. Key 0 is below every output.
+__device__ __forceinline__ unsigned long long argmax_key(uint32_t bits, int n) {
+  bits &= 0xFFFFu;
+  if (bits == 0x8000u) bits = 0;
+  uint32_t o = (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
+  if ((bits & 0x7F80u) == 0x7F80u && (bits & 0x7Fu)) o = 0xFFFFu;
+  return ((unsigned long long)o << 32) | (0xFFFFFFFFu - (uint32_t)n);
+}
+
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

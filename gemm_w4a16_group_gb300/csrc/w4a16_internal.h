@@ -32,6 +32,7 @@ struct GemmCall {
   int *err;    // device error word (bounded waits that gave up)
   int device;  // current device ordinal, < kMaxDevices
   bool overlap;  // programmatic overlap with the previous kernel (M <= 16 kernels)
+  int64_t *amax = nullptr;  // argmax keys per x row (M <= 16 plain GEMM), or null
 };
 
 // Rows covered by the packed buffer of a call (padded; interleaved for gate/up).
@@ -49,5 +50,10 @@ cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, flo
 cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count);  // 1 <= M <= 16
 cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count);     // M == 1, not gate/up
 cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count);   // any M
+// argmax of bf16 y rows: keys (zeroed before) -> indices in place; and, for
+// y already written, the keys of every row
+cudaError_t launch_argmax_init(int64_t *amax, int M, bool overlap, cudaStream_t stream);
+cudaError_t launch_argmax_finalize(int64_t *amax, int M, bool overlap, cudaStream_t stream);
+cudaError_t launch_row_argmax(const uint16_t *y, int M, int N, int64_t *amax, cudaStream_t stream);
 
 }  // namespace w4a16

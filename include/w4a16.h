@@ -118,6 +118,29 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,
  * SiLU and the product; h is rounded once to bf16. `packed_gateup` comes from
  * w4a16_repack_gateup. Any M >= 1.
  */
+/*
+ * Greedy pick over the output columns: argmax[m] = the first n at which the
+ * bf16 output y[m][n] of w4a16_gemm (same x, packed, sizes) is largest, as
+ * torch.argmax over a bf16 row returns it: among equal values the lowest n;
+ * -0 equals +0; a NaN counts as the maximum. For the output-vocabulary head
+ * this replaces reading back M x N logits with M indices (the GPU argmax
+ * after the tall head in lucebox PR #823; one pass over all verify rows as in
+ * the GRIMOIRE v1.8 release notes, "INT4 verify faster").
+ *
+ *   argmax  int64 [M], device, 8-byte aligned; written by this call
+ *   y       bf16 [M][N] or NULL. M <= 16: the decode kernel forms the argmax
+ *           in its epilogue and stores y only when y is not NULL (the logits
+ *           need not exist). M > 16: required; the tcgen05 GEMM writes y and
+ *           a second kernel reads it back.
+ *
+ * Launches three kernels on `stream` (zero the keys, the GEMM, turn keys
+ * into indices), all taking part in programmatic overlap when it is on; the
+ * result is ready when the stream reaches the end of the call. Errors as
+ * w4a16_gemm.
+ */
+int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym,
+                      uint16_t *y, int64_t *argmax, w4a16_stream_t stream);
+
 int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N_each, int K,
                       int group, int sym, uint16_t *h, w4a16_stream_t stream);
 

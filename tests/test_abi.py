@@ -106,3 +106,14 @@ def test_programmatic_overlap_switch(L):
     assert L.w4a16_set_programmatic_overlap(prev) == 1
     assert w4.set_programmatic_overlap(False) == bool(prev)
     assert w4.set_programmatic_overlap(prev) is False
+
+
+def test_argmax_entry_point_argument_checks(L):
+    P = ctypes.c_void_p
+    g = L.w4a16_gemm_argmax
+    assert g(None, P(FAKE), 4, 64, 128, 64, 1, P(FAKE), P(FAKE), None) == INVALID
+    assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, P(FAKE), None, None) == INVALID     # no output
+    assert g(P(FAKE), P(FAKE), 17, 64, 128, 64, 1, None, P(FAKE), None) == INVALID    # M > 16 needs y
+    assert g(P(FAKE), P(FAKE), 4, 64, 96, 64, 1, None, P(FAKE), None) == INVALID      # K % G
+    assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, None, P(FAKE + 4), None) == MISALIGNED
+    assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, P(FAKE + 2), P(FAKE), None) == MISALIGNED

@@ -152,3 +152,56 @@ def test_gateup_buffer_is_a_plain_repack_of_interleaved_rows():
     inter = y.reshape(M, N // 16, 2, 16)
     np.testing.assert_array_equal(inter[:, :, 0].reshape(M, N), yg)
     np.testing.assert_array_equal(inter[:, :, 1].reshape(M, N), yu)
+
+
+ARGMAX_CASES = [
+    # (M, N, K, group, sym): one tile pair, ragged N, cluster split-K, tcgen05 path
+    (1, 250, 512, 128, True),
+    (5, 1040, 2048, 64, False),
+    (16, 520, 5120, 64, False),
+    (1, 96, 17408, 128, True),
+    (24, 300, 640, 128, True),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group,sym", ARGMAX_CASES)
+def test_gemm_argmax_matches_first_max_of_y(M, N, K, group, sym):
+    """Fused argmax = numpy's first maximum of the bf16 row that w4a16_gemm
+    writes (which is torch.argmax's choice), with and without stored logits."""
+    p = synth.make_problem(M, N, K, group, sym, seed=70 + M + N)
+    d = upload(p)
+    packed = packed_of(p, d)
+    y = bf16_f64(run_gemm(p, d=d, packed=packed))
+    want = np.argmax(y, axis=1)
+    a1, y1 = w4.gemm_argmax(d["x"], packed, N, K, group, sym, logits=True)
+    a2, y2 = w4.gemm_argmax(d["x"], packed, N, K, group, sym)
+    torch().cuda.synchronize()
+    assert w4.kernel_status() == 0
+    np.testing.assert_array_equal(a1.cpu().numpy(), want)
+    np.testing.assert_array_equal(a2.cpu().numpy(), want)
+    np.testing.assert_array_equal(bf16_f64(host_bits(y1)), y)
+    assert (y2 is None) == (M <= 16)
+
+
+@pytest.mark.parametrize("M", [1, 7, 30])
+def test_gemm_argmax_ties_pick_the_first_column(M):
+    """Rows of equal weights give equal outputs: the lowest such column wins.
+    Weight rows 40..47 repeat row 40 of a weight whose other rows are scaled
+    down, so each x row's maximum is shared by columns 40..47 (or is lower)."""
+    N, K, group = 200, 512, 64
+    p = synth.make_problem(M, N, K, group, True, seed=81)
+    q, sc = p["qweight"].copy(), p["scales"].copy()
+    q[40:48] = q[40]
+    sc[40:48] = sc[40]
+    # x = the sign pattern of row 40's dequantised weight, so row 40 is the largest dot product
+    w40 = oracle.dequant(q[40:41], sc[40:41], None, 1, K, group, True)[0]
+    x = np.tile(np.where(w40 >= 0, 0x3F80, 0xBF80).astype(np.uint16), (M, 1))
+    pp = dict(p, qweight=q, scales=sc, x=x)
+    d = upload(pp)
+    packed = packed_of(pp, d)
+    y = bf16_f64(run_gemm(pp, d=d, packed=packed))
+    a, _ = w4.gemm_argmax(d["x"], packed, N, K, group, True, logits=M > 16)
+    torch().cuda.synchronize()
+    got = a.cpu().numpy()
+    np.testing.assert_array_equal(got, np.argmax(y, axis=1))
+    assert (got == 40).all()

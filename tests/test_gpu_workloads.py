@@ -11,7 +11,7 @@ from synth.workloads import WORKLOADS
 
 import gemm_w4a16_group_gb300 as w4
 
-from gpu_helpers import assert_within, bf16_f64, run_gateup, run_gemm, sample_pairs, upload
+from gpu_helpers import assert_within, bf16_f64, packed_of, run_gateup, run_gemm, sample_pairs, torch, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -44,9 +44,18 @@ def test_workload_sampled(name):
 
 @pytest.mark.parametrize("M", [1, 5, 16])
 def test_lm_head_argmax(M):
+    """The head's greedy pick, from the logits and from the fused device
+    argmax (which stores no logits), against the oracle's exact maximum."""
     name = f"lm_head_m{M}_k5120_n248320"
     p = problem(name)
-    y = bf16_f64(run_gemm(p))
+    d = upload(p)
+    packed = packed_of(p, d)
+    yb = run_gemm(p, d=d, packed=packed)
+    fused, none = w4.gemm_argmax(d["x"], packed, p["N"], p["K"], p["group"], p["sym"])
+    torch().cuda.synchronize()
+    assert none is None and w4.kernel_status() == 0
+    y = bf16_f64(yb)
+    np.testing.assert_array_equal(fused.cpu().numpy(), np.argmax(y, axis=1))
     ref, sa = oracle.gemm(p["x"], p["qweight"], p["scales"], p["zeros"], p["M"], p["N"], p["K"],
                           p["group"], p["sym"])
     bound = oracle.gemm_bound(ref, sa)

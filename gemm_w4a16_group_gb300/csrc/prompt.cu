@@ -48,9 +48,9 @@
 namespace w4a16 {
 namespace {
 
-constexpr int BW = 256, BX = 256, BK = 64;  // pair tile: weight rows, x rows, k per stage
-constexpr int HW = BW / 2, HX = BX / 2;     // weight rows and x rows of one CTA
-constexpr int NT16 = HW / 16;               // 16-row weight tiles of one CTA
+constexpr int BW = 256, BK = 64;  // pair tile: weight rows, k per stage
+constexpr int HW = BW / 2;        // weight rows of one CTA
+constexpr int NT16 = HW / 16;     // 16-row weight tiles of one CTA
 #ifndef W4A16_PROMPT_SL
 #define W4A16_PROMPT_SL 6
 #endif
@@ -60,36 +60,42 @@ constexpr int SS = 2;                // scale-block ring (4 groups each)
 constexpr int kThreads = 512;
 constexpr uint16_t kPairMask = 0x3;
 
-constexpr int X_BYTES = HX * BK * 2;  // 16384
 constexpr int W_BYTES = HW * BK * 2;  // 16384
 constexpr int Q_BYTES = HW * BK / 2;  // 4096
 constexpr int RS_BYTES = NT16 * kScaleBlockBytes;  // 1024
 constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256
-
-constexpr int OFF_X = 0;
-constexpr int OFF_W = OFF_X + SL * X_BYTES;
-constexpr int OFF_Q = OFF_W + SW * W_BYTES;
-constexpr int OFF_RS = OFF_Q + SL * Q_BYTES;
-constexpr int OFF_RZ = OFF_RS + SS * RS_BYTES;
-constexpr int OFF_BAR = OFF_RZ + SS * RZ_BYTES;
 // barriers: full_L, empty_L [SL]; full_W, empty_W [SW]; full_S, empty_S [SS];
 // tfull, tempty [2]; mma_done [1]
 constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * 2 + 1;
-constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 
-static_assert(OFF_W % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-
-constexpr uint32_t kIdesc = idesc_bf16_f32(BW, BX);
-constexpr uint32_t kTmemCols = 512;  // two buffers x 256 fp32 columns
+// Everything that depends on the pair's x rows per tile, BX = 256 for long
+// prompts, 128 or 64 for a few dozen rows: a short M then issues MMAs of
+// N = BX instead of computing 256 columns of which most are padding.
+template <int BXT>
+struct XGeo {
+  static constexpr int BX = BXT, HX = BX / 2;  // x rows of the pair, of one CTA
+  static constexpr int X_BYTES = HX * BK * 2;
+  static constexpr int OFF_X = 0;
+  static constexpr int OFF_W = OFF_X + SL * X_BYTES;
+  static constexpr int OFF_Q = OFF_W + SW * W_BYTES;
+  static constexpr int OFF_RS = OFF_Q + SL * Q_BYTES;
+  static constexpr int OFF_RZ = OFF_RS + SS * RS_BYTES;
+  static constexpr int OFF_BAR = OFF_RZ + SS * RZ_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(BW, BX);
+  static constexpr uint32_t kTmemCols = 2 * BX;  // two buffers of BX fp32 columns (a power of two)
+  static_assert(BX == 64 || BX == 128 || BX == 256, "pair x rows");
+  static_assert(OFF_W % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
 
 struct PromptParams {
   uint16_t *y;
   int M, N, K;     // N: output columns (N_each for gate/up)
   int ld;          // y row stride (elements)
-  int mtiles, ntiles;  // tiles of 256 x rows, of 256 weight rows
+  int mtiles, ntiles;  // tiles of BX x rows, of 256 weight rows
   int nk;          // K / 64
   int ng;          // K / group
   int spg;         // 64-wide stages per group (1 or 2)
@@ -130,21 +136,22 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return *reinterpret_cast<uint16_t *>(&b);
 }
 
-template <bool SYM, bool GATEUP>
+template <bool SYM, bool GATEUP, int BXT>
 __global__ void __launch_bounds__(kThreads, 1)
     prompt_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
                      PromptParams p) {
+  using G = XGeo<BXT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  Bars bars{sbase + OFF_BAR};
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+  Bars bars{sbase + G::OFF_BAR};
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + G::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd
-  const uint32_t peer_abort = mapa_shared(smem_u32(smem + OFF_MISC + 4), rank ^ 1u);
+  const uint32_t peer_abort = mapa_shared(smem_u32(smem + G::OFF_MISC + 4), rank ^ 1u);
   const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
   const int ntot = p.mtiles * p.ntiles;
 
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc2(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc2(smem_u32(tmem_slot), G::kTmemCols);
     tmem_relinquish2();
   }
   // barriers of both CTAs initialised before any remote arrival or commit
@@ -208,16 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : RZ_BYTES));
             const int blk = kb / (4 * p.spg);
-            tma_load_2d(sbase + OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, qt, bars.full_S(slot));
-            if (!SYM) tma_load_2d(sbase + OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, qt, bars.full_S(slot));
+            tma_load_2d(sbase + G::OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, qt, bars.full_S(slot));
+            if (!SYM) tma_load_2d(sbase + G::OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, qt, bars.full_S(slot));
             ++sc;
           }
           const int slot = ls % SL;
           if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(bars.full_L(slot), X_BYTES + Q_BYTES);
-          tma_load_2d_hint(sbase + OFF_X + slot * X_BYTES, &tm_x, kb * BK, mt * BX + (int)rank * HX,
+          mbar_arrive_expect_tx(bars.full_L(slot), G::X_BYTES + Q_BYTES);
+          tma_load_2d_hint(sbase + G::OFF_X + slot * G::X_BYTES, &tm_x, kb * BK, mt * G::BX + (int)rank * G::HX,
                            bars.full_L(slot), pol_keep);
-          tma_load_2d_hint(sbase + OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, qt, bars.full_L(slot), pol_stream);
+          tma_load_2d_hint(sbase + G::OFF_Q + slot * Q_BYTES, &tm_q, kb * 128, qt, bars.full_L(slot), pol_stream);
           ++ls;
         }
       }
@@ -244,19 +251,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = gc & 1;
           if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(b * BX);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(b * G::BX);
           for (int ks = 0; ks < p.spg; ++ks) {
             const int sl = ls % SL, sw = ws % SW;
             if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
             // the odd CTA's dequantisers arrive only after its own x and codes landed
             if (!mbar_wait(bars.full_W(sw), (ws / SW) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t wdesc = sw128_desc(sbase + OFF_W + sw * W_BYTES);
-            const uint64_t xdesc = sw128_desc(sbase + OFF_X + sl * X_BYTES);
+            const uint64_t wdesc = sw128_desc(sbase + G::OFF_W + sw * W_BYTES);
+            const uint64_t xdesc = sw128_desc(sbase + G::OFF_X + sl * G::X_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
-              tc_mma2_f16(d_tmem, wdesc + 2 * kk, xdesc + 2 * kk, kIdesc, (ks | kk) != 0);
+              tc_mma2_f16(d_tmem, wdesc + 2 * kk, xdesc + 2 * kk, G::kIdesc, (ks | kk) != 0);
             }
             tc_commit2_mc(bars.empty_L(sl), kPairMask);
             tc_commit2_mc(bars.empty_W(sw), kPairMask);
@@ -293,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sl = ls % SL, sw = ws % SW;
         if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
         if (!mbar_wait(bars.empty_W(sw), ((ws / SW) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        const uint32_t qs = sbase + OFF_Q + sl * Q_BYTES;
-        const uint32_t wt = sbase + OFF_W + sw * W_BYTES;
+        const uint32_t qs = sbase + G::OFF_Q + sl * Q_BYTES;
+        const uint32_t wt = sbase + G::OFF_W + sw * W_BYTES;
 #pragma unroll
         for (int r = 0; r < NT16 / 4; ++r) {
           const int i = dw + 4 * r;  // 16-row tile within the CTA's 128 rows
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SYM) {
             zg = zg8 = zero_pair(8);
           } else {
-            const uint32_t zb = lds8(sbase + OFF_RZ + cur * RZ_BYTES + (i * 8 + g) * 4 + (gi & 3));
+            const uint32_t zb = lds8(sbase + G::OFF_RZ + cur * RZ_BYTES + (i * 8 + g) * 4 + (gi & 3));
             zg = zero_pair(zb & 0xF);
             zg8 = zero_pair(zb >> 4);
           }
@@ -346,29 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wr = 32 * q + lane;     // weight row within the CTA's 128
     // this row's scale in a scale block: tile wr/16, g = wr%8, half (wr/8)%2
     const uint32_t soff = (uint32_t)((wr >> 4) * kScaleBlockBytes + (wr & 7) * 16 + ((wr >> 3) & 1) * 2);
-    float acc[128];
+    float acc[G::HX];
     uint32_t gc = 0, sc = 0;
     int cur = 0;
     bool ok = true;
     for (int tile = pair; ok && tile < ntot; tile += npairs) {
       const int mt = tile % p.mtiles, nt = tile / p.mtiles;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+      for (int c = 0; c < G::HX; ++c) acc[c] = 0.f;
       for (int gi = 0; gi < p.ng; ++gi) {
         if ((gi & 3) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
           ++sc;
         }
-        const float s = __uint_as_float(lds16(sbase + OFF_RS + cur * RS_BYTES + soff + (gi & 3) * 4) << 16);
+        const float s = __uint_as_float(lds16(sbase + G::OFF_RS + cur * RS_BYTES + soff + (gi & 3) * 4) << 16);
         const int b = gc & 1;
         if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const float2 s2 = make_float2(s, s);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < G::HX / 32; ++ch) {
           float d[32];
-          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BX + ch2 * HX + ch * 32), d);
+          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * G::BX + ch2 * G::HX + ch * 32), d);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float2 a = make_float2(acc[ch * 32 + c], acc[ch * 32 + c + 1]);
@@ -386,27 +393,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gc;
       }
       if (!ok) break;
-      // thread = one weight row, 128 x rows m0 + c
-      const int m0 = mt * BX + ch2 * HX;
+      // thread = one weight row, HX x rows m0 + c
+      const int m0 = mt * G::BX + ch2 * G::HX;
       if (GATEUP) {
         // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows (16-row
-        // tiles alternate); lanes 0-15 form h for x rows c < 64, lanes 16-31
-        // for c >= 64, each taking the other operand from its partner lane
+        // tiles alternate); lanes 0-15 form h for x rows c < HX/2, lanes 16-31
+        // for c >= HX/2, each taking the other operand from its partner lane
+        constexpr int H2 = G::HX / 2;
         const bool gate = lane < 16;
         const int n = 16 * (nt * (BW / 32) + (int)rank * (NT16 / 2) + q) + (lane & 15);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float mine = gate ? acc[c] : acc[c + 64];
-          const float other = __shfl_xor_sync(0xffffffffu, gate ? acc[c + 64] : acc[c], 16);
+        for (int c = 0; c < H2; ++c) {
+          const float mine = gate ? acc[c] : acc[c + H2];
+          const float other = __shfl_xor_sync(0xffffffffu, gate ? acc[c + H2] : acc[c], 16);
           const float gv = gate ? mine : other, uv = gate ? other : mine;
-          const int m = m0 + c + (gate ? 0 : 64);
+          const int m = m0 + c + (gate ? 0 : H2);
           if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(silu_f32(gv) * uv);
         }
       } else {
         const int n = nt * BW + (int)rank * HW + wr;
         if (n < p.N) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
+          for (int c = 0; c < G::HX; ++c)
             if (m0 + c < p.M) p.y[(size_t)(m0 + c) * p.ld + n] = bf16_bits(acc[c]);
         }
       }
@@ -419,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc2(tmem_base, kTmemCols);
+    tmem_dealloc2(tmem_base, G::kTmemCols);
   }
 }
 
@@ -453,15 +461,17 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 }
 
 // Launch as clusters of two CTAs: one pair per tile, as many pairs as fit at
-// once (found once per instantiation), each walking the tiles with a stride.
-template <bool SYM, bool GATEUP>
+// once (found once per instantiation and device), each walking the tiles with
+// a stride.
+template <bool SYM, bool GATEUP, int BXT>
 cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
                            const CUtensorMap &tz, const PromptParams &p, int ntot, int device,
                            cudaStream_t s) {
-  auto kern = prompt_tc_kernel<SYM, GATEUP>;
+  using G = XGeo<BXT>;
+  auto kern = prompt_tc_kernel<SYM, GATEUP, BXT>;
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(kThreads, 1, 1);
-  lc.dynamicSmemBytes = SMEM_ALLOC;
+  lc.dynamicSmemBytes = G::SMEM_ALLOC;
   lc.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -473,7 +483,7 @@ cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const C
   static PerDevice max_pairs;  // clusters of this kernel that fit at once, per device
   int np = max_pairs.v[device].load(std::memory_order_relaxed);
   if (np == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     lc.gridDim = dim3(2, 1, 1);
     e = cudaOccupancyMaxActiveClusters(&np, kern, &lc);
@@ -486,15 +496,14 @@ cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const C
   return cudaLaunchKernelEx(&lc, kern, tx, tq, ts, tz, p);
 }
 
-}  // namespace
-
-cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
-  (void)sm_count;  // the pair count comes from the cluster occupancy query
+template <int BXT>
+cudaError_t launch_bx(const GemmCall &c) {
+  using G = XGeo<BXT>;
   const int rows = packed_rows(c);
   const Layout L = make_layout(rows, c.K, c.group, c.sym);
   CUtensorMap tx, tq, ts, tz;
   bool ok = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, (uint64_t)c.K, (uint64_t)c.M,
-                      (uint64_t)c.K * 2, BK, HX, CU_TENSOR_MAP_SWIZZLE_128B);
+                      (uint64_t)c.K * 2, BK, G::HX, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.codes_off, (uint64_t)L.chunks * 128,
                        (uint64_t)L.tiles, (uint64_t)L.chunks * kChunkBytes, 128, NT16, CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.scales_off, (uint64_t)L.gblocks * 32,
@@ -514,7 +523,7 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   p.N = c.N;
   p.K = c.K;
   p.ld = c.N;
-  p.mtiles = (c.M + BX - 1) / BX;
+  p.mtiles = (c.M + G::BX - 1) / G::BX;
   p.ntiles = (rows + BW - 1) / BW;
   p.nk = c.K / BK;
   p.ng = c.K / c.group;
@@ -523,11 +532,21 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
   p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;
   if (c.sym) {
-    return c.gateup ? launch_variant<true, true>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
-                    : launch_variant<true, false>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
+    return c.gateup ? launch_variant<true, true, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
+                    : launch_variant<true, false, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
   }
-  return c.gateup ? launch_variant<false, true>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
-                  : launch_variant<false, false>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
+  return c.gateup ? launch_variant<false, true, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
+                  : launch_variant<false, false, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
+}
+
+}  // namespace
+
+cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
+  (void)sm_count;  // the pair count comes from the cluster occupancy query
+  // x-row tile: the smallest that holds M (a tile of 256 otherwise)
+  if (c.M <= 64) return launch_bx<64>(c);
+  if (c.M <= 128) return launch_bx<128>(c);
+  return launch_bx<256>(c);
 }
 
 }  // namespace w4a16

@@ -52,6 +52,11 @@ CASES = [
     (TC, 200, 520, 1024, 128, True),
     (TC, 130, 300, 640, 64, False),
     (TC, 256, 512, 512, 128, False),
+    # the 64- and 128-row x tiles of short M, at and across their boundaries
+    (TC, 64, 520, 1024, 128, True),
+    (TC, 65, 300, 640, 64, False),
+    (TC, 100, 1040, 768, 64, True),
+    (TC, 128, 520, 1024, 128, False),
     # several 256 x 256 pair tiles in both directions, ragged in M and N
     (TC, 600, 700, 1024, 64, True),
     (TC, 513, 1040, 768, 128, False),
@@ -122,6 +127,8 @@ GATEUP_CASES = [
     (SMALLM, 5, 300, 1024, 64, False),
     (SMALLM, 16, 128, 2048, 128, True),
     (TC, 17, 136, 512, 64, False),
+    (TC, 64, 300, 1024, 64, False),
+    (TC, 120, 136, 512, 128, True),
     (TC, 200, 300, 1024, 128, True),
     (TC, 300, 200, 768, 64, True),
 ]

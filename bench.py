@@ -152,6 +152,28 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: one process per GPU, no data exchange)
+# ---------------------------------------------------------------------------
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (every rank calls this); x itself on one
+    process. The timed region's length is the slowest rank's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_step: float, steps: int, world: int, ms: float, scale: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (ms), in the metric's unit (scale 1e-9 for GB/s, 1e-12 for TFLOP/s)."""
+    return world * units_per_step * steps / (ms * 1e-3) * scale
+
+
+# ---------------------------------------------------------------------------
 # CUDA arm
 # ---------------------------------------------------------------------------
 def run_cuda(args, rank, world):
@@ -271,10 +293,8 @@ def run_cuda(args, rank, world):
     t_end = time.time()
     if w4.kernel_status() != 0:
         raise RuntimeError("a kernel's bounded wait gave up during the timed region")
+    ms = max_over_ranks(ms, world)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
 
     # end to end, eager through the public API: pinned host x -> device, the
@@ -296,18 +316,15 @@ def run_cuda(args, rank, world):
     torch.cuda.synchronize()
     sampler.stop()
     e2e_ms = e_start.elapsed_time(e_stop)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     if rank != 0:
         return None
 
     units_step = sum(pt["units"] for pt in parts)
     is_flops = parts[0]["is_flops"]
     scale = 1e-12 if is_flops else 1e-9
-    value = world * units_step * nsteps / (ms * 1e-3) * scale
-    e2e = world * units_step * nsteps / (e2e_ms * 1e-3) * scale
+    value = job_value(units_step, nsteps, world, ms, scale)
+    e2e = job_value(units_step, nsteps, world, e2e_ms, scale)
     dom = max(range(len(parts)), key=lambda j: parts[j]["units"])
     d = parts[dom]
     achieved = d["units"] / (per_call_ms[dom] * 1e-3) * scale

@@ -350,7 +350,9 @@ def run_cuda(args, rank, world):
                      "peak_src": peaks["src"] + (" bf16 burst" if is_flops else " copy")},
         "e2e": {"value": round(e2e, 2), "unit": parts[0]["unit"], "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": nsteps * len(parts),
+        # kernels of this library per timed step: one per call (three for the
+        # argmax form: zero the keys, the GEMM, keys to indices)
+        "gpu_launches": nsteps * sum(3 if args.argmax and pt["w"]["kind"] != "gateup" else 1 for pt in parts),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

@@ -52,10 +52,12 @@ constexpr int BW = 256, BK = 64;  // pair tile: weight rows, k per stage
 constexpr int HW = BW / 2;        // weight rows of one CTA
 constexpr int NT16 = HW / 16;     // 16-row weight tiles of one CTA
 #ifndef W4A16_PROMPT_SL
-#define W4A16_PROMPT_SL 6
+#define W4A16_PROMPT_SL 5
 #endif
-constexpr int SL = W4A16_PROMPT_SL;  // x + codes ring
-constexpr int SW = 4;                // dequantised W ring
+// x + codes ring and dequantised W ring, in step: stage s uses slot s % SL of
+// both, and one MMA commit per stage releases both (empty_L == empty_W)
+constexpr int SL = W4A16_PROMPT_SL;
+constexpr int SW = SL;
 constexpr int SS = 2;                // scale-block ring (4 groups each)
 constexpr int kThreads = 512;
 constexpr uint16_t kPairMask = 0x3;
@@ -64,7 +66,7 @@ constexpr int W_BYTES = HW * BK * 2;  // 16384
 constexpr int Q_BYTES = HW * BK / 2;  // 4096
 constexpr int RS_BYTES = NT16 * kScaleBlockBytes;  // 1024
 constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256
-// barriers: full_L, empty_L [SL]; full_W, empty_W [SW]; full_S, empty_S [SS];
+// barriers: full_L, empty_L [SL]; full_W, (unused) [SW]; full_S, empty_S [SS];
 // tfull, tempty [2]; mma_done [1]
 constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * 2 + 1;
 
@@ -108,7 +110,7 @@ struct Bars {
   __device__ uint32_t full_L(int i) const { return base + 8 * i; }
   __device__ uint32_t empty_L(int i) const { return base + 8 * (SL + i); }
   __device__ uint32_t full_W(int i) const { return base + 8 * (2 * SL + i); }
-  __device__ uint32_t empty_W(int i) const { return base + 8 * (2 * SL + SW + i); }
+  __device__ uint32_t empty_W(int i) const { return empty_L(i); }  // the same barrier (SW == SL)
   __device__ uint32_t full_S(int i) const { return base + 8 * (2 * SL + 2 * SW + i); }
   __device__ uint32_t empty_S(int i) const { return base + 8 * (2 * SL + 2 * SW + SS + i); }
   __device__ uint32_t tfull(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + i); }
@@ -160,10 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.full_L(i), 1);
       mbar_init(bars.empty_L(i), 1);  // the MMA commit (multicast to both CTAs)
     }
-    for (int i = 0; i < SW; ++i) {
-      mbar_init(bars.full_W(i), 8);  // even CTA: 4 local + 4 remote dequant warps
-      mbar_init(bars.empty_W(i), 1);
-    }
+    for (int i = 0; i < SW; ++i) mbar_init(bars.full_W(i), 8);  // even CTA: 4 local + 4 remote dequant warps
     for (int i = 0; i < SS; ++i) {
       mbar_init(bars.full_S(i), 1);
       mbar_init(bars.empty_S(i), SYM ? 8 : 8 + 4);  // epilogue warps (+ dequantisers reading zeros)
@@ -254,8 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = tmem_base + (uint32_t)(b * G::BX);
           for (int ks = 0; ks < p.spg; ++ks) {
             const int sl = ls % SL, sw = ws % SW;
-            if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
-            // the odd CTA's dequantisers arrive only after its own x and codes landed
+            // The W barrier implies the stage's x and codes landed in both CTAs:
+            // every dequantising warp waits on its own CTA's full_L before it
+            // arrives, so the MMA thread waits on full_W alone (one acquire per
+            // stage on the critical path of the single issuing thread).
             if (!mbar_wait(bars.full_W(sw), (ws / SW) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint64_t wdesc = sw128_desc(sbase + G::OFF_W + sw * W_BYTES);
@@ -265,8 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
               tc_mma2_f16(d_tmem, wdesc + 2 * kk, xdesc + 2 * kk, G::kIdesc, (ks | kk) != 0);
             }
-            tc_commit2_mc(bars.empty_L(sl), kPairMask);
-            tc_commit2_mc(bars.empty_W(sw), kPairMask);
+            tc_commit2_mc(bars.empty_L(sl), kPairMask);  // frees x, codes and W of the stage
             ++ls;
             ++ws;
           }

@@ -55,7 +55,7 @@ constexpr int NT16 = HW / 16;     // 16-row weight tiles of one CTA
 #define W4A16_PROMPT_SL 5
 #endif
 // x + codes ring and dequantised W ring, in step: stage s uses slot s % SL of
-// both, and one MMA commit per stage releases both (empty_L == empty_W)
+// both, and one MMA commit per stage (empty_L) releases both
 constexpr int SL = W4A16_PROMPT_SL;
 constexpr int SW = SL;
 constexpr int SS = 2;                // scale-block ring (4 groups each)
@@ -110,7 +110,6 @@ struct Bars {
   __device__ uint32_t full_L(int i) const { return base + 8 * i; }
   __device__ uint32_t empty_L(int i) const { return base + 8 * (SL + i); }
   __device__ uint32_t full_W(int i) const { return base + 8 * (2 * SL + i); }
-  __device__ uint32_t empty_W(int i) const { return empty_L(i); }  // the same barrier (SW == SL)
   __device__ uint32_t full_S(int i) const { return base + 8 * (2 * SL + 2 * SW + i); }
   __device__ uint32_t empty_S(int i) const { return base + 8 * (2 * SL + 2 * SW + SS + i); }
   __device__ uint32_t tfull(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + i); }
@@ -251,14 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(b * G::BX);
+          // One wait per group, on the W barrier of the group's last stage.
+          // It implies every stage of the group is ready in both CTAs: each
+          // dequantising warp waits on its own CTA's full_L before it works on
+          // a stage, and arrives on the group's stages in order. (Every barrier
+          // operation costs this single issuing thread a few hundred cycles.)
+          {
+            const uint32_t wl = ws + (uint32_t)p.spg - 1;
+            if (!mbar_wait(bars.full_W(wl % SW), (wl / SW) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+          }
           for (int ks = 0; ks < p.spg; ++ks) {
             const int sl = ls % SL, sw = ws % SW;
-            // The W barrier implies the stage's x and codes landed in both CTAs:
-            // every dequantising warp waits on its own CTA's full_L before it
-            // arrives, so the MMA thread waits on full_W alone (one acquire per
-            // stage on the critical path of the single issuing thread).
-            if (!mbar_wait(bars.full_W(sw), (ws / SW) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
             const uint64_t wdesc = sw128_desc(sbase + G::OFF_W + sw * W_BYTES);
             const uint64_t xdesc = sw128_desc(sbase + G::OFF_X + sl * G::X_BYTES);
 #pragma unroll
@@ -298,8 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++sc;
         }
         const int sl = ls % SL, sw = ws % SW;
+        // full_L of the stage also means its W slot is free: the producer
+        // issued the stage's loads only after the MMA commit that released
+        // the slot (one ring for codes and W), so no empty_W wait is needed
         if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(bars.empty_W(sw), ((ws / SW) & 1) ^ 1, abort_flag)) { ok = false; break; }
         const uint32_t qs = sbase + G::OFF_Q + sl * Q_BYTES;
         const uint32_t wt = sbase + G::OFF_W + sw * W_BYTES;
 #pragma unroll

@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
-from synth.workloads import WORKLOADS, algorithmic_bytes, gemm_flops  # noqa: E402
+from synth.workloads import WORKLOADS, algorithmic_bytes, gateup_bytes, gemm_flops  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -85,9 +85,12 @@ def step_parts(workload: str):
 
 
 def part_units(w):
-    """(units per call, metric unit, is_flops)"""
+    """(units per call, metric unit, is_flops): FLOPs for the prompt regime
+    (M > 16, tensor-bound), algorithmic bytes for decode (M <= 16, HBM-bound)."""
     if w["kind"] == "gateup":
-        return gemm_flops(w["M"], 2 * w["N"], w["K"]), "TFLOP/s", True
+        if w["M"] > 16:
+            return gemm_flops(w["M"], 2 * w["N"], w["K"]), "TFLOP/s", True
+        return gateup_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"]), "GB/s", False
     return algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"]), "GB/s", False
 
 
@@ -378,7 +381,7 @@ def cpu_baseline(workload, budget_s=10.0, steps=None):
     while True:
         for name, w, p in probs:
             if w["kind"] == "gateup":
-                rows = 16  # sample of M rows x every output column
+                rows = min(16, w["M"])  # sample of M rows x every output column
                 mi = np.repeat(np.arange(rows), w["N"])
                 ni = np.tile(np.arange(w["N"]), rows)
                 t0 = time.perf_counter()
@@ -386,7 +389,8 @@ def cpu_baseline(workload, budget_s=10.0, steps=None):
                                       p["scales_up"], p["zeros_up"], w["M"], w["N"], w["K"], w["group"],
                                       w["sym"], mi, ni)
                 t_total += time.perf_counter() - t0
-                units_done += gemm_flops(rows, 2 * w["N"], w["K"])
+                units_done += (gemm_flops(rows, 2 * w["N"], w["K"]) if is_flops else
+                               gateup_bytes(rows, w["N"], w["K"], w["group"], w["sym"]))
                 desc = f"{rows} of {w['M']} rows x all {2 * w['N']} gate/up columns"
             else:
                 t0 = time.perf_counter()

@@ -34,6 +34,9 @@ _add("decode_down_m1_k17408_n5120", M=1, K=FFN, N=HIDDEN, group=128, sym=True)
 for _M in (2, 4, 5, 8, 16):
     for _K, _N in ((HIDDEN, HIDDEN), (HIDDEN, 2 * FFN), (FFN, HIDDEN)):
         _add(f"smallm_m{_M}_k{_K}_n{_N}", M=_M, K=_K, N=_N, group=64, sym=False)
+# single-user decode through the fused gate/up: h = SiLU(x Wg^T) * (x Wu^T),
+# both weights read once (the same 34,816 weight rows as above)
+_add("decode_gateup_silu_m1_k5120_n17408", M=1, K=HIDDEN, N=FFN, group=128, sym=True, kind="gateup")
 # output-vocabulary head
 for _M in (1, 5, 16):
     _add(f"lm_head_m{_M}_k5120_n248320", M=_M, K=HIDDEN, N=VOCAB, group=128, sym=True,
@@ -57,3 +60,10 @@ def algorithmic_bytes(M: int, N: int, K: int, group: int, sym: bool) -> int:
 
 def gemm_flops(M: int, N: int, K: int) -> int:
     return 2 * M * N * K
+
+
+def gateup_bytes(M: int, N_each: int, K: int, group: int, sym: bool) -> int:
+    """Bytes a fused gate/up call must move at least: both packed weights with
+    their scales (and zero points), x, and the N_each-wide output h."""
+    w = algorithmic_bytes(0, N_each, K, group, sym)  # one weight, no x or y
+    return 2 * w + M * K * 2 + M * N_each * 2

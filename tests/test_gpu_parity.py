@@ -212,3 +212,25 @@ def test_gemm_argmax_ties_pick_the_first_column(M):
     got = a.cpu().numpy()
     np.testing.assert_array_equal(got, np.argmax(y, axis=1))
     assert (got == 40).all()
+
+
+DEGENERATE_KERNELS = [(GEMV, 1), (SMALLM, 1), (SMALLM, 7), (SMALLM, 16), (TC, 20), (TC, 300)]
+
+
+@pytest.mark.parametrize("which,M", DEGENERATE_KERNELS)
+def test_zero_scales_or_zero_x_give_exact_zero(which, M):
+    """w = (q - z) * 0 = 0, and x = 0, each give y = +-0 exactly."""
+    N, K, group = 72, 256, 64
+    p = synth.make_problem(M, N, K, group, False, seed=90 + M)
+    y = run_gemm(dict(p, scales=np.zeros_like(p["scales"])), which)
+    assert np.all((y & 0x7FFF) == 0)
+    y = run_gemm(dict(p, x=np.zeros_like(p["x"])), which)
+    assert np.all((y & 0x7FFF) == 0)
+
+
+@pytest.mark.parametrize("which,M", DEGENERATE_KERNELS)
+@pytest.mark.parametrize("N,K,group,sym", [(1, 64, 64, True), (17, 64, 64, False), (1, 128, 128, False)])
+def test_smallest_shapes(which, M, N, K, group, sym):
+    """One output row and/or one 64-wide K chunk (a single group)."""
+    p = synth.make_problem(M, N, K, group, sym, seed=95 + N + K)
+    check_gemm_full(p, run_gemm(p, which))

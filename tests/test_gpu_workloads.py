@@ -70,8 +70,11 @@ def test_lm_head_argmax(M):
     assert exact >= M - 1
 
 
-def test_prompt_gateup_sampled():
-    name = "prompt_gateup_m4096_k5120_n17408"
+GATEUP_NAMES = [n for n, w in WORKLOADS.items() if w["kind"] == "gateup"]
+
+
+@pytest.mark.parametrize("name", GATEUP_NAMES)
+def test_gateup_workload_sampled(name):
     p = problem(name)
     h = run_gateup(p)
     mi, ni = sample_pairs(p["M"], p["N"], 2000, seed=1)

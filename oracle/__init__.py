@@ -6,7 +6,9 @@ this package. The product path (``gemm_w4a16_group_gb300``) never does, and
 this package never imports the product path.
 
 The arithmetic lives in ``w4a16_oracle.c`` (plain C, float64); this module only
-compiles it with gcc on first use and marshals numpy arrays.
+compiles it with gcc on first use and marshals numpy arrays. Besides the
+zero-point form w = (q - z) * scale it holds the affine form w = scale * q +
+bias of the MLX 4-bit checkpoints (TensorFold PR #859).
 
 Error bounds (used by the parity tests):
 
@@ -82,6 +84,19 @@ def lib() -> ctypes.CDLL:
             L.oracle_gateup_silu_at.restype = i32
             L.oracle_silu_mul.argtypes = [ctypes.c_double, ctypes.c_double]
             L.oracle_silu_mul.restype = ctypes.c_double
+            L.oracle_weight_affine.argtypes = [P, P, P, i32, i32, i32, i32]
+            L.oracle_weight_affine.restype = ctypes.c_double
+            L.oracle_dequant_affine.argtypes = [P, P, P, i32, i32, i32, P]
+            L.oracle_dequant_affine.restype = None
+            L.oracle_gemm_affine.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, i32]
+            L.oracle_gemm_affine.restype = i32
+            L.oracle_gemm_affine_at.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, i64, P, P, i32]
+            L.oracle_gemm_affine_at.restype = i32
+            L.oracle_gateup_silu_affine_at.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, P, P, i64,
+                                                       P, P, P, P, P, i32]
+            L.oracle_gateup_silu_affine_at.restype = i32
+            L.oracle_group_sums.argtypes = [P, i32, i32, i32, P]
+            L.oracle_group_sums.restype = i32
             L.oracle_threads.argtypes = [i32]
             L.oracle_threads.restype = i32
             _lib = L
@@ -117,6 +132,39 @@ def dequant(qweight, scales, zeros, N, K, group, sym) -> np.ndarray:
     w = np.empty((N, K), dtype=np.float64)
     lib().oracle_dequant(_p(q), _p(s), _p(z), N, K, group, int(sym), _p(w))
     return w
+
+
+def dequant_affine(qweight, scales, biases, N, K, group) -> np.ndarray:
+    """float64 [N, K]: w = scale * q + bias (the affine form)."""
+    q, s, b = _c(qweight, np.int32), _c(scales, np.uint16), _c(biases, np.uint16)
+    w = np.empty((N, K), dtype=np.float64)
+    lib().oracle_dequant_affine(_p(q), _p(s), _p(b), N, K, group, _p(w))
+    return w
+
+
+def gemm_affine(x, qweight, scales, biases, M, N, K, group, nthreads: int = 0):
+    """(y, sum_abs) of the affine form, float64 [M, N] each."""
+    x, q, s, b = (_c(x, np.uint16), _c(qweight, np.int32), _c(scales, np.uint16), _c(biases, np.uint16))
+    y = np.empty((M, N), dtype=np.float64)
+    a = np.empty((M, N), dtype=np.float64)
+    rc = lib().oracle_gemm_affine(_p(x), _p(q), _p(s), _p(b), M, N, K, group, _p(y), _p(a), nthreads)
+    if rc:
+        raise ValueError("oracle_gemm_affine: bad arguments")
+    return y, a
+
+
+def gemm_affine_at(x, qweight, scales, biases, M, N, K, group, m_idx, n_idx, nthreads: int = 0):
+    """(y, sum_abs) of the affine form at the given (m, n) pairs."""
+    x, q, s, b = (_c(x, np.uint16), _c(qweight, np.int32), _c(scales, np.uint16), _c(biases, np.uint16))
+    mi, ni = _c(m_idx, np.int64), _c(n_idx, np.int64)
+    cnt = mi.size
+    y = np.empty(cnt, dtype=np.float64)
+    a = np.empty(cnt, dtype=np.float64)
+    rc = lib().oracle_gemm_affine_at(_p(x), _p(q), _p(s), _p(b), M, N, K, group, _p(mi), _p(ni), cnt,
+                                     _p(y), _p(a), nthreads)
+    if rc:
+        raise ValueError("oracle_gemm_affine_at: bad arguments")
+    return y, a
 
 
 def gemm(x, qweight, scales, zeros, M, N, K, group, sym, nthreads: int = 0):
@@ -162,6 +210,31 @@ def gateup_silu_at(x, qg, sg, zg, qu, su, zu, M, N, K, group, sym, m_idx, n_idx,
     if rc:
         raise ValueError("oracle_gateup_silu_at: bad arguments")
     return tuple(outs)
+
+
+def gateup_silu_affine_at(x, qg, sg, bg, qu, su, bu, M, N, K, group, m_idx, n_idx, nthreads: int = 0):
+    """(h, g, u, gsum_abs, usum_abs) of the affine form at the given (m, n) pairs."""
+    x = _c(x, np.uint16)
+    qg, sg, bg = _c(qg, np.int32), _c(sg, np.uint16), _c(bg, np.uint16)
+    qu, su, bu = _c(qu, np.int32), _c(su, np.uint16), _c(bu, np.uint16)
+    mi, ni = _c(m_idx, np.int64), _c(n_idx, np.int64)
+    cnt = mi.size
+    outs = [np.empty(cnt, dtype=np.float64) for _ in range(5)]
+    rc = lib().oracle_gateup_silu_affine_at(_p(x), _p(qg), _p(sg), _p(bg), _p(qu), _p(su), _p(bu),
+                                            M, N, K, group, _p(mi), _p(ni), cnt, *[_p(o) for o in outs],
+                                            nthreads)
+    if rc:
+        raise ValueError("oracle_gateup_silu_affine_at: bad arguments")
+    return tuple(outs)
+
+
+def group_sums(x, M, K, group) -> np.ndarray:
+    """float64 [K/G, M]: the sum of x[m] over each group of K."""
+    x = _c(x, np.uint16)
+    xs = np.empty((K // group, M), dtype=np.float64)
+    if lib().oracle_group_sums(_p(x), M, K, group, _p(xs)):
+        raise ValueError("oracle_group_sums: bad arguments")
+    return xs
 
 
 def silu_mul(g: float, u: float) -> float:

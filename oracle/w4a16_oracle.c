@@ -13,6 +13,11 @@
  *   y[m][n] = sum_k x[m][k] * w[n][k]          (k ascending, float64)
  *   h[m][n] = SiLU(g) * u,  g = y_gate[m][n],  u = y_up[m][n],  SiLU(v) = v / (1 + exp(-v))
  *
+ * Affine form (the *_affine functions): w[n][k] = scale[n][k/G] * q[n][k] +
+ * bias[n][k/G], q the unsigned 4-bit code and scale, bias bf16 per (row,
+ * group); the MLX affine 4-bit checkpoints of TensorFold PR #859 ("What this
+ * changes": every code keeps its value, scale and bias; groups of 64).
+ *
  * Sources: the exact "(q - z) * scale" dequantisation of the INT4 decode
  * kernels (GRIMOIRE v1.7 release notes, "What changed"); symmetric GPTQ-Int4
  * at group 128 and AutoRound W4A16 at group 64 (same page, measurement
@@ -68,6 +73,24 @@ double oracle_weight(const int32_t *qweight, const uint16_t *scales, const int32
   return (double)(q - z) * bf16_value(scales[(size_t)n * (size_t)Kg + (size_t)g]);
 }
 
+/* w[n][k] = scale * q + bias, exact in float64 (a 12-bit product plus a bf16) */
+double oracle_weight_affine(const int32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                            int K, int G, int n, int k) {
+  int Kg = K / G;
+  int g = k / G;
+  int q = oracle_code(qweight, K, n, k);
+  size_t i = (size_t)n * (size_t)Kg + (size_t)g;
+  return bf16_value(scales[i]) * (double)q + bf16_value(biases[i]);
+}
+
+/* Affine dequantised weight matrix, float64 [N][K]. */
+void oracle_dequant_affine(const int32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                           int N, int K, int G, double *w) {
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k)
+      w[(size_t)n * K + k] = oracle_weight_affine(qweight, scales, biases, K, G, n, k);
+}
+
 /* Dequantised weight matrix, float64 [N][K]. */
 void oracle_dequant(const int32_t *qweight, const uint16_t *scales, const int32_t *zeros,
                     int N, int K, int G, int sym, double *w) {
@@ -89,9 +112,12 @@ static void dot_one(const uint16_t *x, const double *wrow, int K, int m, double 
   *a = sa;
 }
 
+/* One weight row; biases != NULL selects the affine form (zeros, sym unused). */
 static void weight_row(const int32_t *qweight, const uint16_t *scales, const int32_t *zeros,
-                       int K, int G, int sym, int n, double *wrow) {
-  for (int k = 0; k < K; ++k) wrow[k] = oracle_weight(qweight, scales, zeros, K, G, sym, n, k);
+                       const uint16_t *biases, int K, int G, int sym, int n, double *wrow) {
+  for (int k = 0; k < K; ++k)
+    wrow[k] = biases ? oracle_weight_affine(qweight, scales, biases, K, G, n, k)
+                     : oracle_weight(qweight, scales, zeros, K, G, sym, n, k);
 }
 
 static int pick_threads(int nthreads) {
@@ -106,15 +132,9 @@ static int pick_threads(int nthreads) {
 /* Threads the library would use for nthreads (0 = all). */
 int oracle_threads(int nthreads) { return pick_threads(nthreads); }
 
-/*
- * y[m][n] (float64 [M][N]) and ysum_abs[m][n] = sum_k |x w| for all outputs.
- * x: bf16 bits [M][K]; qweight int32 [N][K/8]; scales bf16 bits [N][K/G];
- * zeros int32 [N][ceil(K/G/8)] (ignored when sym). Returns 0, or -1 on bad sizes
- * or when memory runs out.
- */
-int oracle_gemm(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
-                const int32_t *zeros, int M, int N, int K, int G, int sym,
-                double *y, double *ysum_abs, int nthreads) {
+static int gemm_all(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                    const int32_t *zeros, const uint16_t *biases, int M, int N, int K, int G, int sym,
+                    double *y, double *ysum_abs, int nthreads) {
   if (M < 0 || N < 0 || K <= 0 || G <= 0 || K % G || K % 8) return -1;
   int bad = 0;
   int nt = pick_threads(nthreads);
@@ -127,7 +147,7 @@ int oracle_gemm(const uint16_t *x, const int32_t *qweight, const uint16_t *scale
     } else {
 #pragma omp for schedule(dynamic, 8)
       for (int n = 0; n < N; ++n) {
-        weight_row(qweight, scales, zeros, K, G, sym, n, wrow);
+        weight_row(qweight, scales, zeros, biases, K, G, sym, n, wrow);
         for (int m = 0; m < M; ++m)
           dot_one(x, wrow, K, m, &y[(size_t)m * N + n], &ysum_abs[(size_t)m * N + n]);
       }
@@ -137,11 +157,10 @@ int oracle_gemm(const uint16_t *x, const int32_t *qweight, const uint16_t *scale
   return bad ? -1 : 0;
 }
 
-/* Selected outputs one by one: y[i] = y(m_idx[i], n_idx[i]). */
-int oracle_gemm_at(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
-                   const int32_t *zeros, int M, int N, int K, int G, int sym,
-                   const int64_t *m_idx, const int64_t *n_idx, int64_t count,
-                   double *y, double *ysum_abs, int nthreads) {
+static int gemm_some(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                     const int32_t *zeros, const uint16_t *biases, int M, int N, int K, int G, int sym,
+                     const int64_t *m_idx, const int64_t *n_idx, int64_t count,
+                     double *y, double *ysum_abs, int nthreads) {
   if (M < 0 || N < 0 || K <= 0 || G <= 0 || K % G || K % 8) return -1;
   for (int64_t i = 0; i < count; ++i)
     if (m_idx[i] < 0 || m_idx[i] >= M || n_idx[i] < 0 || n_idx[i] >= N) return -1;
@@ -156,13 +175,65 @@ int oracle_gemm_at(const uint16_t *x, const int32_t *qweight, const uint16_t *sc
     } else {
 #pragma omp for schedule(dynamic, 4)
       for (int64_t i = 0; i < count; ++i) {
-        weight_row(qweight, scales, zeros, K, G, sym, (int)n_idx[i], wrow);
+        weight_row(qweight, scales, zeros, biases, K, G, sym, (int)n_idx[i], wrow);
         dot_one(x, wrow, K, (int)m_idx[i], &y[i], &ysum_abs[i]);
       }
       free(wrow);
     }
   }
   return bad ? -1 : 0;
+}
+
+/*
+ * y[m][n] (float64 [M][N]) and ysum_abs[m][n] = sum_k |x w| for all outputs.
+ * x: bf16 bits [M][K]; qweight int32 [N][K/8]; scales bf16 bits [N][K/G];
+ * zeros int32 [N][ceil(K/G/8)] (ignored when sym). Returns 0, or -1 on bad sizes
+ * or when memory runs out.
+ */
+int oracle_gemm(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                const int32_t *zeros, int M, int N, int K, int G, int sym,
+                double *y, double *ysum_abs, int nthreads) {
+  return gemm_all(x, qweight, scales, zeros, NULL, M, N, K, G, sym, y, ysum_abs, nthreads);
+}
+
+/* Selected outputs one by one: y[i] = y(m_idx[i], n_idx[i]). */
+int oracle_gemm_at(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                   const int32_t *zeros, int M, int N, int K, int G, int sym,
+                   const int64_t *m_idx, const int64_t *n_idx, int64_t count,
+                   double *y, double *ysum_abs, int nthreads) {
+  return gemm_some(x, qweight, scales, zeros, NULL, M, N, K, G, sym, m_idx, n_idx, count, y, ysum_abs,
+                   nthreads);
+}
+
+/* The affine form of oracle_gemm: biases bf16 bits [N][K/G]. */
+int oracle_gemm_affine(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                       const uint16_t *biases, int M, int N, int K, int G,
+                       double *y, double *ysum_abs, int nthreads) {
+  if (!biases) return -1;
+  return gemm_all(x, qweight, scales, NULL, biases, M, N, K, G, 0, y, ysum_abs, nthreads);
+}
+
+/* The affine form of oracle_gemm_at. */
+int oracle_gemm_affine_at(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                          const uint16_t *biases, int M, int N, int K, int G,
+                          const int64_t *m_idx, const int64_t *n_idx, int64_t count,
+                          double *y, double *ysum_abs, int nthreads) {
+  if (!biases) return -1;
+  return gemm_some(x, qweight, scales, NULL, biases, M, N, K, G, 0, m_idx, n_idx, count, y, ysum_abs,
+                   nthreads);
+}
+
+/* Group sums of x (the X_g of the affine form's bias term), float64
+ * [K/G][M]: xs[g][m] = sum_{k in g} x[m][k]. Returns 0, or -1 on bad sizes. */
+int oracle_group_sums(const uint16_t *x, int M, int K, int G, double *xs) {
+  if (M < 0 || K <= 0 || G <= 0 || K % G) return -1;
+  for (int g = 0; g < K / G; ++g)
+    for (int m = 0; m < M; ++m) {
+      double acc = 0.0;
+      for (int k = g * G; k < (g + 1) * G; ++k) acc += bf16_value(x[(size_t)m * K + k]);
+      xs[(size_t)g * M + m] = acc;
+    }
+  return 0;
 }
 
 /* SiLU(g) * u in float64 */
@@ -186,6 +257,23 @@ int oracle_gateup_silu_at(const uint16_t *x,
     return -1;
   if (oracle_gemm_at(x, qw_up, sc_up, z_up, M, N, K, G, sym, m_idx, n_idx, count, u,
                      usum_abs, nthreads))
+    return -1;
+  for (int64_t i = 0; i < count; ++i) h[i] = oracle_silu_mul(g[i], u[i]);
+  return 0;
+}
+
+/* The affine form of oracle_gateup_silu_at: b_gate, b_up bf16 biases [N][K/G]. */
+int oracle_gateup_silu_affine_at(const uint16_t *x,
+                                 const int32_t *qw_gate, const uint16_t *sc_gate, const uint16_t *b_gate,
+                                 const int32_t *qw_up, const uint16_t *sc_up, const uint16_t *b_up,
+                                 int M, int N, int K, int G,
+                                 const int64_t *m_idx, const int64_t *n_idx, int64_t count,
+                                 double *h, double *g, double *u, double *gsum_abs, double *usum_abs,
+                                 int nthreads) {
+  if (oracle_gemm_affine_at(x, qw_gate, sc_gate, b_gate, M, N, K, G, m_idx, n_idx, count, g, gsum_abs,
+                            nthreads))
+    return -1;
+  if (oracle_gemm_affine_at(x, qw_up, sc_up, b_up, M, N, K, G, m_idx, n_idx, count, u, usum_abs, nthreads))
     return -1;
   for (int64_t i = 0; i < count; ++i) h[i] = oracle_silu_mul(g[i], u[i]);
   return 0;

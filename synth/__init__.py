@@ -7,6 +7,7 @@ bf16 activations, all in the canonical layout
     qweight int32 [N, K/8]     nibble j (bits 4j..4j+3) of word c holds k = 8c + j
     scales  bf16  [N, K/G]     one scale per (output row, K-group)
     zeros   int32 [N, ceil(K/G/8)]  nibble j of word c holds group 8c + j
+    biases  bf16  [N, K/G]     one bias per (output row, K-group), affine form only
 
 It holds no part of the method's arithmetic (no dequantisation, no products,
 no sums): only random-number generation, rounding of the sampled reals to
@@ -24,7 +25,7 @@ import numpy as np
 __all__ = [
     "splitmix64_stream", "uniform01", "normal01", "f32_to_bf16_bits",
     "bf16_bits_to_f32", "pack_nibbles_rows", "make_codes", "make_qweight",
-    "make_scales", "make_zeros", "make_x", "make_problem", "TENSOR_IDS",
+    "make_scales", "make_zeros", "make_biases", "make_x", "make_problem", "TENSOR_IDS",
 ]
 
 def _signed(c: int) -> np.int64:
@@ -39,7 +40,7 @@ _M2 = _signed(0x94D049BB133111EB)
 
 # stream id of every tensor a problem draws
 TENSOR_IDS = {"x": 1, "qweight": 2, "scales": 3, "zeros": 4,
-              "qweight_up": 5, "scales_up": 6, "zeros_up": 7}
+              "qweight_up": 5, "scales_up": 6, "zeros_up": 7, "biases": 8, "biases_up": 9}
 
 
 _BLOCK = 1 << 20  # draws per in-place block (reused buffers keep page faults down)
@@ -181,6 +182,12 @@ def make_zeros(N: int, Kg: int, seed: int, tid: int = TENSOR_IDS["zeros"]) -> np
     return pack_nibbles_rows(z)
 
 
+def make_biases(N: int, Kg: int, lo: float, hi: float, seed: int,
+                tid: int = TENSOR_IDS["biases"]) -> np.ndarray:
+    """bf16 bits [N, Kg], uniform in [lo, hi), drawn like the scales from their own stream."""
+    return make_scales(N, Kg, lo, hi, seed, tid)
+
+
 def make_x(M: int, K: int, seed: int, x_scale: float = 1.0,
            tid: int = TENSOR_IDS["x"]) -> np.ndarray:
     """bf16 bits [M, K] of N(0, 1) * x_scale (float64 -> float32 -> bf16)."""
@@ -192,9 +199,10 @@ def make_x(M: int, K: int, seed: int, x_scale: float = 1.0,
 
 def make_problem(M: int, N: int, K: int, group: int, sym: bool,
                  scale_range=(0.005, 0.02), x_scale: float = 1.0, seed: int = 0,
-                 gateup: bool = False) -> dict:
+                 gateup: bool = False, affine: bool = False, bias_range=(-0.16, -0.04)) -> dict:
     """All host arrays of one problem. With ``gateup`` a second weight (the up
-    projection, same shapes) is drawn from its own streams."""
+    projection, same shapes) is drawn from its own streams. With ``affine``
+    each weight has biases (uniform in ``bias_range``) and no zero points."""
     assert K % group == 0 and K % 8 == 0
     Kg = K // group
     lo, hi = scale_range
@@ -202,9 +210,14 @@ def make_problem(M: int, N: int, K: int, group: int, sym: bool,
          "x": make_x(M, K, seed, x_scale),
          "qweight": make_qweight(N, K, seed),
          "scales": make_scales(N, Kg, lo, hi, seed),
-         "zeros": None if sym else make_zeros(N, Kg, seed)}
+         "zeros": None if (sym or affine) else make_zeros(N, Kg, seed),
+         "affine": bool(affine)}
+    if affine:
+        p["biases"] = make_biases(N, Kg, bias_range[0], bias_range[1], seed)
     if gateup:
         p["qweight_up"] = make_qweight(N, K, seed, TENSOR_IDS["qweight_up"])
         p["scales_up"] = make_scales(N, Kg, lo, hi, seed, TENSOR_IDS["scales_up"])
-        p["zeros_up"] = None if sym else make_zeros(N, Kg, seed, TENSOR_IDS["zeros_up"])
+        p["zeros_up"] = None if (sym or affine) else make_zeros(N, Kg, seed, TENSOR_IDS["zeros_up"])
+        if affine:
+            p["biases_up"] = make_biases(N, Kg, bias_range[0], bias_range[1], seed, TENSOR_IDS["biases_up"])
     return p

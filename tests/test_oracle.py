@@ -263,3 +263,144 @@ def test_silu_bound_reduces_to_gemm_part_when_exact():
     b = oracle.silu_bound(np.array([2.0]), np.array([1.0]), np.array([3.0]),
                           np.array([0.0]), np.array([0.0]))
     assert b[0] == 2.0 * 2.0 ** -7
+
+
+# --------------------------------------------------------------------------
+# affine form w = scale * q + bias (MLX affine 4-bit checkpoints)
+
+AFFINE_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "affine_worked_example.txt")
+
+
+def _load_affine_golden():
+    d = {}
+    with open(AFFINE_GOLDEN) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            k, v = line.split(":", 1)
+            d[k.strip()] = v.split()
+    N, K, G = int(d["N"][0]), int(d["K"][0]), int(d["G"][0])
+    hexes = lambda key, dt: np.array([int(h, 16) for h in d[key]], dtype=dt)
+    f = lambda key: np.array([float(v) for v in d[key]])
+    return dict(N=N, K=K, G=G, q=hexes("qweight", np.uint32).view(np.int32).reshape(N, K // 8),
+                s=hexes("scales", np.uint16).reshape(N, K // G), b=hexes("biases", np.uint16).reshape(N, K // G),
+                x=hexes("x", np.uint16).reshape(-1, K), w=f("w").reshape(N, K), y=f("y").reshape(-1, N),
+                xsum=f("xsum").reshape(K // G, -1))
+
+
+def test_affine_golden_dequant_gemm_and_group_sums():
+    g = _load_affine_golden()
+    N, K, G = g["N"], g["K"], g["G"]
+    np.testing.assert_array_equal(oracle.dequant_affine(g["q"], g["s"], g["b"], N, K, G), g["w"])
+    y, a = oracle.gemm_affine(g["x"], g["q"], g["s"], g["b"], 2, N, K, G)
+    np.testing.assert_array_equal(y, g["y"])
+    np.testing.assert_array_equal(a[0], np.abs(g["w"]).sum(axis=1))
+    np.testing.assert_array_equal(oracle.group_sums(g["x"], 2, K, G), g["xsum"])
+
+
+def _brute_affine(codes, scales, biases, x, G):
+    """Exact y[m][n] and sum |x w| of the affine form from the unpacked codes."""
+    M, K = x.shape
+    N = codes.shape[0]
+    xs = [[_fr_bf16(x[m, k]) for k in range(K)] for m in range(M)]
+    y = [[Fraction(0)] * N for _ in range(M)]
+    a = [[Fraction(0)] * N for _ in range(M)]
+    for n in range(N):
+        w = [_fr_bf16(scales[n, k // G]) * int(codes[n, k]) + _fr_bf16(biases[n, k // G]) for k in range(K)]
+        for m in range(M):
+            y[m][n] = sum((xs[m][k] * w[k] for k in range(K)), Fraction(0))
+            a[m][n] = sum((abs(xs[m][k] * w[k]) for k in range(K)), Fraction(0))
+    return y, a
+
+
+@pytest.mark.parametrize("G,M,N,K", [(8, 3, 5, 32), (16, 2, 4, 64), (64, 1, 3, 128)])
+def test_affine_bruteforce_exact(G, M, N, K):
+    seed = 31 + K + N
+    Kg = K // G
+    codes = synth.make_codes(N, K, seed, 2)
+    s = synth.make_scales(N, Kg, 0.005, 0.02, seed)
+    b = synth.make_biases(N, Kg, -0.16, -0.04, seed)
+    x = synth.make_x(M, K, seed)
+    y, a = oracle.gemm_affine(x, synth.pack_nibbles_rows(codes), s, b, M, N, K, G)
+    ye, ae = _brute_affine(codes, s, b, x, G)
+    gamma = 1.01 * K * 2.0 ** -53
+    for m in range(M):
+        for n in range(N):
+            assert abs(Fraction(y[m, n]) - ye[m][n]) <= gamma * ae[m][n], (m, n)
+            assert abs(Fraction(a[m, n]) - ae[m][n]) <= gamma * ae[m][n]
+
+
+def test_affine_zero_codes_leave_bias_times_group_sums():
+    """q = 0 everywhere: y = sum_g bias_g * X_g, with X_g summed exactly."""
+    M, N, K, G = 3, 8, 256, 64
+    Kg = K // G
+    q = synth.pack_nibbles_rows(np.zeros((N, K), np.uint8))
+    s = synth.make_scales(N, Kg, 0.005, 0.02, 41)
+    b = synth.make_biases(N, Kg, -0.16, -0.04, 41)
+    x = synth.make_x(M, K, 41)
+    y, a = oracle.gemm_affine(x, q, s, b, M, N, K, G)
+    for m in range(M):
+        xg = [sum((_fr_bf16(x[m, k]) for k in range(g * G, (g + 1) * G)), Fraction(0)) for g in range(Kg)]
+        for n in range(N):
+            expect = sum((_fr_bf16(b[n, g]) * xg[g] for g in range(Kg)), Fraction(0))
+            assert abs(Fraction(y[m, n]) - expect) <= 1.01 * K * 2.0 ** -53 * Fraction(a[m, n])
+
+
+def test_affine_without_bias_is_the_zero_point_form_with_zero_points_0():
+    M, N, K, G = 2, 24, 256, 64
+    Kg = K // G
+    p = synth.make_problem(M, N, K, G, False, seed=43)
+    zeros0 = synth.pack_nibbles_rows(np.zeros((N, Kg), np.uint8))
+    b0 = np.zeros((N, Kg), np.uint16)
+    ya, aa = oracle.gemm_affine(p["x"], p["qweight"], p["scales"], b0, M, N, K, G)
+    yz, az = oracle.gemm(p["x"], p["qweight"], p["scales"], zeros0, M, N, K, G, False)
+    np.testing.assert_array_equal(ya, yz)
+    np.testing.assert_array_equal(aa, az)
+
+
+def test_affine_one_hot_x_selects_weight():
+    N, K, G = 20, 256, 64
+    Kg = K // G
+    codes = synth.make_codes(N, K, 45, 2)
+    s = synth.make_scales(N, Kg, 0.005, 0.02, 45)
+    b = synth.make_biases(N, Kg, -0.16, -0.04, 45)
+    ks = [0, 9, 64, 200, 255]
+    x = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = 0x3F80
+    y, _ = oracle.gemm_affine(x, synth.pack_nibbles_rows(codes), s, b, len(ks), N, K, G)
+    sf = synth.bf16_bits_to_f32(s).astype(np.float64)
+    bf = synth.bf16_bits_to_f32(b).astype(np.float64)
+    for i, k in enumerate(ks):
+        np.testing.assert_array_equal(y[i], sf[:, k // G] * codes[:, k] + bf[:, k // G])
+
+
+def test_affine_gemm_at_and_gateup_match_their_parts():
+    M, N, K, G = 4, 32, 256, 64
+    p = synth.make_problem(M, N, K, G, False, seed=47, gateup=True, affine=True)
+    assert p["zeros"] is None and p["zeros_up"] is None
+    y, a = oracle.gemm_affine(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, G)
+    rng = np.random.default_rng(1)
+    mi, ni = rng.integers(0, M, 40), rng.integers(0, N, 40)
+    ys, as_ = oracle.gemm_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, G, mi, ni)
+    np.testing.assert_array_equal(ys, y[mi, ni])
+    np.testing.assert_array_equal(as_, a[mi, ni])
+    h, g, u, _, _ = oracle.gateup_silu_affine_at(p["x"], p["qweight"], p["scales"], p["biases"],
+                                                 p["qweight_up"], p["scales_up"], p["biases_up"], M, N, K, G, mi, ni)
+    np.testing.assert_array_equal(g, ys)
+    yu, _ = oracle.gemm_affine(p["x"], p["qweight_up"], p["scales_up"], p["biases_up"], M, N, K, G)
+    np.testing.assert_array_equal(u, yu[mi, ni])
+    for i in range(len(mi)):
+        assert h[i] == pytest.approx(g[i] / (1.0 + math.exp(-g[i])) * u[i], rel=1e-14)
+
+
+def test_group_sums_closed_forms():
+    K, G = 512, 128
+    ones = np.full((2, K), 0x3F80, np.uint16)
+    np.testing.assert_array_equal(oracle.group_sums(ones, 2, K, G), np.full((K // G, 2), float(G)))
+    x = synth.make_x(3, K, 49)
+    xs = oracle.group_sums(x, 3, K, G)
+    for m in range(3):
+        for g in range(K // G):
+            exact = sum((_fr_bf16(x[m, k]) for k in range(g * G, (g + 1) * G)), Fraction(0))
+            assert xs[g, m] == float(exact)  # at most 128 bf16 terms: exact in float64

@@ -70,7 +70,7 @@ DEFAULT = "decode_ffn_m1"  # gate+up GEMV followed by the down GEMV
 def parse_shape(spec: str) -> dict:
     """'M,N,K,G,sym|asym' -> an ad-hoc workload (profiling cases)."""
     m, n, k, g, s = spec.split(",")
-    return dict(kind="gemm", M=int(m), N=int(n), K=int(k), group=int(g), sym=(s == "sym"),
+    return dict(kind="gemm", M=int(m), N=int(n), K=int(k), group=int(g), sym=(s == "sym"), affine=(s == "affine"),
                 scale_range=(0.005, 0.02), x_scale=1.0)
 
 
@@ -87,18 +87,29 @@ def step_parts(workload: str):
 def part_units(w):
     """(units per call, metric unit, is_flops): FLOPs for the prompt regime
     (M > 16, tensor-bound), algorithmic bytes for decode (M <= 16, HBM-bound)."""
+    aff = w.get("affine", False)
     if w["kind"] == "gateup":
         if w["M"] > 16:
             return gemm_flops(w["M"], 2 * w["N"], w["K"]), "TFLOP/s", True
-        return gateup_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"]), "GB/s", False
-    return algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"]), "GB/s", False
+        return gateup_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"], aff), "GB/s", False
+    if w["M"] > 16:
+        return gemm_flops(w["M"], w["N"], w["K"]), "TFLOP/s", True
+    return algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"], aff), "GB/s", False
 
 
 def metric_name(workload):
     parts = step_parts(workload)
     if part_units(parts[0][1])[2]:
-        return "W4A16 fused gate/up GEMM TFLOP/s (M=4096, K=5120, 2x17408)"
+        if parts[0][1]["kind"] == "gateup":
+            return "W4A16 fused gate/up GEMM TFLOP/s (M=4096, K=5120, 2x17408)"
+        return "W4A16 GEMM TFLOP/s (M>16)"
     return "W4A16 GEMM eff. HBM GB/s (M=1..16)"
+
+
+def new_problem(w):
+    return synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
+                              x_scale=w["x_scale"], seed=0, gateup=w["kind"] == "gateup",
+                              affine=w.get("affine", False))
 
 
 def load_peaks():
@@ -199,13 +210,15 @@ def run_cuda(args, rank, world):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
 
     parts = []
+    if args.argmax and any(w.get("affine", False) for _, w in step_parts(args.workload)):
+        raise SystemExit("--argmax takes the zero-point forms only")
     for name, w in step_parts(args.workload):
-        p = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
-                               x_scale=w["x_scale"], seed=0, gateup=w["kind"] == "gateup")
+        p = new_problem(w)
         units, unit, is_flops = part_units(w)
         if args.argmax and not is_flops:
             units -= 2 * w["M"] * w["N"]  # no logits written
-        wbytes = algorithmic_bytes(1, w["N"], w["K"], w["group"], w["sym"]) * (2 if w["kind"] == "gateup" else 1)
+        wbytes = algorithmic_bytes(1, w["N"], w["K"], w["group"], w["sym"], w.get("affine", False)) * \
+            (2 if w["kind"] == "gateup" else 1)
         parts.append(dict(name=name, w=w, p=p, units=units, unit=unit, is_flops=is_flops, wbytes=wbytes))
     # weight copies to rotate through so that L2 never holds the next call's weights
     total_w = sum(pt["wbytes"] for pt in parts)
@@ -213,7 +226,12 @@ def run_cuda(args, rank, world):
     for pt in parts:
         p, w = pt["p"], pt["w"]
         zd = None if p["zeros"] is None else up(p["zeros"])
-        if w["kind"] == "gateup":
+        if p["affine"] and w["kind"] == "gateup":
+            packed = w4.repack_affine_gateup(up(p["qweight"]), up(p["scales"]), up(p["biases"]), up(p["qweight_up"]),
+                                             up(p["scales_up"]), up(p["biases_up"]), w["N"], w["K"], w["group"])
+        elif p["affine"]:
+            packed = w4.repack_affine(up(p["qweight"]), up(p["scales"]), up(p["biases"]), w["N"], w["K"], w["group"])
+        elif w["kind"] == "gateup":
             packed = w4.repack_gateup(up(p["qweight"]), up(p["scales"]), zd, up(p["qweight_up"]),
                                       up(p["scales_up"]), None if p["zeros_up"] is None else up(p["zeros_up"]),
                                       w["N"], w["K"], w["group"], w["sym"])
@@ -222,6 +240,9 @@ def run_cuda(args, rank, world):
         pt["packed"] = [packed] + [packed.clone() for _ in range(copies - 1)]
         pt["x"] = up(p["x"])
         pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+        # affine form on the tcgen05 GEMM: the group sums of x, formed every call
+        pt["xs"] = (torch.empty(w4.xsum_bytes(w["M"], w["K"], w["group"]) // 4, dtype=torch.float32, device=dev)
+                    if p["affine"] and (w["M"] > 16 or args.kernel == "tc") else None)
         pt["idx"] = torch.empty(w["M"], dtype=torch.int64, device=dev)
         pt["idx_host"] = torch.empty(w["M"], dtype=torch.int64).pin_memory()
         pt["x_host"] = torch.from_numpy(p["x"].view(np.int16)).pin_memory()
@@ -241,9 +262,16 @@ def run_cuda(args, rank, world):
             idx, _ = w4.gemm_argmax(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"],
                                     w["sym"], stream=s, index_out=pt["idx"])
             return
+        xin = pt["x"] if x is None else x
+        if w.get("affine", False):
+            xs = None
+            if pt["xs"] is not None:
+                xs = w4.xsum(xin, w["K"], w["group"], out=pt["xs"], stream=s)
+            fn = w4.gateup_silu_affine if w["kind"] == "gateup" else w4.gemm_affine
+            fn(xin, pt["packed"][c], w["N"], w["K"], w["group"], xs, out=pt["y"] if y is None else y, stream=s)
+            return
         fn = w4.gateup_silu if w["kind"] == "gateup" else w4.gemm
-        fn(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"],
-           out=pt["y"] if y is None else y, stream=s)
+        fn(xin, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"], out=pt["y"] if y is None else y, stream=s)
 
     def steps(first, n, only=None):
         for i in range(n):
@@ -354,8 +382,10 @@ def run_cuda(args, rank, world):
         "e2e": {"value": round(e2e, 2), "unit": parts[0]["unit"], "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         # kernels of this library per timed step: one per call (three for the
-        # argmax form: zero the keys, the GEMM, keys to indices)
-        "gpu_launches": nsteps * sum(3 if args.argmax and pt["w"]["kind"] != "gateup" else 1 for pt in parts),
+        # argmax form: zero the keys, the GEMM, keys to indices; two for the
+        # affine form on the tcgen05 GEMM: the group sums of x, the GEMM)
+        "gpu_launches": nsteps * sum(3 if args.argmax and pt["w"]["kind"] != "gateup" else
+                                     2 if pt["xs"] is not None else 1 for pt in parts),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -373,9 +403,7 @@ def cpu_baseline(workload, budget_s=10.0, steps=None):
     parts = step_parts(workload)
     probs = []
     for name, w in parts:
-        p = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
-                               x_scale=w["x_scale"], seed=0, gateup=w["kind"] == "gateup")
-        probs.append((name, w, p))
+        probs.append((name, w, new_problem(w)))
     is_flops = part_units(parts[0][1])[2]
     units_done, t_total, reps, desc = 0.0, 0.0, 0, ""
     while True:
@@ -385,20 +413,31 @@ def cpu_baseline(workload, budget_s=10.0, steps=None):
                 mi = np.repeat(np.arange(rows), w["N"])
                 ni = np.tile(np.arange(w["N"]), rows)
                 t0 = time.perf_counter()
-                oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["qweight_up"],
-                                      p["scales_up"], p["zeros_up"], w["M"], w["N"], w["K"], w["group"],
-                                      w["sym"], mi, ni)
+                if p["affine"]:
+                    oracle.gateup_silu_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], p["qweight_up"],
+                                                 p["scales_up"], p["biases_up"], w["M"], w["N"], w["K"],
+                                                 w["group"], mi, ni)
+                else:
+                    oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["qweight_up"],
+                                          p["scales_up"], p["zeros_up"], w["M"], w["N"], w["K"], w["group"],
+                                          w["sym"], mi, ni)
                 t_total += time.perf_counter() - t0
                 units_done += (gemm_flops(rows, 2 * w["N"], w["K"]) if is_flops else
-                               gateup_bytes(rows, w["N"], w["K"], w["group"], w["sym"]))
+                               gateup_bytes(rows, w["N"], w["K"], w["group"], w["sym"], p["affine"]))
                 desc = f"{rows} of {w['M']} rows x all {2 * w['N']} gate/up columns"
             else:
+                rows = w["M"] if not is_flops else min(16, w["M"])  # M > 16: a sample of rows
                 t0 = time.perf_counter()
-                oracle.gemm(p["x"], p["qweight"], p["scales"], p["zeros"], w["M"], w["N"], w["K"], w["group"],
-                            w["sym"])
+                if p["affine"]:
+                    oracle.gemm_affine(p["x"][:rows], p["qweight"], p["scales"], p["biases"], rows, w["N"], w["K"],
+                                       w["group"])
+                else:
+                    oracle.gemm(p["x"][:rows], p["qweight"], p["scales"], p["zeros"], rows, w["N"], w["K"],
+                                w["group"], w["sym"])
                 t_total += time.perf_counter() - t0
-                units_done += algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"])
-                desc = "whole step"
+                units_done += (gemm_flops(rows, w["N"], w["K"]) if is_flops else
+                               algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"], p["affine"]))
+                desc = "whole step" if rows == w["M"] else f"{rows} of {w['M']} rows x all {w['N']} columns"
         reps += 1
         if (steps is not None and reps >= steps) or (steps is None and t_total >= budget_s):
             break

@@ -9,6 +9,12 @@ CPU or PyTorch fallback: if the library cannot be loaded every call raises.
     y = gemm(x, packed, N, K, group, sym)                          # y = x . dequant(W)^T
     pg = repack_gateup(qg, sg, zg, qu, su, zu, N, K, group, sym)
     h = gateup_silu(x, pg, N, K, group, sym)                       # SiLU(x Wg^T) * (x Wu^T)
+
+Affine form w = scale * q + bias (MLX affine 4-bit checkpoints):
+
+    pa = repack_affine(qweight, scales, biases, N, K, group)
+    xs = xsum(x, K, group)                 # group sums of x, shared by every weight on x
+    y = gemm_affine(x, pa, N, K, group, xs)
 """
 from __future__ import annotations
 
@@ -21,6 +27,7 @@ __all__ = [
     "EXPORTS", "W4A16Error", "lib", "library_path", "repacked_bytes", "gateup_repacked_bytes",
     "repack", "repack_gateup", "gemm", "gemm_argmax", "gateup_silu", "dequantize", "kernel_status",
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
+    "AFFINE", "repack_affine", "repack_affine_gateup", "xsum_bytes", "xsum", "gemm_affine", "gateup_silu_affine",
 ]
 
 # symbols declared in include/w4a16.h
@@ -28,9 +35,12 @@ EXPORTS = (
     "w4a16_repacked_bytes", "w4a16_repack", "w4a16_gateup_repacked_bytes", "w4a16_repack_gateup",
     "w4a16_gemm", "w4a16_gemm_argmax", "w4a16_gateup_silu", "w4a16_dequantize", "w4a16_kernel_status",
     "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
-    "w4a16_set_programmatic_overlap",
+    "w4a16_set_programmatic_overlap", "w4a16_repack_affine", "w4a16_repack_affine_gateup", "w4a16_xsum_bytes",
+    "w4a16_xsum", "w4a16_gemm_affine", "w4a16_gateup_silu_affine",
 )
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC = 0, 1, 2, 3
+# the `sym` argument: 0 zero points, 1 symmetric (z = 8), AFFINE scale * q + bias
+AFFINE = 2
 
 
 class W4A16Error(RuntimeError):
@@ -85,6 +95,18 @@ def lib(auto_build: bool = True) -> ctypes.CDLL:
     L.w4a16_set_kernel_override.restype = i32
     L.w4a16_set_programmatic_overlap.argtypes = [i32]
     L.w4a16_set_programmatic_overlap.restype = i32
+    L.w4a16_repack_affine.argtypes = [P, P, P, i32, i32, i32, P, P]
+    L.w4a16_repack_affine.restype = i32
+    L.w4a16_repack_affine_gateup.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, P]
+    L.w4a16_repack_affine_gateup.restype = i32
+    L.w4a16_xsum_bytes.argtypes = [i32, i32, i32]
+    L.w4a16_xsum_bytes.restype = sz
+    L.w4a16_xsum.argtypes = [P, i32, i32, i32, P, P]
+    L.w4a16_xsum.restype = i32
+    L.w4a16_gemm_affine.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
+    L.w4a16_gemm_affine.restype = i32
+    L.w4a16_gateup_silu_affine.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
+    L.w4a16_gateup_silu_affine.restype = i32
     _lib = L
     return L
 
@@ -216,8 +238,97 @@ def gateup_silu(x, packed_gateup, N_each, K, group, sym, out=None, stream=None):
     return out
 
 
+def repack_affine(qweight, scales, biases, N, K, group, stream=None):
+    """Canonical affine weight (qweight int32 [N, K/8], scales and biases bf16 [N, K/G]) -> packed uint8."""
+    torch = _torch()
+    nbytes = repacked_bytes(N, K, group, AFFINE)
+    if nbytes == 0:
+        raise W4A16Error("repack_affine: unsupported sizes")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    b16 = _bf16_types()
+    rc = lib().w4a16_repack_affine(_ptr(qweight, (torch.int32,), "qweight"), _ptr(scales, b16, "scales"),
+                                   _ptr(biases, b16, "biases"), N, K, group, ctypes.c_void_p(out.data_ptr()),
+                                   _stream(stream))
+    _check(rc, "w4a16_repack_affine")
+    return out
+
+
+def repack_affine_gateup(qw_gate, sc_gate, b_gate, qw_up, sc_up, b_up, N_each, K, group, stream=None):
+    torch = _torch()
+    nbytes = gateup_repacked_bytes(N_each, K, group, AFFINE)
+    if nbytes == 0:
+        raise W4A16Error("repack_affine_gateup: unsupported sizes")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=qw_gate.device)
+    i32, b16 = (torch.int32,), _bf16_types()
+    rc = lib().w4a16_repack_affine_gateup(_ptr(qw_gate, i32, "qw_gate"), _ptr(sc_gate, b16, "sc_gate"),
+                                          _ptr(b_gate, b16, "b_gate"), _ptr(qw_up, i32, "qw_up"),
+                                          _ptr(sc_up, b16, "sc_up"), _ptr(b_up, b16, "b_up"), N_each, K, group,
+                                          ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    _check(rc, "w4a16_repack_affine_gateup")
+    return out
+
+
+def xsum_bytes(M: int, K: int, group: int) -> int:
+    return int(lib().w4a16_xsum_bytes(M, K, group))
+
+
+def xsum(x, K, group, out=None, stream=None):
+    """float32 [K/G, ld]: column m < M holds the sums of x[m] over each group (ld >= M)."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    nbytes = xsum_bytes(M, K, group)
+    if nbytes == 0:
+        raise W4A16Error("xsum: unsupported sizes")
+    if out is None:
+        out = torch.empty((K // group, nbytes // 4 // (K // group)), dtype=torch.float32, device=x.device)
+    elif out.numel() * 4 < nbytes:
+        raise ValueError(f"xsum: out holds {out.numel() * 4} bytes, needs {nbytes}")
+    rc = lib().w4a16_xsum(_ptr(x, _bf16_types(), "x"), M, K, group, _ptr(out, (torch.float32,), "out"),
+                          _stream(stream))
+    _check(rc, "w4a16_xsum")
+    return out
+
+
+def _xs_ptr(xs):
+    torch = _torch()
+    return _ptr(xs, (torch.float32,), "xsum")
+
+
+def gemm_affine(x, packed, N, K, group, xs=None, out=None, stream=None):
+    """y[M, N] (bf16) = x . (scale * q + bias)^T. `xs` (from xsum) is needed
+    for M > 16; None lets the M <= 16 kernel form the group sums itself."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    rc = lib().w4a16_gemm_affine(_ptr(x, _bf16_types(), "x"), _xs_ptr(xs), _ptr(packed, (torch.uint8,), "packed"),
+                                 M, N, K, group, _ptr(out, _bf16_types(), "out"), _stream(stream))
+    _check(rc, "w4a16_gemm_affine")
+    return out
+
+
+def gateup_silu_affine(x, packed_gateup, N_each, K, group, xs=None, out=None, stream=None):
+    """h[M, N_each] (bf16) = SiLU(x Wg^T) * (x Wu^T), affine weights."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    if out is None:
+        out = torch.empty((M, N_each), dtype=torch.bfloat16, device=x.device)
+    rc = lib().w4a16_gateup_silu_affine(_ptr(x, _bf16_types(), "x"), _xs_ptr(xs),
+                                        _ptr(packed_gateup, (torch.uint8,), "packed"), M, N_each, K, group,
+                                        _ptr(out, _bf16_types(), "out"), _stream(stream))
+    _check(rc, "w4a16_gateup_silu_affine")
+    return out
+
+
 def dequantize(packed, N, K, group, sym, stream=None):
-    """float32 [N, K] = (q - z) * scale, read back through the kernels' unpack."""
+    """float32 [N, K] = (q - z) * scale (exact), or scale * q + bias rounded once
+    to float32 for sym = AFFINE, read back through the kernels' unpack."""
     torch = _torch()
     out = torch.empty((N, K), dtype=torch.float32, device=packed.device)
     rc = lib().w4a16_dequantize(_ptr(packed, (torch.uint8,), "packed"), N, K, group, int(sym),

@@ -76,24 +76,46 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int finish_launch(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : cuda_fail(e); }
 
+bool form_ok(int form) { return form == kFormZero || form == kFormSym || form == kFormAffine; }
+bool zero_form(int form) { return form == kFormZero || form == kFormSym; }
+
+// The affine calls: the decode kernel for M <= 16 (it forms the x group sums
+// itself), else the tcgen05 GEMM, which reads them from `xsum`.
+bool affine_uses_tc(int M) { return M > 16 || g_override.load() == 3; }
+
+int launch_affine(GemmCall &c, const float *xsum, const DeviceInfo &d) {
+  if (!affine_uses_tc(c.M)) return finish_launch(launch_smallm_mma(c, d.sm_count));
+  c.xsum = xsum;
+  c.xsum_ld = xsum_ld(c.M);
+  return finish_launch(launch_prompt_tc(c, d.sm_count));
+}
+
+// rows of a gate/up buffer (each weight padded to 128 rows), or -1 if too many
+long long gateup_rows(int N_each) {
+  const long long rows = 2LL * ((N_each + 127) / 128 * 128);
+  return rows >= (1LL << 31) / 16 ? -1 : rows;
+}
+
+
 }  // namespace
 
 extern "C" {
 
 size_t w4a16_repacked_bytes(int N, int K, int group, int sym) {
-  if (!sizes_ok(1, N, K, group)) return 0;
-  return make_layout(N, K, group, sym ? 1 : 0).total;
+  if (!sizes_ok(1, N, K, group) || !form_ok(sym)) return 0;
+  return make_layout(N, K, group, sym).total;
 }
 
 size_t w4a16_gateup_repacked_bytes(int N_each, int K, int group, int sym) {
-  if (!sizes_ok(1, N_each, K, group)) return 0;
-  const long long rows = 2LL * ((N_each + 127) / 128 * 128);
-  if (rows >= (1LL << 31) / 16) return 0;
-  return make_layout((int)rows, K, group, sym ? 1 : 0).total;
+  if (!sizes_ok(1, N_each, K, group) || !form_ok(sym)) return 0;
+  const long long rows = gateup_rows(N_each);
+  if (rows < 0) return 0;
+  return make_layout((int)rows, K, group, sym).total;
 }
 
 int w4a16_repack(const int32_t *qweight, const uint16_t *scales, const int32_t *zeros, int N, int K,
                  int group, int sym, void *packed, w4a16_stream_t stream) {
+  if (sym != kFormZero && sym != kFormSym) return W4A16_ERR_INVALID_ARG;
   if (!qweight || !scales || !packed || (!sym && !zeros)) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(1, N, K, group)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(packed, 256) || !aligned(qweight, 4) || !aligned(scales, 2) || (zeros && !aligned(zeros, 4)))
@@ -101,15 +123,47 @@ int w4a16_repack(const int32_t *qweight, const uint16_t *scales, const int32_t *
   DeviceInfo d;
   int st = current_device(d);
   if (st != W4A16_OK) return st;
-  const Layout L = make_layout(N, K, group, sym ? 1 : 0);
-  return finish_launch(launch_repack(qweight, scales, sym ? nullptr : zeros, nullptr, nullptr, nullptr, N,
+  const Layout L = make_layout(N, K, group, sym);
+  return finish_launch(launch_repack(qweight, scales, sym ? nullptr : zeros, nullptr, nullptr, nullptr, nullptr,
+                                     nullptr, N, false, L, static_cast<uint8_t *>(packed),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_repack_affine(const int32_t *qweight, const uint16_t *scales, const uint16_t *biases, int N, int K,
+                        int group, void *packed, w4a16_stream_t stream) {
+  if (!qweight || !scales || !biases || !packed) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(1, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(qweight, 4) || !aligned(scales, 2) || !aligned(biases, 2))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const Layout L = make_layout(N, K, group, kFormAffine);
+  return finish_launch(launch_repack(qweight, scales, nullptr, biases, nullptr, nullptr, nullptr, nullptr, N,
                                      false, L, static_cast<uint8_t *>(packed),
                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_repack_affine_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const uint16_t *b_gate,
+                               const int32_t *qw_up, const uint16_t *sc_up, const uint16_t *b_up, int N_each,
+                               int K, int group, void *packed, w4a16_stream_t stream) {
+  if (!qw_gate || !sc_gate || !b_gate || !qw_up || !sc_up || !b_up || !packed) return W4A16_ERR_INVALID_ARG;
+  if (w4a16_gateup_repacked_bytes(N_each, K, group, kFormAffine) == 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(qw_gate, 4) || !aligned(qw_up, 4) || !aligned(sc_gate, 2) ||
+      !aligned(sc_up, 2) || !aligned(b_gate, 2) || !aligned(b_up, 2))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const Layout L = make_layout((int)gateup_rows(N_each), K, group, kFormAffine);
+  return finish_launch(launch_repack(qw_gate, sc_gate, nullptr, b_gate, qw_up, sc_up, nullptr, b_up, N_each, true,
+                                     L, static_cast<uint8_t *>(packed), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const int32_t *z_gate,
                         const int32_t *qw_up, const uint16_t *sc_up, const int32_t *z_up, int N_each, int K,
                         int group, int sym, void *packed, w4a16_stream_t stream) {
+  if (sym != kFormZero && sym != kFormSym) return W4A16_ERR_INVALID_ARG;
   if (!qw_gate || !sc_gate || !qw_up || !sc_up || !packed) return W4A16_ERR_INVALID_ARG;
   if (!sym && (!z_gate || !z_up)) return W4A16_ERR_INVALID_ARG;
   if (w4a16_gateup_repacked_bytes(N_each, K, group, sym) == 0) return W4A16_ERR_INVALID_ARG;
@@ -119,23 +173,22 @@ int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const i
   DeviceInfo d;
   int st = current_device(d);
   if (st != W4A16_OK) return st;
-  const int rows = 2 * ((N_each + 127) / 128 * 128);
-  const Layout L = make_layout(rows, K, group, sym ? 1 : 0);
-  return finish_launch(launch_repack(qw_gate, sc_gate, sym ? nullptr : z_gate, qw_up, sc_up,
-                                     sym ? nullptr : z_up, N_each, true, L, static_cast<uint8_t *>(packed),
-                                     reinterpret_cast<cudaStream_t>(stream)));
+  const Layout L = make_layout((int)gateup_rows(N_each), K, group, sym);
+  return finish_launch(launch_repack(qw_gate, sc_gate, sym ? nullptr : z_gate, nullptr, qw_up, sc_up,
+                                     sym ? nullptr : z_up, nullptr, N_each, true, L,
+                                     static_cast<uint8_t *>(packed), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, const int32_t *zeros, int M,
                int N, int K, int group, int sym, uint16_t *y, w4a16_stream_t stream) {
   if (!x || !packed || !y) return W4A16_ERR_INVALID_ARG;
   if (scales || zeros) return W4A16_ERR_INVALID_ARG;  // reserved: they travel inside `packed`
-  if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group) || !zero_form(sym)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256)) return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
   int st = current_device(d);
   if (st != W4A16_OK) return st;
-  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false,
+  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym, false,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
   // M <= 16: the tensor-core decode kernel (measured faster than the CUDA-core
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
@@ -148,13 +201,13 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
 int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N_each, int K, int group,
                       int sym, uint16_t *h, w4a16_stream_t stream) {
   if (!x || !packed_gateup || !h) return W4A16_ERR_INVALID_ARG;
-  if (!sizes_ok(M, N_each, K, group) || w4a16_gateup_repacked_bytes(N_each, K, group, sym) == 0)
+  if (!sizes_ok(M, N_each, K, group) || !zero_form(sym) || w4a16_gateup_repacked_bytes(N_each, K, group, sym) == 0)
     return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(h, 16) || !aligned(packed_gateup, 256)) return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
   int st = current_device(d);
   if (st != W4A16_OK) return st;
-  GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym ? 1 : 0, true,
+  GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym, true,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
   if (M <= 16 && g_override.load() != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
@@ -163,7 +216,7 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
 int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym,
                       uint16_t *y, int64_t *argmax, w4a16_stream_t stream) {
   if (!x || !packed || !argmax) return W4A16_ERR_INVALID_ARG;
-  if (!sizes_ok(M, N, K, group) || (M > 16 && !y)) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group) || !zero_form(sym) || (M > 16 && !y)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(argmax, 8))
     return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
@@ -173,8 +226,7 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
   const bool overlap = g_overlap.load() != 0;
   cudaError_t e = launch_argmax_init(argmax, M, overlap, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym ? 1 : 0, false, s, d.err, d.device,
-             overlap};
+  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym, false, s, d.err, d.device, overlap};
   if (M <= 16 && g_override.load() != 3) {
     c.amax = argmax;  // keys from the decode kernel's epilogue; y may be NULL
     e = launch_smallm_mma(c, d.sm_count);
@@ -186,15 +238,59 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
   return finish_launch(e);
 }
 
+size_t w4a16_xsum_bytes(int M, int K, int group) {
+  if (!sizes_ok(M, 1, K, group)) return 0;
+  return (size_t)(K / group) * (size_t)xsum_ld(M) * sizeof(float);
+}
+
+int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_stream_t stream) {
+  if (!x || !xsum) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, 1, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xsum, 16)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  return finish_launch(launch_xsum(x, M, K, group, xsum, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, int M, int N, int K, int group,
+                      uint16_t *y, w4a16_stream_t stream) {
+  if (!x || !packed || !y || (!xsum && affine_uses_tc(M))) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(xsum, 16))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, kFormAffine, false,
+             reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
+  return launch_affine(c, xsum, d);
+}
+
+int w4a16_gateup_silu_affine(const uint16_t *x, const float *xsum, const void *packed_gateup, int M, int N_each,
+                             int K, int group, uint16_t *h, w4a16_stream_t stream) {
+  if (!x || !packed_gateup || !h || (!xsum && affine_uses_tc(M))) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N_each, K, group) || w4a16_gateup_repacked_bytes(N_each, K, group, kFormAffine) == 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(h, 16) || !aligned(packed_gateup, 256) || !aligned(xsum, 16))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, kFormAffine, true,
+             reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
+  return launch_affine(c, xsum, d);
+}
+
 int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float *w_out,
                      w4a16_stream_t stream) {
   if (!packed || !w_out) return W4A16_ERR_INVALID_ARG;
-  if (!sizes_ok(1, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(1, N, K, group) || !form_ok(sym)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(packed, 256) || !aligned(w_out, 16)) return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
   int st = current_device(d);
   if (st != W4A16_OK) return st;
-  const Layout L = make_layout(N, K, group, sym ? 1 : 0);
+  const Layout L = make_layout(N, K, group, sym);
   return finish_launch(launch_dequantize(static_cast<const uint8_t *>(packed), L, N, w_out,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -18,7 +18,10 @@
 //    a mantissa step of 1, the "(0x4300 | c) - 128" rebuild of TensorFold PR
 //    #859) and one bf16x2 subtraction of 128 + z per register leaves q - z.
 //    One group's products sum in a fresh accumulator, then acc += scale *
-//    partial in float32. "2-16 rows ... INT4 weights and bf16 activations" is
+//    partial in float32. Affine form (w = scale * q + bias, the MLX affine
+//    4-bit checkpoints of TensorFold PR #859): the same unpack with z = 0 gives
+//    q exactly, one more MMA per 16 k with an all-ones A sums the group's x
+//    (X_g), and acc += scale * partial + bias * X_g. "2-16 rows ... INT4 weights and bf16 activations" is
 //    the DPAS verify GEMM of the GRIMOIRE v1.7 release notes ("What changed");
 //    their v1.8 notes ("INT4 verify faster") show it occupancy-bound: here each
 //    weight tile is read and unpacked once for all rows and the tensor core
@@ -55,7 +58,8 @@ struct DecodeParams {
   const uint16_t *x;
   const uint8_t *codes;    // [tile][chunk][lane][16 B]
   const uint8_t *scales;   // [tile][gblock][g][4 groups][2 rows] bf16
-  const uint8_t *zeros;    // [tile][gblock][g][4 groups] bytes (row g | row g+8 << 4)
+  const uint8_t *zeros;    // [tile][gblock][g][4 groups] bytes (row g | row g+8 << 4),
+                           // or the biases in the scales' layout (affine form)
   uint16_t *y;
   int M, N, K;             // N: output columns (N_each for gate/up)
   int tiles, chunks, groups, gblocks, units;
@@ -131,20 +135,23 @@ __device__ __forceinline__ void k_slice(int units, int &u0, int &u1) {
 // ---------------------------------------------------------------------------
 // Per-warp ring of K-unit slots filled by bulk copies.
 //   slot layout: codes [TPW][4 chunks][32 lanes][16 B], then the scale block
-//   of each tile [TPW][128 B], then (asymmetric) its zero block [TPW][32 B].
+//   of each tile [TPW][128 B], then its zero block [TPW][32 B] (zero-point
+//   form) or bias block [TPW][128 B] (affine form).
 //   A unit u covers chunks 4u .. 4u+3 (fewer in a ragged last unit) and lies
 //   inside scale block u (group 64) or u/2 (group 128).
 // ---------------------------------------------------------------------------
-template <int TPW, bool SYM, int SLOTS>
+template <int TPW, int QF, int SLOTS>
 struct Ring {
   static constexpr int kTileCode = kUnitChunks * kChunkBytes;
   static constexpr int kScaleOff = TPW * kTileCode;
-  static constexpr int kZeroOff = kScaleOff + TPW * kScaleBlockBytes;
-  static constexpr int kSlotBytes = kZeroOff + (SYM ? 0 : TPW * kZeroBlockBytes);
+  static constexpr int kZeroOff = kScaleOff + TPW * kScaleBlockBytes;  // zero or bias blocks
+  static constexpr int kThirdBytes =
+      QF == kFormZero ? kZeroBlockBytes : QF == kFormAffine ? kScaleBlockBytes : 0;
+  static constexpr int kSlotBytes = kZeroOff + TPW * kThirdBytes;
   static constexpr int kWarpBytes = SLOTS * kSlotBytes;
   // one bulk copy per lane: codes of each tile, then its scale block, then its
-  // zero block (asymmetric)
-  static constexpr int kCopies = TPW * (SYM ? 2 : 3);
+  // zero or bias block
+  static constexpr int kCopies = TPW * (QF == kFormSym ? 2 : 3);
 
   uint32_t sbase;  // this warp's slots, shared-window address
   uint32_t bar0;   // SLOTS mbarriers, 8 bytes apart
@@ -174,9 +181,9 @@ struct Ring {
       stride = kScaleBlockBytes;
       dst_off = kScaleOff + i * kScaleBlockBytes;
     } else {
-      src = p.zeros + tile * p.gblocks * kZeroBlockBytes;
-      stride = kZeroBlockBytes;
-      dst_off = kZeroOff + i * kZeroBlockBytes;
+      src = p.zeros + tile * p.gblocks * kThirdBytes;
+      stride = kThirdBytes;
+      dst_off = kZeroOff + i * kThirdBytes;
     }
     policy = evict_first_policy();
     if (lane == 0) {
@@ -194,7 +201,7 @@ struct Ring {
     const uint32_t bar = bar0 + 8 * s;
     const int nch = min(kUnitChunks, chunks - kUnitChunks * u);
     if (lane == 0)
-      mbar_arrive_expect_tx(bar, TPW * (nch * kChunkBytes + kScaleBlockBytes + (SYM ? 0 : kZeroBlockBytes)));
+      mbar_arrive_expect_tx(bar, TPW * (nch * kChunkBytes + kScaleBlockBytes + kThirdBytes));
     if (lane < kCopies) {
       const uint32_t bytes = is_code ? (uint32_t)(nch * kChunkBytes) : stride;
       const size_t step = is_code ? (size_t)u : (size_t)(u / upb);
@@ -247,9 +254,9 @@ __device__ __forceinline__ bool reduce_partials(float (*red)[E]) {
 
 // Dynamic shared memory of a decode CTA: rings, their barriers, the partials
 // and the abort flag.
-template <int TPW, bool SYM, int SLOTS, int E>
+template <int TPW, int QF, int SLOTS, int E>
 struct DecodeSmem {
-  using R = Ring<TPW, SYM, SLOTS>;
+  using R = Ring<TPW, QF, SLOTS>;
   static constexpr int kRingOff = 0;
   static constexpr int kBarOff = kWarps * R::kWarpBytes;
   static constexpr int kRedOff = kBarOff + kWarps * SLOTS * 8;
@@ -281,12 +288,13 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, int first_unwaited, in
 // ---------------------------------------------------------------------------
 // small-M tensor-core kernel
 // ---------------------------------------------------------------------------
-template <int MT, int TPW, bool SYM, int CPG, int SLOTS, bool GATEUP>
+template <int MT, int TPW, int QF, int CPG, int SLOTS, bool GATEUP>
 __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p) {
   constexpr int E = TPW * MT * 4 * 32;
   constexpr int GPU = kUnitChunks / CPG;  // groups per full unit
-  using SM = DecodeSmem<TPW, SYM, SLOTS, E>;
-  using R = Ring<TPW, SYM, SLOTS>;
+  constexpr bool AFF = QF == kFormAffine;
+  using SM = DecodeSmem<TPW, QF, SLOTS, E>;
+  using R = Ring<TPW, QF, SLOTS>;
   extern __shared__ __align__(128) uint8_t smem[];
   float(*red)[E] = reinterpret_cast<float(*)[E]>(smem + SM::kRedOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kFlagOff);
@@ -351,8 +359,8 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
         uint32_t zg[TPW], zg8[TPW];
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
-          if (SYM) {
-            zg[i] = zg8[i] = zero_pair(8);
+          if (QF != kFormZero) {
+            zg[i] = zg8[i] = zero_pair(AFF ? 0 : 8);
           } else {
             const uint32_t zb = lds8(sl + R::kZeroOff + i * kZeroBlockBytes + g * 4 + (gg & 3));
             zg[i] = zero_pair(zb & 0xF);
@@ -360,6 +368,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
           }
         }
         float part[TPW][MT][4];
+        float xs[MT][4];  // affine: the group's sum of x per column (all-ones A)
 #pragma unroll
         for (int cc = 0; cc < CPG; ++cc) {
           const int cl = j * CPG + cc;  // chunk within the unit
@@ -386,6 +395,16 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
               b0[mt] = word_of(xx[mt][st >> 1], 2 * (st & 1));
               b1[mt] = word_of(xx[mt][st >> 1], 2 * (st & 1) + 1);
             }
+            if (AFF) {
+              const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                if (cc == 0 && st == 0)
+                  mma_bf16_16816_zero(xs[mt], ones, b0[mt], b1[mt]);
+                else
+                  mma_bf16_16816(xs[mt], ones, b0[mt], b1[mt]);
+              }
+            }
 #pragma unroll
             for (int i = 0; i < TPW; ++i) {
               uint32_t a[4];
@@ -410,6 +429,17 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
             acc[i][mt][1] = fmaf(sg, part[i][mt][1], acc[i][mt][1]);
             acc[i][mt][2] = fmaf(sg8, part[i][mt][2], acc[i][mt][2]);
             acc[i][mt][3] = fmaf(sg8, part[i][mt][3], acc[i][mt][3]);
+          }
+          if (AFF) {
+            const uint32_t bw = lds32(sl + R::kZeroOff + i * kScaleBlockBytes + g * 16 + (gg & 3) * 4);
+            const float bg = bf16lo_to_f32(bw), bg8 = bf16hi_to_f32(bw);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              acc[i][mt][0] = fmaf(bg, xs[mt][0], acc[i][mt][0]);
+              acc[i][mt][1] = fmaf(bg, xs[mt][1], acc[i][mt][1]);
+              acc[i][mt][2] = fmaf(bg8, xs[mt][2], acc[i][mt][2]);
+              acc[i][mt][3] = fmaf(bg8, xs[mt][3], acc[i][mt][3]);
+            }
           }
         }
       }
@@ -472,8 +502,9 @@ template <int TPW, bool SYM, int CPG, int SLOTS>
 __global__ void __launch_bounds__(kWarps * 32) gemv_m1_kernel(DecodeParams p) {
   constexpr int E = TPW * 2 * 8;  // (tile, row half, g)
   constexpr int GPU = kUnitChunks / CPG;
-  using SM = DecodeSmem<TPW, SYM, SLOTS, E>;
-  using R = Ring<TPW, SYM, SLOTS>;
+  constexpr int QF = SYM ? kFormSym : kFormZero;  // zero-point forms only
+  using SM = DecodeSmem<TPW, QF, SLOTS, E>;
+  using R = Ring<TPW, QF, SLOTS>;
   extern __shared__ __align__(128) uint8_t smem[];
   float(*red)[E] = reinterpret_cast<float(*)[E]>(smem + SM::kRedOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::kFlagOff);
@@ -679,7 +710,7 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
   p.x = c.x;
   p.codes = c.packed + L.codes_off;
   p.scales = c.packed + L.scales_off;
-  p.zeros = c.packed + (c.sym ? L.scales_off : L.zeros_off);
+  p.zeros = c.packed + (c.sym == kFormAffine ? L.biases_off : c.sym == kFormSym ? L.scales_off : L.zeros_off);
   p.y = c.y;
   p.M = c.M;
   p.N = c.N;
@@ -700,30 +731,35 @@ DecodeParams make_params(const GemmCall &c, const Layout &L) {
 
 constexpr int slots_for(int tpw) { return tpw >= 4 ? 2 : W4A16_DECODE_SLOTS2; }
 
-template <int MT, int TPW, bool SYM, int CPG, bool GATEUP>
+template <int MT, int TPW, int QF, int CPG, bool GATEUP>
 cudaError_t run_mma(const DecodeParams &p, int sm_count, cudaStream_t s) {
   constexpr int SLOTS = slots_for(TPW);
-  auto kern = smallm_mma_kernel<MT, TPW, SYM, CPG, SLOTS, GATEUP>;
+  auto kern = smallm_mma_kernel<MT, TPW, QF, CPG, SLOTS, GATEUP>;
   static PerDevice occ;
   DecodeCfg cfg;
-  cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * MT * 4 * 32>::kBytes, p.tiles, p.units,
+  cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, QF, SLOTS, TPW * MT * 4 * 32>::kBytes, p.tiles, p.units,
                            sm_count, TPW, p.device, occ, cfg);
   return e != cudaSuccess ? e : launch_decode(kern, p, cfg, s);
 }
 
 // Two 16-row tiles per warp at every N (measured faster than four at the
 // 248,320-row head: more resident warps per SM).
-template <bool SYM, int CPG, bool GATEUP>
+template <int QF, int CPG, bool GATEUP>
 cudaError_t run_mma_m(const DecodeParams &p, int sm_count, cudaStream_t s) {
-  if (p.M <= 8) return run_mma<1, 2, SYM, CPG, GATEUP>(p, sm_count, s);
-  return run_mma<2, 2, SYM, CPG, GATEUP>(p, sm_count, s);
+  if (p.M <= 8) return run_mma<1, 2, QF, CPG, GATEUP>(p, sm_count, s);
+  return run_mma<2, 2, QF, CPG, GATEUP>(p, sm_count, s);
+}
+
+template <int QF, bool GATEUP>
+cudaError_t run_mma_g(const DecodeParams &p, int sm_count, int group, cudaStream_t s) {
+  return group == 64 ? run_mma_m<QF, 1, GATEUP>(p, sm_count, s) : run_mma_m<QF, 2, GATEUP>(p, sm_count, s);
 }
 
 template <bool GATEUP>
-cudaError_t run_mma_all(const DecodeParams &p, int sm_count, int sym, int group, cudaStream_t s) {
-  if (sym)
-    return group == 64 ? run_mma_m<true, 1, GATEUP>(p, sm_count, s) : run_mma_m<true, 2, GATEUP>(p, sm_count, s);
-  return group == 64 ? run_mma_m<false, 1, GATEUP>(p, sm_count, s) : run_mma_m<false, 2, GATEUP>(p, sm_count, s);
+cudaError_t run_mma_all(const DecodeParams &p, int sm_count, int form, int group, cudaStream_t s) {
+  if (form == kFormSym) return run_mma_g<kFormSym, GATEUP>(p, sm_count, group, s);
+  if (form == kFormAffine) return run_mma_g<kFormAffine, GATEUP>(p, sm_count, group, s);
+  return run_mma_g<kFormZero, GATEUP>(p, sm_count, group, s);
 }
 
 template <bool SYM, int CPG>
@@ -732,7 +768,7 @@ cudaError_t run_gemv(const DecodeParams &p, int sm_count, cudaStream_t s) {
   auto kern = gemv_m1_kernel<TPW, SYM, CPG, SLOTS>;
   static PerDevice occ;
   DecodeCfg cfg;
-  cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, SYM, SLOTS, TPW * 16>::kBytes, p.tiles, p.units, sm_count, TPW,
+  cudaError_t e = pick_cfg(kern, DecodeSmem<TPW, SYM ? kFormSym : kFormZero, SLOTS, TPW * 16>::kBytes, p.tiles, p.units, sm_count, TPW,
                            p.device, occ, cfg);
   return e != cudaSuccess ? e : launch_decode(kern, p, cfg, s);
 }
@@ -749,6 +785,7 @@ cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count) {
 cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(packed_rows(c), c.K, c.group, c.sym);
   DecodeParams p = make_params(c, L);
+  if (c.sym == kFormAffine) return cudaErrorInvalidValue;  // the API routes affine to the MMA kernel
   if (c.sym) return c.group == 64 ? run_gemv<true, 1>(p, sm_count, c.stream) : run_gemv<true, 2>(p, sm_count, c.stream);
   return c.group == 64 ? run_gemv<false, 1>(p, sm_count, c.stream) : run_gemv<false, 2>(p, sm_count, c.stream);
 }

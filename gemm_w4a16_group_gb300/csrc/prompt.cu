@@ -5,7 +5,11 @@
 // The integer (q - z) is exact in bf16 and each product with a bf16 x is exact
 // in float32, so the tensor core sums one group's products into a TMEM tile
 // (fp32), and CUDA cores fold it into a register accumulator with the group's
-// scale in float32. Rounding a dequantised (q - z) * scale to bf16 before the
+// scale in float32. The affine form w = scale * q + bias (the MLX affine 4-bit
+// checkpoints of TensorFold PR #859) runs the same MMAs on the exact codes q
+// and adds bias * X_g per group, X_g = sum_{k in g} x[m][k] read from a
+// float32 table of group sums (w4a16_xsum) that TMA brings in beside the
+// scales. Rounding a dequantised (q - z) * scale to bf16 before the
 // MMA, as the TensorFold PR #859 prompt GEMM does ("each weight rounded once to
 // bf16"), would cost up to 2^-9 per weight; this split keeps every weight
 // exact. The feed-forward gate is fused as in the GRIMOIRE v1.8 release notes
@@ -27,7 +31,7 @@
 // One persistent CTA pair per two SMs, 512 threads per CTA, warp-specialised:
 //   warp 0       TMA producer: the CTA's x rows [128 x 64] (128-byte swizzle), the
 //                packed codes of its 128 weight rows x 64 k, and per four groups
-//                their scale (+ zero) block
+//                their scale (+ zero, or + bias and the tile's x group sums) block
 //   warp 1       TMEM allocation (both CTAs); in the even CTA the single thread
 //                issuing D[b] (+)= W . X^T for the pair, b = group parity
 //   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
@@ -72,17 +76,22 @@ constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * 2 + 1;
 
 // Everything that depends on the pair's x rows per tile, BX = 256 for long
 // prompts, 128 or 64 for a few dozen rows: a short M then issues MMAs of
-// N = BX instead of computing 256 columns of which most are padding.
-template <int BXT>
+// N = BX instead of computing 256 columns of which most are padding; and on
+// the weight form QF (a scale-block slot holds zeros, or biases and the x
+// group sums of the tile, [4 groups][BX] float32).
+template <int BXT, int QF>
 struct XGeo {
   static constexpr int BX = BXT, HX = BX / 2;  // x rows of the pair, of one CTA
   static constexpr int X_BYTES = HX * BK * 2;
+  static constexpr int RZS = QF == kFormAffine ? RS_BYTES : RZ_BYTES;  // zero or bias block slot
+  static constexpr int XS_BYTES = QF == kFormAffine ? 4 * BX * 4 : 0;
   static constexpr int OFF_X = 0;
   static constexpr int OFF_W = OFF_X + SL * X_BYTES;
   static constexpr int OFF_Q = OFF_W + SW * W_BYTES;
   static constexpr int OFF_RS = OFF_Q + SL * Q_BYTES;
   static constexpr int OFF_RZ = OFF_RS + SS * RS_BYTES;
-  static constexpr int OFF_BAR = OFF_RZ + SS * RZ_BYTES;
+  static constexpr int OFF_XS = OFF_RZ + SS * RZS;
+  static constexpr int OFF_BAR = OFF_XS + SS * XS_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -90,6 +99,7 @@ struct XGeo {
   static constexpr uint32_t kTmemCols = 2 * BX;  // two buffers of BX fp32 columns (a power of two)
   static_assert(BX == 64 || BX == 128 || BX == 256, "pair x rows");
   static_assert(OFF_W % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(OFF_RZ % 128 == 0 && OFF_XS % 128 == 0, "TMA destinations");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -137,12 +147,15 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return *reinterpret_cast<uint16_t *>(&b);
 }
 
-template <bool SYM, bool GATEUP, int BXT>
+// tm_z: the zero blocks (zero-point form) or the bias blocks (affine form);
+// tm_xs: the x group sums (affine form)
+template <int QF, bool GATEUP, int BXT>
 __global__ void __launch_bounds__(kThreads, 1)
     prompt_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
-                     PromptParams p) {
-  using G = XGeo<BXT>;
+                     const __grid_constant__ CUtensorMap tm_xs, PromptParams p) {
+  using G = XGeo<BXT, QF>;
+  constexpr bool SYM = QF == kFormSym, AFF = QF == kFormAffine, ZP = QF == kFormZero;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -164,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < SW; ++i) mbar_init(bars.full_W(i), 8);  // even CTA: 4 local + 4 remote dequant warps
     for (int i = 0; i < SS; ++i) {
       mbar_init(bars.full_S(i), 1);
-      mbar_init(bars.empty_S(i), SYM ? 8 : 8 + 4);  // epilogue warps (+ dequantisers reading zeros)
+      mbar_init(bars.empty_S(i), ZP ? 8 + 4 : 8);  // epilogue warps (+ dequantisers reading zeros)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.tfull(i), 1);
@@ -202,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_s);
       if (!SYM) tma_prefetch_desc(&tm_z);
+      if (AFF) tma_prefetch_desc(&tm_xs);
       uint32_t ls = 0, sc = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
@@ -211,10 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kb % (4 * p.spg) == 0) {
             const int slot = sc % SS;
             if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : RZ_BYTES));
+            mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : G::RZS) + G::XS_BYTES);
             const int blk = kb / (4 * p.spg);
             tma_load_2d(sbase + G::OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, qt, bars.full_S(slot));
-            if (!SYM) tma_load_2d(sbase + G::OFF_RZ + slot * RZ_BYTES, &tm_z, blk * 8, qt, bars.full_S(slot));
+            if (ZP) tma_load_2d(sbase + G::OFF_RZ + slot * G::RZS, &tm_z, blk * 8, qt, bars.full_S(slot));
+            if (AFF) {
+              tma_load_2d(sbase + G::OFF_RZ + slot * G::RZS, &tm_z, blk * 32, qt, bars.full_S(slot));
+              tma_load_2d(sbase + G::OFF_XS + slot * G::XS_BYTES, &tm_xs, mt * G::BX, 4 * blk, bars.full_S(slot));
+            }
             ++sc;
           }
           const int slot = ls % SL;
@@ -295,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = pair; ok && tile < ntot; tile += npairs) {
       for (int kb = 0; kb < p.nk; ++kb) {
         const int gi = kb / p.spg;
-        if (!SYM && kb % (4 * p.spg) == 0) {
+        if (ZP && kb % (4 * p.spg) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
           ++sc;
@@ -311,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < NT16 / 4; ++r) {
           const int i = dw + 4 * r;  // 16-row tile within the CTA's 128 rows
           uint32_t zg, zg8;
-          if (SYM) {
-            zg = zg8 = zero_pair(8);
+          if (!ZP) {
+            zg = zg8 = zero_pair(SYM ? 8 : 0);  // affine: the code q itself
           } else {
-            const uint32_t zb = lds8(sbase + G::OFF_RZ + cur * RZ_BYTES + (i * 8 + g) * 4 + (gi & 3));
+            const uint32_t zb = lds8(sbase + G::OFF_RZ + cur * G::RZS + (i * 8 + g) * 4 + (gi & 3));
             zg = zero_pair(zb & 0xF);
             zg8 = zero_pair(zb >> 4);
           }
@@ -343,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           arrive_even(bars.full_W(sw), rank);
-          if (!SYM && ((kb + 1) % (4 * p.spg) == 0 || kb + 1 == p.nk)) mbar_arrive(bars.empty_S(cur));
+          if (ZP && ((kb + 1) % (4 * p.spg) == 0 || kb + 1 == p.nk)) mbar_arrive(bars.empty_S(cur));
         }
         ++ls;
         ++ws;
@@ -373,6 +391,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++sc;
         }
         const float s = __uint_as_float(lds16(sbase + G::OFF_RS + cur * RS_BYTES + soff + (gi & 3) * 4) << 16);
+        // affine: this row's bias, and the group's x sums of the tile's x rows
+        const float bias = AFF ? __uint_as_float(lds16(sbase + G::OFF_RZ + cur * G::RZS + soff + (gi & 3) * 4) << 16)
+                               : 0.f;
+        const uint32_t xs_row = sbase + G::OFF_XS + cur * G::XS_BYTES + ((gi & 3) * G::BX + ch2 * G::HX) * 4;
+        if (AFF) {
+          // acc += bias * X_g needs no MMA result: done before the TMEM wait
+          const float2 b2 = make_float2(bias, bias);
+#pragma unroll
+          for (int c = 0; c < G::HX; c += 4) {
+            const float4 xv = lds128f(xs_row + c * 4);  // the same address in every lane
+            float2 a = make_float2(acc[c], acc[c + 1]);
+            float2 a2 = make_float2(acc[c + 2], acc[c + 3]);
+            a = __ffma2_rn(b2, make_float2(xv.x, xv.y), a);
+            a2 = __ffma2_rn(b2, make_float2(xv.z, xv.w), a2);
+            acc[c] = a.x;
+            acc[c + 1] = a.y;
+            acc[c + 2] = a2.x;
+            acc[c + 3] = a2.y;
+          }
+        }
         const int b = gc & 1;
         if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -388,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[ch * 32 + c] = a.x;
             acc[ch * 32 + c + 1] = a.y;
           }
+
         }
         tc_fence_before();
         __syncwarp();
@@ -468,12 +507,12 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 // Launch as clusters of two CTAs: one pair per tile, as many pairs as fit at
 // once (found once per instantiation and device), each walking the tiles with
 // a stride.
-template <bool SYM, bool GATEUP, int BXT>
+template <int QF, bool GATEUP, int BXT>
 cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
-                           const CUtensorMap &tz, const PromptParams &p, int ntot, int device,
-                           cudaStream_t s) {
-  using G = XGeo<BXT>;
-  auto kern = prompt_tc_kernel<SYM, GATEUP, BXT>;
+                           const CUtensorMap &tz, const CUtensorMap &txs, const PromptParams &p, int ntot,
+                           int device, cudaStream_t s) {
+  using G = XGeo<BXT, QF>;
+  auto kern = prompt_tc_kernel<QF, GATEUP, BXT>;
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = G::SMEM_ALLOC;
@@ -498,15 +537,21 @@ cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const C
   }
   const int pairs = ntot < np ? ntot : np;
   lc.gridDim = dim3(2 * pairs, 1, 1);
-  return cudaLaunchKernelEx(&lc, kern, tx, tq, ts, tz, p);
+  return cudaLaunchKernelEx(&lc, kern, tx, tq, ts, tz, txs, p);
+}
+
+template <int QF, bool GATEUP, int BXT>
+cudaError_t launch_form(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts, const CUtensorMap &tz,
+                        const CUtensorMap &txs, const PromptParams &p, int ntot, const GemmCall &c) {
+  return launch_variant<QF, GATEUP, BXT>(tx, tq, ts, tz, txs, p, ntot, c.device, c.stream);
 }
 
 template <int BXT>
 cudaError_t launch_bx(const GemmCall &c) {
-  using G = XGeo<BXT>;
+  using G = XGeo<BXT, kFormSym>;
   const int rows = packed_rows(c);
   const Layout L = make_layout(rows, c.K, c.group, c.sym);
-  CUtensorMap tx, tq, ts, tz;
+  CUtensorMap tx, tq, ts, tz, txs;
   bool ok = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.x, (uint64_t)c.K, (uint64_t)c.M,
                       (uint64_t)c.K * 2, BK, G::HX, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.codes_off, (uint64_t)L.chunks * 128,
@@ -514,12 +559,20 @@ cudaError_t launch_bx(const GemmCall &c) {
   ok = ok && encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.scales_off, (uint64_t)L.gblocks * 32,
                        (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, NT16,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (c.sym) {
-    tz = ts;  // unused
-  } else {
+  tz = txs = ts;  // unused unless set below
+  if (c.sym == kFormZero) {
     ok = ok && encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.zeros_off, (uint64_t)L.gblocks * 8,
                          (uint64_t)L.tiles, (uint64_t)L.gblocks * kZeroBlockBytes, 8, NT16,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else if (c.sym == kFormAffine) {
+    if (!c.xsum) return cudaErrorInvalidValue;
+    ok = ok && encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.biases_off, (uint64_t)L.gblocks * 32,
+                         (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, NT16,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    // xsum [groups][ld] float32, ld a multiple of 256 >= M: the box of BX x
+    // rows and four groups never starts past the row (x coordinate mt * BX)
+    ok = ok && encode_2d(&txs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c.xsum, (uint64_t)c.xsum_ld,
+                         (uint64_t)(c.K / c.group), (uint64_t)c.xsum_ld * 4, G::BX, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return cudaErrorInvalidValue;
   PromptParams p;
@@ -536,12 +589,14 @@ cudaError_t launch_bx(const GemmCall &c) {
   p.err = c.err;
   p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;
-  if (c.sym) {
-    return c.gateup ? launch_variant<true, true, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
-                    : launch_variant<true, false, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
-  }
-  return c.gateup ? launch_variant<false, true, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream)
-                  : launch_variant<false, false, BXT>(tx, tq, ts, tz, p, ntot, c.device, c.stream);
+  if (c.sym == kFormSym)
+    return c.gateup ? launch_form<kFormSym, true, BXT>(tx, tq, ts, tz, txs, p, ntot, c)
+                    : launch_form<kFormSym, false, BXT>(tx, tq, ts, tz, txs, p, ntot, c);
+  if (c.sym == kFormAffine)
+    return c.gateup ? launch_form<kFormAffine, true, BXT>(tx, tq, ts, tz, txs, p, ntot, c)
+                    : launch_form<kFormAffine, false, BXT>(tx, tq, ts, tz, txs, p, ntot, c);
+  return c.gateup ? launch_form<kFormZero, true, BXT>(tx, tq, ts, tz, txs, p, ntot, c)
+                  : launch_form<kFormZero, false, BXT>(tx, tq, ts, tz, txs, p, ntot, c);
 }
 
 }  // namespace

@@ -1,10 +1,12 @@
-// Offline repack (canonical -> tiled layout) and the exact dequantisation
-// read-back used by the tests.
+// Offline repack (canonical -> tiled layout) and the dequantisation read-back
+// used by the tests.
 //
 // The canonical packing (nibble j of word c holds k = 8c + j) and the exact
 // w = (q - z) * scale follow the INT4 kernels of the GRIMOIRE v1.7 release
-// notes ("What changed"); the tiled order is this library's own, described in
-// w4a16_common.cuh.
+// notes ("What changed"); the affine form w = scale * q + bias is that of the
+// MLX affine 4-bit checkpoints in TensorFold PR #859 ("What this changes":
+// every code keeps its value, scale and bias). The tiled order is this
+// library's own, described in w4a16_common.cuh.
 #include "w4a16_internal.h"
 
 namespace w4a16 {
@@ -14,6 +16,7 @@ struct RepackSrc {
   const uint32_t *qw[2];
   const uint16_t *sc[2];
   const uint32_t *z[2];
+  const uint16_t *b[2];  // biases (affine form)
   int n_src;     // rows of each source weight
   int gateup;    // 0: one weight, tile T = rows 16T..; 1: tiles alternate gate, up
 };
@@ -67,7 +70,8 @@ __global__ void repack_codes_kernel(RepackSrc s, Layout L, uint32_t *out) {
   }
 }
 
-__global__ void repack_scales_kernel(RepackSrc s, Layout L, uint16_t *out) {
+// scale blocks, or with `bias` the bias blocks of the same layout
+__global__ void repack_scales_kernel(RepackSrc s, Layout L, bool bias, uint16_t *out) {
   const size_t total = (size_t)L.tiles * L.gblocks * 64;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
@@ -80,8 +84,8 @@ __global__ void repack_scales_kernel(RepackSrc s, Layout L, uint16_t *out) {
     const int gi = 4 * blk + j;
     int which;
     const int row = src_row(s, T, g + 8 * h, which);
-    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0
-                                           : s.sc[which][(size_t)row * L.groups + gi];
+    const uint16_t *src = bias ? s.b[which] : s.sc[which];
+    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0 : src[(size_t)row * L.groups + gi];
   }
 }
 
@@ -107,12 +111,15 @@ __global__ void repack_zeros_kernel(RepackSrc s, Layout L, uint8_t *out) {
   }
 }
 
-// w[n][k] = (q - z) * scale through the same unpack as the GEMM kernels
+// w[n][k] = (q - z) * scale (exact), or scale * q + bias rounded once to
+// float32 (affine), through the same unpack as the GEMM kernels
 __global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float *w, UnpackConsts uc) {
   const size_t total = (size_t)L.tiles * L.chunks * 32;
   const uint4 *codes = reinterpret_cast<const uint4 *>(packed + L.codes_off);
   const uint32_t *scales = reinterpret_cast<const uint32_t *>(packed + L.scales_off);
   const uint8_t *zeros = packed + L.zeros_off;
+  const uint32_t *biases = reinterpret_cast<const uint32_t *>(packed + L.biases_off);
+  const bool affine = L.sym == kFormAffine;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
     const int lane = (int)(idx & 31);
@@ -125,7 +132,13 @@ __global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float 
     const uint32_t sw = scales[bi * 4 + (gi & 3)];
     const float s_g = bf16lo_to_f32(sw), s_g8 = bf16hi_to_f32(sw);
     uint32_t zg, zg8;
-    if (L.sym) {
+    float b_g = 0.f, b_g8 = 0.f;
+    if (affine) {
+      zg = zg8 = zero_pair(0);
+      const uint32_t bw = biases[bi * 4 + (gi & 3)];
+      b_g = bf16lo_to_f32(bw);
+      b_g8 = bf16hi_to_f32(bw);
+    } else if (L.sym == kFormSym) {
       zg = zg8 = zero_pair(8);
     } else {
       const uint32_t zb = zeros[bi * 4 + (gi & 3)];
@@ -141,19 +154,20 @@ __global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float 
       unpack_word(words[s], zg, zg8, uc, u);
       const int k = 64 * c + 16 * t + 4 * s;
       // u[0]: row g, k+0 / k+1; u[1]: row g+8, k+0 / k+1; u[2]: row g, k+2 / k+3; u[3]: row g+8
+      // (q - z) * scale + 0 is the exact product; scale * q + bias one rounding
       if (n0 < N) {
         float *r = w + (size_t)n0 * L.K + k;
-        r[0] = bf16lo_to_f32(u[0]) * s_g;
-        r[1] = bf16hi_to_f32(u[0]) * s_g;
-        r[2] = bf16lo_to_f32(u[2]) * s_g;
-        r[3] = bf16hi_to_f32(u[2]) * s_g;
+        r[0] = fmaf(bf16lo_to_f32(u[0]), s_g, b_g);
+        r[1] = fmaf(bf16hi_to_f32(u[0]), s_g, b_g);
+        r[2] = fmaf(bf16lo_to_f32(u[2]), s_g, b_g);
+        r[3] = fmaf(bf16hi_to_f32(u[2]), s_g, b_g);
       }
       if (n1 < N) {
         float *r = w + (size_t)n1 * L.K + k;
-        r[0] = bf16lo_to_f32(u[1]) * s_g8;
-        r[1] = bf16hi_to_f32(u[1]) * s_g8;
-        r[2] = bf16lo_to_f32(u[3]) * s_g8;
-        r[3] = bf16hi_to_f32(u[3]) * s_g8;
+        r[0] = fmaf(bf16lo_to_f32(u[1]), s_g8, b_g8);
+        r[1] = fmaf(bf16hi_to_f32(u[1]), s_g8, b_g8);
+        r[2] = fmaf(bf16lo_to_f32(u[3]), s_g8, b_g8);
+        r[3] = fmaf(bf16hi_to_f32(u[3]), s_g8, b_g8);
       }
     }
   }
@@ -167,8 +181,8 @@ int grid_for(size_t work, int threads) {
 
 }  // namespace
 
-cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0,
-                          const int32_t *qw1, const uint16_t *sc1, const int32_t *z1,
+cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0, const uint16_t *b0,
+                          const int32_t *qw1, const uint16_t *sc1, const int32_t *z1, const uint16_t *b1,
                           int n_src, bool gateup, const Layout &L, uint8_t *packed,
                           cudaStream_t stream) {
   RepackSrc s;
@@ -178,6 +192,8 @@ cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t
   s.sc[1] = sc1 ? sc1 : sc0;
   s.z[0] = reinterpret_cast<const uint32_t *>(z0);
   s.z[1] = reinterpret_cast<const uint32_t *>(z1 ? z1 : z0);
+  s.b[0] = b0;
+  s.b[1] = b1 ? b1 : b0;
   s.n_src = n_src;
   s.gateup = gateup ? 1 : 0;
   const int th = 256;
@@ -186,8 +202,11 @@ cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t
                                                           reinterpret_cast<uint32_t *>(packed + L.codes_off));
   size_t ns = (size_t)L.tiles * L.gblocks * 64;
   repack_scales_kernel<<<grid_for(ns, th), th, 0, stream>>>(
-      s, L, reinterpret_cast<uint16_t *>(packed + L.scales_off));
-  if (!L.sym) {
+      s, L, false, reinterpret_cast<uint16_t *>(packed + L.scales_off));
+  if (L.sym == kFormAffine)
+    repack_scales_kernel<<<grid_for(ns, th), th, 0, stream>>>(
+        s, L, true, reinterpret_cast<uint16_t *>(packed + L.biases_off));
+  if (L.sym == kFormZero) {
     size_t nz = (size_t)L.tiles * L.gblocks * 32;
     repack_zeros_kernel<<<grid_for(nz, th), th, 0, stream>>>(s, L, packed + L.zeros_off);
   }

@@ -27,8 +27,9 @@ namespace w4a16 {
 //
 //  Scales: per tile, per block of four groups, [g 0..7][group j 0..3][h 0..1]
 //  bf16 = scale(row 16T + g + 8h, group 4*blk + j): 128 bytes per block.
-//  Zeros (asymmetric only): per tile and block, [g][j] bytes holding
+//  Zeros (zero-point form only): per tile and block, [g][j] bytes holding
 //  zero(row g) | zero(row g+8) << 4: 32 bytes per block.
+//  Biases (affine form only): the scales' layout with bias for scale.
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 16;
 constexpr int kChunkK = 64;
@@ -36,20 +37,26 @@ constexpr int kChunkBytes = 512;      // 32 lanes x 16 bytes
 constexpr int kScaleBlockBytes = 128; // per tile, per 4 groups
 constexpr int kZeroBlockBytes = 32;
 
+// Weight forms (the `sym` argument of the C ABI):
+//   kFormZero   w = (q - z) * scale, z a packed 4-bit zero point per group
+//   kFormSym    w = (q - 8) * scale
+//   kFormAffine w = scale * q + bias, bias bf16 per group
+constexpr int kFormZero = 0, kFormSym = 1, kFormAffine = 2;
+
 struct Layout {
-  int N, K, group, sym;
+  int N, K, group, sym;  // sym: the form
   int tiles;       // ceil(N / 16)
   int chunks;      // K / 64
   int groups;      // K / group
   int gblocks;     // ceil(groups / 4)
-  size_t codes_off, scales_off, zeros_off, total;
+  size_t codes_off, scales_off, zeros_off, biases_off, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline Layout make_layout(int N, int K, int group, int sym) {
+__host__ __device__ inline Layout make_layout(int N, int K, int group, int form) {
   Layout L;
-  L.N = N; L.K = K; L.group = group; L.sym = sym;
+  L.N = N; L.K = K; L.group = group; L.sym = form;
   L.tiles = (N + kTileRows - 1) / kTileRows;
   L.chunks = K / kChunkK;
   L.groups = K / group;
@@ -57,8 +64,8 @@ __host__ __device__ inline Layout make_layout(int N, int K, int group, int sym) 
   L.codes_off = 0;
   L.scales_off = align_up((size_t)L.tiles * L.chunks * kChunkBytes, 256);
   L.zeros_off = align_up(L.scales_off + (size_t)L.tiles * L.gblocks * kScaleBlockBytes, 256);
-  size_t end = L.zeros_off + (sym ? 0 : (size_t)L.tiles * L.gblocks * kZeroBlockBytes);
-  L.total = align_up(end, 256);
+  L.biases_off = align_up(L.zeros_off + (form == kFormZero ? (size_t)L.tiles * L.gblocks * kZeroBlockBytes : 0), 256);
+  L.total = align_up(L.biases_off + (form == kFormAffine ? (size_t)L.tiles * L.gblocks * kScaleBlockBytes : 0), 256);
   return L;
 }
 

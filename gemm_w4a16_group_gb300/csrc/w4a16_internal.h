@@ -26,13 +26,15 @@ struct GemmCall {
   const uint16_t *x;
   const uint8_t *packed;
   uint16_t *y;
-  int M, N, K, group, sym;
+  int M, N, K, group, sym;  // sym: the form (kFormZero, kFormSym, kFormAffine)
   bool gateup;
   cudaStream_t stream;
   int *err;    // device error word (bounded waits that gave up)
   int device;  // current device ordinal, < kMaxDevices
   bool overlap;  // programmatic overlap with the previous kernel (M <= 16 kernels)
   int64_t *amax = nullptr;  // argmax keys per x row (M <= 16 plain GEMM), or null
+  const float *xsum = nullptr;  // affine form, tcgen05 GEMM: x group sums [K/G][xsum_ld]
+  int xsum_ld = 0;
 };
 
 // Rows covered by the packed buffer of a call (padded; interleaved for gate/up).
@@ -40,8 +42,10 @@ inline int packed_rows(const GemmCall &c) {
   return c.gateup ? 2 * ((c.N + 127) / 128 * 128) : c.N;
 }
 
-cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0,
-                          const int32_t *qw1, const uint16_t *sc1, const int32_t *z1,
+// canonical weight(s) -> tiled layout; z* for the zero-point form, b* (biases)
+// for the affine form, each null otherwise; the second set for gate/up only
+cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0, const uint16_t *b0,
+                          const int32_t *qw1, const uint16_t *sc1, const int32_t *z1, const uint16_t *b1,
                           int n_src, bool gateup, const Layout &L, uint8_t *packed,
                           cudaStream_t stream);
 cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, float *w,
@@ -54,6 +58,9 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count);   // any M
 // y already written, the keys of every row
 cudaError_t launch_argmax_init(int64_t *amax, int M, bool overlap, cudaStream_t stream);
 cudaError_t launch_argmax_finalize(int64_t *amax, int M, bool overlap, cudaStream_t stream);
+// affine form: X[g][m] = sum of x[m][k] over group g, float32 [K/G][xsum_ld(M)]
+int xsum_ld(int M);
+cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, float *xs, cudaStream_t stream);
 cudaError_t launch_row_argmax(const uint16_t *y, int M, int N, int64_t *amax, cudaStream_t stream);
 
 }  // namespace w4a16

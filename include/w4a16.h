@@ -15,11 +15,18 @@
  * (GRIMOIRE v1.8 release notes, "INT4 verify faster" and "INT4 prompt
  * processing").
  *
+ * A third weight form, affine, rebuilds w[n][k] = scale[n][k/G] * q[n][k] +
+ * bias[n][k/G] with a bf16 bias per group in place of the zero point: the MLX
+ * affine 4-bit checkpoints that TensorFold PR #859 runs ("What this changes":
+ * every code keeps its value, scale and bias; groups of 64). Its calls carry
+ * "affine" in their names; the others take zero-point forms only.
+ *
  * Canonical (input) layout, row-major, little-endian:
  *   qweight int32  [N][K/8]            nibble j (bits 4j..4j+3) of word c holds k = 8c + j
  *   scales  bf16   [N][K/G]            bf16 values passed as uint16_t bit patterns
  *   zeros   int32  [N][ceil(K/G/8)]    nibble j of word c holds the zero of group 8c + j
  *                                      (asymmetric only; unused nibbles ignored)
+ *   biases  bf16   [N][K/G]            affine form only
  *
  * Conventions for every call:
  *   - Pointers named x, y, h, qweight, scales, zeros, packed, w_out are DEVICE
@@ -33,7 +40,10 @@
  *     its cudaError_t value (thread-local).
  *   - bf16 values are IEEE bfloat16 bit patterns in uint16_t; outputs are
  *     rounded to nearest-even from float32.
- *   - sym != 0 selects z = 8; then `zeros` is ignored and may be NULL.
+ *   - `sym` names the weight form: 0 = packed zero points, 1 = symmetric
+ *     (z = 8; `zeros` is ignored and may be NULL), W4A16_AFFINE (2) =
+ *     scale * q + bias, accepted only where a comment says so. Any other
+ *     value is W4A16_ERR_INVALID_ARG (size queries return 0).
  *   - Supported sizes: 1 <= M, 1 <= N, 64 <= K, K % G == 0, G in {64, 128},
  *     M, N, K below 2^31 / 16.
  *   - Alignment: x, y, h 16 bytes; packed 256 bytes (cudaMalloc gives both).
@@ -58,11 +68,17 @@ typedef struct CUstream_st *w4a16_stream_t;
 #define W4A16_ERR_CUDA (-4)         /* a CUDA call failed; see w4a16_last_cuda_error() */
 #define W4A16_ERR_TIMEOUT (-5)      /* a bounded wait inside a kernel gave up */
 
+/* Weight forms (the `sym` argument). */
+#define W4A16_ZERO_POINTS 0
+#define W4A16_SYMMETRIC 1
+#define W4A16_AFFINE 2
+
 /*
- * Size in bytes of the repacked weight that w4a16_repack writes for an
- * N x K weight (codes, scales and, when !sym, zero points, each section
+ * Size in bytes of the repacked weight that w4a16_repack (sym 0 or 1) or
+ * w4a16_repack_affine (sym = W4A16_AFFINE) writes for an N x K weight (codes,
+ * scales, and the zero points (sym = 0) or the biases (affine), each section
  * 256-byte aligned; rows padded to a multiple of 16). Returns 0 when the
- * sizes are not supported.
+ * sizes or the form are not supported.
  */
 size_t w4a16_repacked_bytes(int N, int K, int group, int sym);
 
@@ -80,7 +96,8 @@ size_t w4a16_repacked_bytes(int N, int K, int group, int sym);
 int w4a16_repack(const int32_t *qweight, const uint16_t *scales, const int32_t *zeros,
                  int N, int K, int group, int sym, void *packed, w4a16_stream_t stream);
 
-/* Size of the repacked gate/up pair of w4a16_repack_gateup (N_each rows each). */
+/* Size of the repacked gate/up pair of w4a16_repack_gateup or, for sym =
+ * W4A16_AFFINE, w4a16_repack_affine_gateup (N_each rows each). */
 size_t w4a16_gateup_repacked_bytes(int N_each, int K, int group, int sym);
 
 /*
@@ -112,13 +129,6 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,
                w4a16_stream_t stream);
 
 /*
- * Fused feed-forward gate (GRIMOIRE v1.8, "INT4 prompt processing"):
- *   h[M][N_each] = SiLU(x Wg^T) * (x Wu^T),  SiLU(v) = v / (1 + e^-v),
- * with both products accumulated in float32 and never rounded before the
- * SiLU and the product; h is rounded once to bf16. `packed_gateup` comes from
- * w4a16_repack_gateup. Any M >= 1.
- */
-/*
  * Greedy pick over the output columns: argmax[m] = the first n at which the
  * bf16 output y[m][n] of w4a16_gemm (same x, packed, sizes) is largest, as
  * torch.argmax over a bf16 row returns it: among equal values the lowest n;
@@ -141,15 +151,72 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,
 int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym,
                       uint16_t *y, int64_t *argmax, w4a16_stream_t stream);
 
+/*
+ * Fused feed-forward gate (GRIMOIRE v1.8, "INT4 prompt processing"):
+ *   h[M][N_each] = SiLU(x Wg^T) * (x Wu^T),  SiLU(v) = v / (1 + e^-v),
+ * with both products accumulated in float32 and never rounded before the
+ * SiLU and the product; h is rounded once to bf16. `packed_gateup` comes from
+ * w4a16_repack_gateup. Any M >= 1.
+ */
 int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N_each, int K,
                       int group, int sym, uint16_t *h, w4a16_stream_t stream);
 
 /*
  * Test export: w_out[N][K] (float32, row-major) = (q - z) * scale read back
- * from a repacked buffer through the kernels' own unpack. Exact.
+ * from a repacked buffer through the kernels' own unpack (exact), or, for
+ * sym = W4A16_AFFINE, scale * q + bias rounded once to float32.
  */
 int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float *w_out,
                      w4a16_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Affine form: w[n][k] = scale[n][k/G] * q[n][k] + bias[n][k/G]
+ * (TensorFold PR #859, "What this changes" and the AffineN notes). Every
+ * code is used exactly; the products x * q are summed per group on the
+ * tensor cores in float32 and each group adds scale * sum + bias * X[g][m],
+ * X[g][m] = sum over the group of x[m][k]. Sizes, alignment, streams and
+ * errors as for the calls above.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Offline repack of an affine weight: qweight as above, scales and biases
+ * bf16 [N][K/G]. The biases sit in the scales' tiled layout. Writes
+ * w4a16_repacked_bytes(N, K, group, W4A16_AFFINE) bytes; padding rows get
+ * code 0, scale 0 and bias 0.
+ */
+int w4a16_repack_affine(const int32_t *qweight, const uint16_t *scales, const uint16_t *biases, int N, int K,
+                        int group, void *packed, w4a16_stream_t stream);
+
+/* The gate/up pair of w4a16_repack_gateup in the affine form. */
+int w4a16_repack_affine_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const uint16_t *b_gate,
+                               const int32_t *qw_up, const uint16_t *sc_up, const uint16_t *b_up, int N_each,
+                               int K, int group, void *packed, w4a16_stream_t stream);
+
+/*
+ * Group sums of the activations: xsum[g][m] = sum_{k in group g} x[m][k]
+ * (float32, summed in float32), rows of ld = M rounded up to a multiple of
+ * 256 floats; entries m >= M are written as 0. They depend on x alone, so one
+ * table serves every affine weight that reads the same x with the same group
+ * size. `xsum` is caller-owned device memory of w4a16_xsum_bytes(M, K, group)
+ * bytes, 16-byte aligned; w4a16_xsum_bytes returns 0 for unsupported sizes.
+ */
+size_t w4a16_xsum_bytes(int M, int K, int group);
+int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_stream_t stream);
+
+/*
+ * y[M][N] (bf16) = x . (scale * q + bias)^T, W from w4a16_repack_affine.
+ * `xsum` (w4a16_xsum of the same x, K and group, complete when the stream
+ * reaches this call) is read by the tcgen05 GEMM (M > 16); it may be NULL
+ * when M <= 16, where the decode kernel forms the group sums itself with one
+ * more tensor-core product per 16 k (then it is not read).
+ */
+int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, int M, int N, int K, int group,
+                      uint16_t *y, w4a16_stream_t stream);
+
+/* h = SiLU(x Wg^T) * (x Wu^T) as w4a16_gateup_silu, affine weights from
+ * w4a16_repack_affine_gateup; `xsum` as for w4a16_gemm_affine. */
+int w4a16_gateup_silu_affine(const uint16_t *x, const float *xsum, const void *packed_gateup, int M, int N_each,
+                             int K, int group, uint16_t *h, w4a16_stream_t stream);
 
 /*
  * Waits for all work on the current device, then reads and clears the

@@ -7,6 +7,8 @@ v1.8 release notes, "What changed": the output layer checked in one pass, the
 prompt path with the feed-forward gate fused, 4,096-token prompts). Group 128
 with the symmetric zero point 8 is the GPTQ-Int4 checkpoint and group 64 with
 packed 4-bit zero points the AutoRound W4A16 one (v1.7, measurement table).
+The affine workloads take the same shapes in the MLX affine 4-bit form, group
+64 with a bf16 bias per group (TensorFold PR #859, "What this changes").
 """
 from __future__ import annotations
 
@@ -20,6 +22,7 @@ WORKLOADS: dict[str, dict] = {}
 
 def _add(name, **kw):
     kw.setdefault("kind", "gemm")
+    kw.setdefault("affine", False)
     kw.setdefault("scale_range", (0.005, 0.02))
     kw.setdefault("x_scale", 1.0)
     WORKLOADS[name] = kw
@@ -45,15 +48,25 @@ for _M in (1, 5, 16):
 _add("prompt_gateup_m4096_k5120_n17408", M=4096, K=HIDDEN, N=FFN, group=128, sym=True,
      kind="gateup")
 
+# the affine form (scale * q + bias, group 64): decode rows, verify rows, and
+# the prompt with the fused gate
+_add("affine_decode_m1_k5120_n34816", M=1, K=HIDDEN, N=2 * FFN, group=64, sym=False, affine=True)
+_add("affine_smallm_m16_k5120_n34816", M=16, K=HIDDEN, N=2 * FFN, group=64, sym=False, affine=True)
+_add("affine_prompt_gateup_m4096_k5120_n17408", M=4096, K=HIDDEN, N=FFN, group=64, sym=False, affine=True,
+     kind="gateup")
+
 # the configuration the headline throughput line is quoted on
 HEADLINE = "decode_gateup_m1_k5120_n34816"
 
 
-def algorithmic_bytes(M: int, N: int, K: int, group: int, sym: bool) -> int:
-    """Bytes one call must move at least: packed codes, scales, zero points, x and y."""
+def algorithmic_bytes(M: int, N: int, K: int, group: int, sym: bool, affine: bool = False) -> int:
+    """Bytes one call must move at least: packed codes, scales, zero points (or
+    affine biases), x and y."""
     Kg = K // group
     b = N * K // 2 + N * Kg * 2 + M * K * 2 + M * N * 2
-    if not sym:
+    if affine:
+        b += N * Kg * 2
+    elif not sym:
         b += N * Kg // 2
     return b
 
@@ -62,8 +75,8 @@ def gemm_flops(M: int, N: int, K: int) -> int:
     return 2 * M * N * K
 
 
-def gateup_bytes(M: int, N_each: int, K: int, group: int, sym: bool) -> int:
+def gateup_bytes(M: int, N_each: int, K: int, group: int, sym: bool, affine: bool = False) -> int:
     """Bytes a fused gate/up call must move at least: both packed weights with
-    their scales (and zero points), x, and the N_each-wide output h."""
-    w = algorithmic_bytes(0, N_each, K, group, sym)  # one weight, no x or y
+    their scales (and zero points or biases), x, and the N_each-wide output h."""
+    w = algorithmic_bytes(0, N_each, K, group, sym, affine)  # one weight, no x or y
     return 2 * w + M * K * 2 + M * N_each * 2

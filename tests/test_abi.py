@@ -117,3 +117,32 @@ def test_argmax_entry_point_argument_checks(L):
     assert g(P(FAKE), P(FAKE), 4, 64, 96, 64, 1, None, P(FAKE), None) == INVALID      # K % G
     assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, None, P(FAKE + 4), None) == MISALIGNED
     assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, P(FAKE + 2), P(FAKE), None) == MISALIGNED
+
+
+def test_affine_layout_and_argument_checks(L):
+    P = ctypes.c_void_p
+    # the bias section is the scales' size: N=256, K=512, G=128 -> 2048 B
+    assert w4.repacked_bytes(256, 512, 128, w4.AFFINE) == 65536 + 2048 + 2048
+    assert w4.gateup_repacked_bytes(100, 512, 128, w4.AFFINE) == w4.repacked_bytes(256, 512, 128, w4.AFFINE)
+    assert w4.repacked_bytes(256, 512, 128, 3) == 0  # no such form
+    # group sums: K/G rows of M rounded up to 256 floats
+    assert w4.xsum_bytes(17, 512, 64) == 8 * 256 * 4
+    assert w4.xsum_bytes(300, 5120, 128) == 40 * 512 * 4
+    assert w4.xsum_bytes(0, 512, 64) == 0 and w4.xsum_bytes(4, 100, 64) == 0
+    # the zero-point calls reject the affine form, and the affine repack needs biases
+    assert _gemm(L, sym=2) == INVALID
+    assert L.w4a16_gateup_silu(P(FAKE), P(FAKE), 4, 64, 128, 64, 2, P(FAKE), None) == INVALID
+    assert L.w4a16_gemm_argmax(P(FAKE), P(FAKE), 4, 64, 128, 64, 2, None, P(FAKE), None) == INVALID
+    assert L.w4a16_repack(P(FAKE), P(FAKE), P(FAKE), 64, 128, 64, 2, P(FAKE), None) == INVALID
+    assert L.w4a16_repack_affine(P(FAKE), P(FAKE), None, 64, 128, 64, P(FAKE), None) == INVALID
+    assert L.w4a16_repack_affine(P(FAKE), P(FAKE), P(FAKE + 1), 64, 128, 64, P(FAKE), None) == MISALIGNED
+    assert L.w4a16_repack_affine_gateup(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 64, 128, 64,
+                                        P(FAKE), None) == INVALID
+    # M > 16 runs the tcgen05 GEMM, which reads the group sums: they are required
+    ga = L.w4a16_gemm_affine
+    assert ga(P(FAKE), None, P(FAKE), 17, 64, 128, 64, P(FAKE), None) == INVALID
+    assert ga(P(FAKE), P(FAKE + 4), P(FAKE), 17, 64, 128, 64, P(FAKE), None) == MISALIGNED
+    assert ga(P(FAKE), P(FAKE), P(FAKE), 17, 64, 96, 64, P(FAKE), None) == INVALID
+    assert L.w4a16_gateup_silu_affine(P(FAKE), None, P(FAKE), 300, 64, 128, 64, P(FAKE), None) == INVALID
+    assert L.w4a16_xsum(P(FAKE), 4, 128, 64, None, None) == INVALID
+    assert L.w4a16_xsum(P(FAKE), 4, 128, 64, P(FAKE + 8), None) == MISALIGNED

@@ -212,6 +212,8 @@ def run_cuda(args, rank, world):
     parts = []
     if args.argmax and any(w.get("affine", False) for _, w in step_parts(args.workload)):
         raise SystemExit("--argmax takes the zero-point forms only")
+    if args.noalloc and any(not w.get("affine", False) or w["kind"] != "gemm" for _, w in step_parts(args.workload)):
+        raise SystemExit("--noalloc takes the affine plain-GEMM workloads only")
     for name, w in step_parts(args.workload):
         p = new_problem(w)
         units, unit, is_flops = part_units(w)
@@ -263,6 +265,10 @@ def run_cuda(args, rank, world):
                                     w["sym"], stream=s, index_out=pt["idx"])
             return
         xin = pt["x"] if x is None else x
+        if w.get("affine", False) and args.noalloc:
+            w4.gemm_affine_noalloc(xin, pt["packed"][c], w["N"], w["K"], w["group"], out=pt["y"] if y is None else y,
+                                   stream=s)
+            return
         if w.get("affine", False):
             xs = None
             if pt["xs"] is not None:
@@ -372,7 +378,8 @@ def run_cuda(args, rank, world):
         "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
                    "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
-                   "parallelism": f"replicas x{world}", "output": "argmax" if args.argmax else "y", "launch": ("eager" if args.eager else "cuda graph")
+                   "parallelism": f"replicas x{world}", "output": "argmax" if args.argmax else "y",
+                   "entry": "w4a16_gemm_affine_noalloc" if args.noalloc else "default", "launch": ("eager" if args.eager else "cuda graph")
                    + ("" if args.no_overlap else ", programmatic overlap"),
                    "per_call_ms": [round(v, 5) for v in per_call_ms]},
         "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
@@ -476,6 +483,8 @@ def main():
     ap.add_argument("--no-overlap", action="store_true", help="no programmatic overlap between decode calls")
     ap.add_argument("--argmax", action="store_true",
                     help="time the fused argmax (w4a16_gemm_argmax, no logits stored) instead of the GEMM")
+    ap.add_argument("--noalloc", action="store_true",
+                    help="affine plain GEMM through w4a16_gemm_affine_noalloc (group sums in the library's array)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],

@@ -28,6 +28,7 @@ __all__ = [
     "repack", "repack_gateup", "gemm", "gemm_argmax", "gateup_silu", "dequantize", "kernel_status",
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
     "AFFINE", "repack_affine", "repack_affine_gateup", "xsum_bytes", "xsum", "gemm_affine", "gateup_silu_affine",
+    "gemm_affine_noalloc",
 ]
 
 # symbols declared in include/w4a16.h
@@ -36,7 +37,7 @@ EXPORTS = (
     "w4a16_gemm", "w4a16_gemm_argmax", "w4a16_gateup_silu", "w4a16_dequantize", "w4a16_kernel_status",
     "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
     "w4a16_set_programmatic_overlap", "w4a16_repack_affine", "w4a16_repack_affine_gateup", "w4a16_xsum_bytes",
-    "w4a16_xsum", "w4a16_gemm_affine", "w4a16_gateup_silu_affine",
+    "w4a16_xsum", "w4a16_gemm_affine", "w4a16_gateup_silu_affine", "w4a16_gemm_affine_noalloc",
 )
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC = 0, 1, 2, 3
 # the `sym` argument: 0 zero points, 1 symmetric (z = 8), AFFINE scale * q + bias
@@ -107,6 +108,8 @@ def lib(auto_build: bool = True) -> ctypes.CDLL:
     L.w4a16_gemm_affine.restype = i32
     L.w4a16_gateup_silu_affine.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
     L.w4a16_gateup_silu_affine.restype = i32
+    L.w4a16_gemm_affine_noalloc.argtypes = [P, P, i32, i32, i32, i32, P, P]
+    L.w4a16_gemm_affine_noalloc.restype = i32
     _lib = L
     return L
 
@@ -308,6 +311,21 @@ def gemm_affine(x, packed, N, K, group, xs=None, out=None, stream=None):
     rc = lib().w4a16_gemm_affine(_ptr(x, _bf16_types(), "x"), _xs_ptr(xs), _ptr(packed, (torch.uint8,), "packed"),
                                  M, N, K, group, _ptr(out, _bf16_types(), "out"), _stream(stream))
     _check(rc, "w4a16_gemm_affine")
+    return out
+
+
+def gemm_affine_noalloc(x, packed, N, K, group, out=None, stream=None):
+    """gemm_affine with the group sums in the library's fixed device array (no
+    table argument; calls in flight at once on one device race on it)."""
+    torch = _torch()
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, K]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    rc = lib().w4a16_gemm_affine_noalloc(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), M, N,
+                                         K, group, _ptr(out, _bf16_types(), "out"), _stream(stream))
+    _check(rc, "w4a16_gemm_affine_noalloc")
     return out
 
 

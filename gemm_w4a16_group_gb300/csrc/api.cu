@@ -20,12 +20,18 @@ std::atomic<int> g_overlap{0};
 // Device error word set by kernels whose bounded waits gave up.
 __device__ int g_kernel_error;
 
+// Fixed table of x group sums for w4a16_gemm_affine_noalloc (4 MiB per device,
+// part of the module image: nothing is allocated at run time).
+constexpr size_t kNoAllocXsumBytes = size_t(4) << 20;
+static __device__ __align__(256) float g_noalloc_xsum[kNoAllocXsumBytes / sizeof(float)];
+
 struct DeviceInfo {
   int device = 0;
   bool ready = false;
   int status = W4A16_OK;
   int sm_count = 0;
   int *err = nullptr;
+  float *noalloc_xsum = nullptr;  // this device's copy of g_noalloc_xsum
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -55,6 +61,8 @@ int current_device(DeviceInfo &out) {
       void *p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_kernel_error)) != cudaSuccess) return cuda_fail(e);
       d.err = static_cast<int *>(p);
+      if ((e = cudaGetSymbolAddress(&p, g_noalloc_xsum)) != cudaSuccess) return cuda_fail(e);
+      d.noalloc_xsum = static_cast<float *>(p);
       d.sm_count = sms;
       d.status = W4A16_OK;
     }
@@ -265,6 +273,26 @@ int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, 
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, kFormAffine, false,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
   return launch_affine(c, xsum, d);
+}
+
+int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int group, uint16_t *y,
+                              w4a16_stream_t stream) {
+  if (!x || !packed || !y) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
+  const bool tc = affine_uses_tc(M);
+  if (tc && w4a16_xsum_bytes(M, K, group) > kNoAllocXsumBytes) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, kFormAffine, false, s, d.err, d.device,
+             g_overlap.load() != 0};
+  if (!tc) return launch_affine(c, nullptr, d);
+  // every entry the GEMM reads (padding included) is written by this pre-pass
+  cudaError_t e = launch_xsum(x, M, K, group, d.noalloc_xsum, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return launch_affine(c, d.noalloc_xsum, d);
 }
 
 int w4a16_gateup_silu_affine(const uint16_t *x, const float *xsum, const void *packed_gateup, int M, int N_each,

@@ -213,6 +213,23 @@ int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_st
 int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, int M, int N, int K, int group,
                       uint16_t *y, w4a16_stream_t stream);
 
+/*
+ * w4a16_gemm_affine without the caller's group-sum table: this library's own
+ * addition, with no counterpart on the pages the method comes from. For
+ * M > 16 the group sums go to a fixed 4 MiB device array inside the library's
+ * module image (one per device, found once with cudaGetSymbolAddress), so the
+ * call allocates nothing and needs no workspace argument; sizes whose table
+ * (w4a16_xsum_bytes) exceeds 4 MiB are W4A16_ERR_INVALID_ARG (at K = 5120 and
+ * group 64, M up to 13,056). Every entry the GEMM reads, the zero padding
+ * included, is written by the call itself before the GEMM reads it, so
+ * nothing has to start at zero. The array is shared: calls in flight at the
+ * same time on one device (other streams, other host threads) race on it and
+ * may compute wrong results; calls in order on one stream are safe. M <= 16
+ * uses no table and behaves exactly as w4a16_gemm_affine.
+ */
+int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int group, uint16_t *y,
+                              w4a16_stream_t stream);
+
 /* h = SiLU(x Wg^T) * (x Wu^T) as w4a16_gateup_silu, affine weights from
  * w4a16_repack_affine_gateup; `xsum` as for w4a16_gemm_affine. */
 int w4a16_gateup_silu_affine(const uint16_t *x, const float *xsum, const void *packed_gateup, int M, int N_each,

@@ -54,6 +54,9 @@ _add("affine_decode_m1_k5120_n34816", M=1, K=HIDDEN, N=2 * FFN, group=64, sym=Fa
 _add("affine_smallm_m16_k5120_n34816", M=16, K=HIDDEN, N=2 * FFN, group=64, sym=False, affine=True)
 _add("affine_prompt_gateup_m4096_k5120_n17408", M=4096, K=HIDDEN, N=FFN, group=64, sym=False, affine=True,
      kind="gateup")
+# the same prompt rows through the plain GEMM of the 34,816 gate+up rows (the
+# form w4a16_gemm_affine_noalloc runs)
+_add("affine_prompt_m4096_k5120_n34816", M=4096, K=HIDDEN, N=2 * FFN, group=64, sym=False, affine=True)
 
 # the configuration the headline throughput line is quoted on
 HEADLINE = "decode_gateup_m1_k5120_n34816"

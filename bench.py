@@ -199,7 +199,7 @@ def run_cuda(args, rank, world):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     w4.lib()
-    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3}[args.kernel])
+    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3, "xstaged": 4}[args.kernel])
     # decode calls stream their (read-only, already complete) weights while
     # the previous kernel finishes; x and y wait for it
     w4.set_programmatic_overlap(not args.no_overlap)
@@ -487,7 +487,7 @@ def main():
                     help="affine plain GEMM through w4a16_gemm_affine_noalloc (group sums in the library's array)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc", "xstaged"],
                     help="kernel override for A/B measurement (default: automatic choice)")
     args = ap.parse_args()
     if args.print_source_hash:

@@ -27,6 +27,7 @@ __all__ = [
     "EXPORTS", "W4A16Error", "lib", "library_path", "repacked_bytes", "gateup_repacked_bytes",
     "repack", "repack_gateup", "gemm", "gemm_argmax", "gateup_silu", "dequantize", "kernel_status",
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
+    "KERNEL_XSTAGED",
     "AFFINE", "repack_affine", "repack_affine_gateup", "xsum_bytes", "xsum", "gemm_affine", "gateup_silu_affine",
     "gemm_affine_noalloc",
 ]
@@ -39,7 +40,7 @@ EXPORTS = (
     "w4a16_set_programmatic_overlap", "w4a16_repack_affine", "w4a16_repack_affine_gateup", "w4a16_xsum_bytes",
     "w4a16_xsum", "w4a16_gemm_affine", "w4a16_gateup_silu_affine", "w4a16_gemm_affine_noalloc",
 )
-KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC, KERNEL_XSTAGED = 0, 1, 2, 3, 4
 # the `sym` argument: 0 zero points, 1 symmetric (z = 8), AFFINE scale * q + bias
 AFFINE = 2
 

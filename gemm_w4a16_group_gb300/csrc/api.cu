@@ -84,6 +84,15 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int finish_launch(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : cuda_fail(e); }
 
+// The M <= 16 kernels: override 2 keeps the per-warp-ring kernel, override 4
+// forces the x-staged one, otherwise the x-staged kernel takes M <= 8 calls
+// whose grid fills a wave
+cudaError_t launch_decode_kernel(GemmCall &c, int sm_count) {
+  const int ov = g_override.load();
+  c.xs_mode = ov == 4 ? 2 : ov == 2 ? 0 : 1;
+  return launch_smallm_mma(c, sm_count);
+}
+
 bool form_ok(int form) { return form == kFormZero || form == kFormSym || form == kFormAffine; }
 bool zero_form(int form) { return form == kFormZero || form == kFormSym; }
 
@@ -92,7 +101,7 @@ bool zero_form(int form) { return form == kFormZero || form == kFormSym; }
 bool affine_uses_tc(int M) { return M > 16 || g_override.load() == 3; }
 
 int launch_affine(GemmCall &c, const float *xsum, const DeviceInfo &d) {
-  if (!affine_uses_tc(c.M)) return finish_launch(launch_smallm_mma(c, d.sm_count));
+  if (!affine_uses_tc(c.M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
   c.xsum = xsum;
   c.xsum_ld = xsum_ld(c.M);
   return finish_launch(launch_prompt_tc(c, d.sm_count));
@@ -202,7 +211,7 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
   const int ov = g_override.load();
   if (M == 1 && ov == 1) return finish_launch(launch_gemv_m1(c, d.sm_count));
-  if (M <= 16 && ov != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
+  if (M <= 16 && ov != 3) return finish_launch(launch_decode_kernel(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
@@ -217,7 +226,7 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym, true,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
-  if (M <= 16 && g_override.load() != 3) return finish_launch(launch_smallm_mma(c, d.sm_count));
+  if (M <= 16 && g_override.load() != 3) return finish_launch(launch_decode_kernel(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
@@ -237,7 +246,7 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym, false, s, d.err, d.device, overlap};
   if (M <= 16 && g_override.load() != 3) {
     c.amax = argmax;  // keys from the decode kernel's epilogue; y may be NULL
-    e = launch_smallm_mma(c, d.sm_count);
+    e = launch_decode_kernel(c, d.sm_count);
   } else {
     e = launch_prompt_tc(c, d.sm_count);
     if (e == cudaSuccess) e = launch_row_argmax(y, M, N, argmax, s);
@@ -354,7 +363,7 @@ const char *w4a16_strerror(int status) {
 int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
 
 int w4a16_set_kernel_override(int which) {
-  if (which < 0 || which > 3) return -1;
+  if (which < 0 || which > 4) return -1;
   return g_override.exchange(which);
 }
 

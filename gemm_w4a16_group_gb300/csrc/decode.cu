@@ -118,6 +118,14 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
+// same copy without a cache hint: x is read by every CTA, so it stays in L2
+__device__ __forceinline__ void bulk_copy_keep(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -244,6 +252,39 @@ __device__ __forceinline__ bool reduce_partials(float (*red)[E]) {
         s += v;
       }
       red[0][e] = s;
+    }
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+  __syncthreads();
+  return rank == 0;
+}
+
+// Partials red[e] of every CTA of a cluster summed into rank 0's, in rank
+// order. Returns true in the CTA that writes the outputs.
+template <int E>
+__device__ __forceinline__ bool cluster_sum(float *red) {
+  if (gridDim.y == 1) {
+    __syncthreads();
+    return true;
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  if (rank == 0) {
+    const uint32_t nranks = gridDim.y;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float s = red[e];
+      const uint32_t local = smem_u32(&red[e]);
+      for (uint32_t r = 1; r < nranks; ++r) {
+        uint32_t remote;
+        float v;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(r));
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+        s += v;
+      }
+      red[e] = s;
     }
   }
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -490,6 +531,317 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
   }
   if (!GATEUP && p.amax) {
     // one global arrival per x row and CTA: the largest key of this CTA's outputs
+    __syncthreads();
+    if (threadIdx.x < p.M && best[threadIdx.x] != 0) atomicMax(p.amax + threadIdx.x, best[threadIdx.x]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// small-M tensor-core kernel with x staged once per CTA
+//
+// At M >= 2 the x rows of a call (80 KB at M = 8, 160 KB at M = 16, K = 5120)
+// no longer stay in L1 beside the weight rings, and per-warp 16-byte x loads
+// from L2 stall the warps. Here the four compute warps of a CTA work on
+// different tiles of the same K range, so one copy of each 256-wide K unit of
+// x serves all of them: a fifth warp fills a ring of slots, each holding one
+// K unit of every tile's codes, scale (and zero or bias) blocks and the x rows
+// (bulk asynchronous copies, one mbarrier per slot for the bytes, one per slot
+// for the four warps' release). x rows sit 528 bytes apart, so the 16-byte B
+// fragment loads of a warp touch 32 distinct banks. K is split only across
+// the CTAs of a cluster.
+// ---------------------------------------------------------------------------
+constexpr int kXsWarps = 4;  // compute warps; warp kXsWarps issues the copies
+constexpr int kXsThreads = (kXsWarps + 1) * 32;
+constexpr int kXsSlots = 2;
+constexpr int kXRowStride = kUnitChunks * 128 + 16;
+
+template <int MT, int TPW, int QF>
+struct XsSmem {
+  static constexpr int kTiles = kXsWarps * TPW;  // 16-row tiles of a CTA
+  static constexpr int kTileCode = kUnitChunks * kChunkBytes;
+  static constexpr int kThird = QF == kFormZero ? kZeroBlockBytes : QF == kFormAffine ? kScaleBlockBytes : 0;
+  static constexpr int kScaleOff = kTiles * kTileCode;
+  static constexpr int kThirdOff = kScaleOff + kTiles * kScaleBlockBytes;
+  static constexpr int kXOff = kThirdOff + kTiles * kThird;
+  static constexpr int kXRows = 8 * MT;
+  static constexpr int kSlotBytes = (kXOff + kXRows * kXRowStride + 127) / 128 * 128;
+  static constexpr int kCopies = kTiles * (QF == kFormSym ? 2 : 3);  // weight copies per unit (+ x rows)
+  static constexpr int E = kTiles * MT * 128;  // partial sums of the CTA
+  static constexpr int kRingOff = 0;
+  static constexpr int kRedOff = 0;  // the partials reuse the ring once every unit is consumed
+  static constexpr int kBarOff = kXsSlots * kSlotBytes;  // full[s], then empty[s]
+  static constexpr int kBestOff = kBarOff + 2 * kXsSlots * 8;
+  static constexpr int kFlagOff = kBestOff + 16 * 8;
+  static constexpr int kBytes = kFlagOff + 16;
+  static_assert(E * 4 <= kXsSlots * kSlotBytes, "partials fit in the ring");
+  static_assert(kXOff % 16 == 0 && kSlotBytes % 128 == 0, "bulk copy destinations");
+};
+
+template <int MT, int TPW, int QF, int CPG, bool GATEUP>
+__global__ void __launch_bounds__(kXsThreads) smallm_xs_kernel(DecodeParams p) {
+  using S = XsSmem<MT, TPW, QF>;
+  constexpr int E = S::E;
+  constexpr int GPU = kUnitChunks / CPG;  // groups per full unit
+  constexpr bool AFF = QF == kFormAffine;
+  extern __shared__ __align__(128) uint8_t smem[];
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlagOff);
+  unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + S::kBestOff);
+  const uint32_t ring = smem_u32(smem + S::kRingOff);
+  const uint32_t full0 = smem_u32(smem + S::kBarOff), empty0 = full0 + 8 * kXsSlots;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int tile_base = blockIdx.x * S::kTiles;
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kXsSlots; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kXsWarps);
+    }
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 16) best[threadIdx.x] = 0;
+  __syncthreads();
+  // this CTA's K units: the cluster ranks split K
+  const int ub = (int)((long long)p.units * blockIdx.y / gridDim.y);
+  const int ue = (int)((long long)p.units * (blockIdx.y + 1) / gridDim.y);
+  const int nu = ue - ub;
+
+  float acc[TPW][MT][4];
+#pragma unroll
+  for (int i = 0; i < TPW; ++i)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][mt][r] = 0.f;
+
+  if (warp == kXsWarps) {
+    // ------------------------------------------------------------ copies
+    const uint64_t policy = evict_first_policy();
+    // copy q of a unit: q < kTiles codes, then scale blocks, then zero/bias
+    // blocks, then (q - kCopies) an x row
+    auto issue = [&](int s, int u, bool weights, bool xrows) {
+      const int nch = min(kUnitChunks, p.chunks - kUnitChunks * u);
+      const uint32_t slot = ring + s * S::kSlotBytes;
+      const uint32_t bar = full0 + 8 * s;
+      const int upb = 4 * CPG / kUnitChunks;  // units per scale block
+      const int nq = S::kCopies + p.M;
+      for (int q = lane; q < nq; q += 32) {
+        if (q < S::kCopies) {
+          if (!weights) continue;
+          const int kind = q / S::kTiles, i = q % S::kTiles;
+          const size_t tile = (size_t)min(tile_base + i, p.tiles - 1);
+          if (kind == 0)
+            bulk_copy(slot + i * S::kTileCode, p.codes + (tile * p.chunks + (size_t)kUnitChunks * u) * kChunkBytes,
+                      nch * kChunkBytes, bar, policy);
+          else if (kind == 1)
+            bulk_copy(slot + S::kScaleOff + i * kScaleBlockBytes,
+                      p.scales + (tile * p.gblocks + (size_t)(u / upb)) * kScaleBlockBytes, kScaleBlockBytes, bar,
+                      policy);
+          else
+            bulk_copy(slot + S::kThirdOff + i * S::kThird,
+                      p.zeros + (tile * p.gblocks + (size_t)(u / upb)) * S::kThird, S::kThird, bar, policy);
+        } else if (xrows) {
+          const int m = q - S::kCopies;
+          bulk_copy_keep(slot + S::kXOff + m * kXRowStride, p.x + (size_t)m * p.K + (size_t)kUnitChunks * 64 * u,
+                         nch * 128, bar);
+        }
+      }
+    };
+    auto tx_bytes = [&](int u) {
+      const int nch = min(kUnitChunks, p.chunks - kUnitChunks * u);
+      return (uint32_t)(S::kTiles * (nch * kChunkBytes + kScaleBlockBytes + S::kThird) + p.M * nch * 128);
+    };
+    // the weights of the first slots stream before the previous kernel has
+    // finished (programmatic overlap); x only after it
+    const int first = min(kXsSlots, nu);
+    for (int it = 0; it < first; ++it) {
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * it, tx_bytes(ub + it));
+      __syncwarp();
+      issue(it, ub + it, true, false);
+    }
+    grid_launch_dependents();
+    grid_dependency_wait();
+    for (int it = 0; it < first; ++it) issue(it, ub + it, false, true);
+    int issued = first;
+    bool ok = true;
+    for (; issued < nu; ++issued) {
+      const int s = issued % kXsSlots;
+      // every compute warp has released the slot (its previous unit)
+      bool got = true;
+      if (lane == 0) got = mbar_wait(empty0 + 8 * s, ((issued / kXsSlots) - 1) & 1, abort_flag);
+      got = __shfl_sync(0xFFFFFFFFu, got, 0);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async_smem();
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, tx_bytes(ub + issued));
+      __syncwarp();
+      issue(s, ub + issued, true, true);
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      atomicExch(p.err, kErrTimeout);
+    }
+    // every copy issued has landed before the slots are reused for the partials
+    if (lane == 0)
+      for (int it = max(0, issued - kXsSlots); it < issued; ++it)
+        mbar_wait_drain(full0 + 8 * (it % kXsSlots), (it / kXsSlots) & 1);
+  } else {
+    // ------------------------------------------------------------ compute warps
+    grid_launch_dependents();
+    grid_dependency_wait();
+    for (int it = 0; it < nu; ++it) {
+      const int u = ub + it;
+      const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);
+      const int s = it % kXsSlots;
+      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, (it / kXsSlots) & 1, abort_flag));
+      if (!got) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicExch(p.err, kErrTimeout);
+        }
+        break;
+      }
+      const uint32_t sl = ring + s * S::kSlotBytes;
+      // B fragment column g + 8 mt reads x row min(g + 8 mt, M - 1)
+      uint32_t xrow[MT];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        xrow[mt] = sl + S::kXOff + min(g + 8 * mt, p.M - 1) * kXRowStride + t * 32;
+#pragma unroll
+      for (int j = 0; j < GPU; ++j) {
+        if (j < ngu) {
+          const int gg = u * GPU + j;
+          uint32_t zg[TPW], zg8[TPW];
+#pragma unroll
+          for (int i = 0; i < TPW; ++i) {
+            if (QF != kFormZero) {
+              zg[i] = zg8[i] = zero_pair(AFF ? 0 : 8);
+            } else {
+              const uint32_t zb = lds8(sl + S::kThirdOff + (warp * TPW + i) * kZeroBlockBytes + g * 4 + (gg & 3));
+              zg[i] = zero_pair(zb & 0xF);
+              zg8[i] = zero_pair(zb >> 4);
+            }
+          }
+          float part[TPW][MT][4];
+          float xs[MT][4];  // affine: the group's sum of x per column (all-ones A)
+#pragma unroll
+          for (int cc = 0; cc < CPG; ++cc) {
+            const int cl = j * CPG + cc;  // chunk within the unit
+            uint4 xx[MT][2];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              xx[mt][0] = lds128(xrow[mt] + cl * 128);
+              xx[mt][1] = lds128(xrow[mt] + cl * 128 + 16);
+            }
+            uint4 w[TPW];
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+              w[i] = lds128(sl + (warp * TPW + i) * S::kTileCode + (cl * 32 + lane) * 16);
+#pragma unroll
+            for (int st = 0; st < 4; ++st) {
+              uint32_t b0[MT], b1[MT];
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                b0[mt] = word_of(xx[mt][st >> 1], 2 * (st & 1));
+                b1[mt] = word_of(xx[mt][st >> 1], 2 * (st & 1) + 1);
+              }
+              if (AFF) {
+                const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  if (cc == 0 && st == 0)
+                    mma_bf16_16816_zero(xs[mt], ones, b0[mt], b1[mt]);
+                  else
+                    mma_bf16_16816(xs[mt], ones, b0[mt], b1[mt]);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < TPW; ++i) {
+                uint32_t a[4];
+                unpack_word(word_of(w[i], st), zg[i], zg8[i], p.uc, a);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  if (cc == 0 && st == 0)
+                    mma_bf16_16816_zero(part[i][mt], a, b0[mt], b1[mt]);
+                  else
+                    mma_bf16_16816(part[i][mt], a, b0[mt], b1[mt]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < TPW; ++i) {
+            const uint32_t blk = (warp * TPW + i) * kScaleBlockBytes + g * 16 + (gg & 3) * 4;
+            const uint32_t sw = lds32(sl + S::kScaleOff + blk);
+            const float sg = bf16lo_to_f32(sw), sg8 = bf16hi_to_f32(sw);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              acc[i][mt][0] = fmaf(sg, part[i][mt][0], acc[i][mt][0]);
+              acc[i][mt][1] = fmaf(sg, part[i][mt][1], acc[i][mt][1]);
+              acc[i][mt][2] = fmaf(sg8, part[i][mt][2], acc[i][mt][2]);
+              acc[i][mt][3] = fmaf(sg8, part[i][mt][3], acc[i][mt][3]);
+            }
+            if (AFF) {
+              const uint32_t bw = lds32(sl + S::kThirdOff + blk);
+              const float bg = bf16lo_to_f32(bw), bg8 = bf16hi_to_f32(bw);
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                acc[i][mt][0] = fmaf(bg, xs[mt][0], acc[i][mt][0]);
+                acc[i][mt][1] = fmaf(bg, xs[mt][1], acc[i][mt][1]);
+                acc[i][mt][2] = fmaf(bg8, xs[mt][2], acc[i][mt][2]);
+                acc[i][mt][3] = fmaf(bg8, xs[mt][3], acc[i][mt][3]);
+              }
+            }
+          }
+        }
+      }
+      // this warp is done with the slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+  }
+
+  // partials into the (now idle) ring, then the cluster's ranks are summed
+  __syncthreads();
+  float *red = reinterpret_cast<float *>(smem + S::kRedOff);
+  if (warp < kXsWarps) {
+#pragma unroll
+    for (int i = 0; i < TPW; ++i)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) red[(((warp * TPW + i) * MT + mt) * 4 + r) * 32 + lane] = acc[i][mt][r];
+  }
+  if (!cluster_sum<E>(red)) return;
+
+  // element e = ((ti*MT + mt)*4 + r)*32 + lane, ti = the CTA's tile index:
+  //   row n = 16*(tile_base+ti) + g + 8*(r>>1), column m = 8*mt + 2t + (r&1)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int ln = e & 31, r = (e >> 5) & 3, im = e >> 7;
+    const int mt = im % MT, ti = im / MT;
+    const int m = 8 * mt + 2 * (ln & 3) + (r & 1);
+    const int nl = (ln >> 2) + 8 * (r >> 1);
+    if (m >= p.M) continue;
+    if (GATEUP) {
+      if (ti & 1) continue;
+      const int n = 16 * ((tile_base + ti) >> 1) + nl;
+      if (n < p.N) {
+        const float gv = red[e], uv = red[e + MT * 4 * 32];
+        p.y[(size_t)m * p.ld + n] = f32_to_bf16_bits(silu_f32(gv) * uv);
+      }
+    } else {
+      const int n = 16 * (tile_base + ti) + nl;
+      if (n < p.N) {
+        const uint16_t v = f32_to_bf16_bits(red[e]);
+        if (p.y) p.y[(size_t)m * p.ld + n] = v;
+        if (p.amax) atomicMax(best + m, argmax_key(v, n));
+      }
+    }
+  }
+  if (!GATEUP && p.amax) {
     __syncthreads();
     if (threadIdx.x < p.M && best[threadIdx.x] != 0) atomicMax(p.amax + threadIdx.x, best[threadIdx.x]);
   }
@@ -762,6 +1114,77 @@ cudaError_t run_mma_all(const DecodeParams &p, int sm_count, int form, int group
   return run_mma_g<kFormZero, GATEUP>(p, sm_count, group, s);
 }
 
+// x-staged kernel: CTAs of kXsWarps * TPW tiles; the same split-K rule over
+// the cluster's CTAs (at least two K units each). With `only_full`, nothing is
+// launched (and *launched stays false) unless the grid covers a whole wave:
+// graph-timed, the kernel is 3-8 % faster than the per-warp-ring kernel on
+// the 248,320-row head at M = 1-8 and at N = 131072, and 20-35 % slower on
+// grids below a wave (N <= 65536), where four times fewer CTAs hide less
+// latency.
+template <int MT, int TPW, int QF, int CPG, bool GATEUP>
+cudaError_t run_xs(const DecodeParams &p, int sm_count, cudaStream_t s, bool only_full, bool *launched) {
+  using S = XsSmem<MT, TPW, QF>;
+  auto kern = smallm_xs_kernel<MT, TPW, QF, CPG, GATEUP>;
+  static PerDevice occ_cache;
+  int occ = occ_cache.v[p.device].load(std::memory_order_relaxed);
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+    if (e != cudaSuccess) return e;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kXsThreads, S::kBytes) != cudaSuccess || occ < 1)
+      occ = 1;
+    occ_cache.v[p.device].store(occ, std::memory_order_relaxed);
+  }
+  const long long ctas = (p.tiles + S::kTiles - 1) / S::kTiles;
+  const long long resident = (long long)occ * sm_count;
+  if (only_full && ctas < resident) return cudaSuccess;
+  *launched = true;
+  int kc = 1;
+  while (kc < 8 && ctas * kc * 2 <= resident && p.units >= kc * 2 * 2) kc *= 2;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)ctas, kc, 1);
+  lc.blockDim = dim3(kXsThreads, 1, 1);
+  lc.dynamicSmemBytes = S::kBytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (kc > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = kc;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (p.overlap) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  lc.attrs = attr;
+  lc.numAttrs = na;
+  return cudaLaunchKernelEx(&lc, kern, p);
+}
+
+template <int QF, int CPG, bool GATEUP>
+cudaError_t run_xs_m(const DecodeParams &p, int sm_count, cudaStream_t s, bool only_full, bool *launched) {
+  if (p.M <= 8) return run_xs<1, 2, QF, CPG, GATEUP>(p, sm_count, s, only_full, launched);
+  return run_xs<2, 2, QF, CPG, GATEUP>(p, sm_count, s, only_full, launched);
+}
+
+template <int QF, bool GATEUP>
+cudaError_t run_xs_g(const DecodeParams &p, int sm_count, int group, cudaStream_t s, bool only_full,
+                     bool *launched) {
+  return group == 64 ? run_xs_m<QF, 1, GATEUP>(p, sm_count, s, only_full, launched)
+                     : run_xs_m<QF, 2, GATEUP>(p, sm_count, s, only_full, launched);
+}
+
+template <bool GATEUP>
+cudaError_t run_xs_all(const DecodeParams &p, int sm_count, int form, int group, cudaStream_t s, bool only_full,
+                       bool *launched) {
+  if (form == kFormSym) return run_xs_g<kFormSym, GATEUP>(p, sm_count, group, s, only_full, launched);
+  if (form == kFormAffine) return run_xs_g<kFormAffine, GATEUP>(p, sm_count, group, s, only_full, launched);
+  return run_xs_g<kFormZero, GATEUP>(p, sm_count, group, s, only_full, launched);
+}
+
 template <bool SYM, int CPG>
 cudaError_t run_gemv(const DecodeParams &p, int sm_count, cudaStream_t s) {
   constexpr int TPW = 2, SLOTS = slots_for(TPW);
@@ -778,6 +1201,14 @@ cudaError_t run_gemv(const DecodeParams &p, int sm_count, cudaStream_t s) {
 cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(packed_rows(c), c.K, c.group, c.sym);
   DecodeParams p = make_params(c, L);
+  // the x-staged kernel: forced, or chosen for M <= 8 when its grid fills a wave
+  if (c.xs_mode == 2 || (c.xs_mode == 1 && c.M <= 8)) {
+    bool launched = false;
+    const bool only_full = c.xs_mode == 1;
+    const cudaError_t e = c.gateup ? run_xs_all<true>(p, sm_count, c.sym, c.group, c.stream, only_full, &launched)
+                                   : run_xs_all<false>(p, sm_count, c.sym, c.group, c.stream, only_full, &launched);
+    if (e != cudaSuccess || launched) return e;
+  }
   if (c.gateup) return run_mma_all<true>(p, sm_count, c.sym, c.group, c.stream);
   return run_mma_all<false>(p, sm_count, c.sym, c.group, c.stream);
 }

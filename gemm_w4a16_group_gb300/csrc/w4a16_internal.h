@@ -35,6 +35,7 @@ struct GemmCall {
   int64_t *amax = nullptr;  // argmax keys per x row (M <= 16 plain GEMM), or null
   const float *xsum = nullptr;  // affine form, tcgen05 GEMM: x group sums [K/G][xsum_ld]
   int xsum_ld = 0;
+  int xs_mode = 1;  // M <= 16, the kernel that stages x once per CTA: 0 never, 1 when it fits, 2 always
 };
 
 // Rows covered by the packed buffer of a call (padded; interleaved for gate/up).

@@ -119,9 +119,11 @@ int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const i
  * float32 accumulation; each group's partial sum is scaled in float32.
  * `scales` and `zeros` are reserved: scales and zero points travel inside
  * `packed`, and both must be NULL (else W4A16_ERR_INVALID_ARG).
- * Kernel choice: M <= 16 -> the decode kernel (each weight read and unpacked
- * once for all rows, multiply-adds on the tensor core); M > 16 -> the tcgen05
- * GEMM. A CUDA-core one-row GEMV is selectable (w4a16_set_kernel_override).
+ * Kernel choice: M <= 16 -> a decode kernel (each weight read and unpacked
+ * once for all rows, multiply-adds on the tensor core): the one that stages x
+ * once per CTA when M <= 8 and its grid fills the GPU, else the one with a
+ * weight ring per warp; M > 16 -> the tcgen05 GEMM. A CUDA-core one-row GEMV
+ * is selectable (w4a16_set_kernel_override).
  * Results are bitwise reproducible run to run (no atomics in any sum).
  */
 int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,
@@ -251,8 +253,11 @@ int w4a16_last_cuda_error(void);
 
 /*
  * Kernel selection override for A/B measurement: 0 = automatic (default),
- * 1 = force the CUDA-core one-row GEMV for M = 1, 2 = force the small-M
- * tensor-core kernel for M <= 16, 3 = force the tcgen05 GEMM for any M.
+ * 1 = force the CUDA-core one-row GEMV for M = 1 (zero-point forms), 2 = force
+ * the small-M tensor-core kernel with per-warp weight rings for M <= 16, 3 =
+ * force the tcgen05 GEMM for any M, 4 = force the small-M kernel that stages x
+ * once per CTA for M <= 16 (automatic choice: M <= 8 calls whose grid of
+ * 128-row CTAs fills the GPU, e.g. the output-vocabulary head).
  * Returns the previous value. Process-wide; not thread-safe against
  * concurrent calls.
  */

@@ -18,7 +18,7 @@ from gpu_helpers import assert_within, dev, host_bits, kernel, sample_pairs, tor
 
 pytestmark = pytest.mark.gpu
 
-AUTO, SMALLM, TC = w4.KERNEL_AUTO, w4.KERNEL_SMALLM, w4.KERNEL_TC
+AUTO, SMALLM, TC, XS = w4.KERNEL_AUTO, w4.KERNEL_SMALLM, w4.KERNEL_TC, w4.KERNEL_XSTAGED
 
 
 def _problem(M, N, K, group, seed, gateup=False):
@@ -72,6 +72,10 @@ GEMM_CASES = [
     (AUTO, 13, 250, 512, 64),
     (AUTO, 16, 520, 2048, 128),
     (AUTO, 16, 32, 5120, 64),       # short N: split K across a cluster
+    (XS, 1, 250, 512, 64),
+    (XS, 5, 250, 1024, 128),
+    (XS, 16, 520, 2048, 128),
+    (XS, 16, 32, 5120, 64),
     (TC, 1, 250, 512, 64),
     (TC, 16, 300, 640, 128),
     (AUTO, 17, 520, 1024, 64),
@@ -116,7 +120,8 @@ def test_affine_one_hot_x_gives_rounded_weight(M):
 
 @pytest.mark.parametrize("which,M,N,K,group", [
     (AUTO, 1, 250, 512, 64), (AUTO, 5, 130, 1024, 128), (AUTO, 16, 300, 640, 64),
-    (AUTO, 40, 250, 512, 128), (AUTO, 130, 300, 640, 64), (AUTO, 300, 200, 1024, 128), (TC, 3, 128, 512, 64)])
+    (AUTO, 40, 250, 512, 128), (AUTO, 130, 300, 640, 64), (AUTO, 300, 200, 1024, 128), (TC, 3, 128, 512, 64),
+    (XS, 2, 250, 512, 64), (XS, 16, 300, 640, 128)])
 def test_gateup_affine_parity(which, M, N, K, group):
     p = _problem(M, N, K, group, seed=M + 3 * N + K, gateup=True)
     x = dev(p["x"])

@@ -20,7 +20,7 @@ from gpu_helpers import (assert_within, bf16_f64, check_gemm_full, dev, host_bit
 
 pytestmark = pytest.mark.gpu
 
-GEMV, SMALLM, TC = w4.KERNEL_GEMV, w4.KERNEL_SMALLM, w4.KERNEL_TC
+GEMV, SMALLM, TC, XS = w4.KERNEL_GEMV, w4.KERNEL_SMALLM, w4.KERNEL_TC, w4.KERNEL_XSTAGED
 
 
 @pytest.mark.parametrize("sym,group", [(True, 128), (False, 64), (True, 64), (False, 128)])
@@ -47,6 +47,17 @@ CASES = [
     (SMALLM, 13, 250, 512, 64, False),
     (SMALLM, 16, 1040, 1024, 128, True),
     (SMALLM, 16, 32, 5120, 64, False),
+    # the small-M kernel that stages x once per CTA: one CTA (8 tiles), ragged
+    # N, cluster split-K on short N, a ragged last K unit (K = 640, 1088)
+    (XS, 1, 250, 512, 128, True),
+    (XS, 2, 1040, 2048, 64, False),
+    (XS, 5, 250, 1024, 128, False),
+    (XS, 8, 520, 2048, 64, True),
+    (XS, 9, 130, 640, 64, False),
+    (XS, 13, 250, 512, 64, False),
+    (XS, 16, 1040, 1024, 128, True),
+    (XS, 16, 32, 5120, 64, False),
+    (XS, 16, 2100, 1088, 64, True),
     (TC, 1, 250, 512, 128, True),
     (TC, 17, 520, 1024, 64, False),
     (TC, 200, 520, 1024, 128, True),
@@ -70,7 +81,7 @@ def test_gemm_parity(which, M, N, K, group, sym):
     check_gemm_full(p, y)
 
 
-@pytest.mark.parametrize("which,M", [(GEMV, 1), (SMALLM, 1), (SMALLM, 8), (SMALLM, 16), (TC, 40)])
+@pytest.mark.parametrize("which,M", [(GEMV, 1), (SMALLM, 1), (SMALLM, 8), (SMALLM, 16), (XS, 3), (XS, 16), (TC, 40)])
 @pytest.mark.parametrize("sym", [True, False])
 def test_one_hot_x_gives_rounded_weight(which, M, sym):
     """x = e_k: y[n] = (q - z) * scale exactly in float32, so y is its bf16 rounding."""
@@ -97,7 +108,7 @@ def test_codes_equal_zero_give_exact_zero(which, M):
     assert np.all((y & 0x7FFF) == 0)
 
 
-@pytest.mark.parametrize("which,M", [(SMALLM, 16), (SMALLM, 5), (TC, 150)])
+@pytest.mark.parametrize("which,M", [(SMALLM, 16), (SMALLM, 5), (XS, 16), (XS, 5), (TC, 150)])
 def test_rows_independent_and_deterministic(which, M):
     """Runs are bitwise reproducible; permuting x rows permutes y rows bitwise."""
     N, K, group = 520, 1024, 64
@@ -126,6 +137,9 @@ GATEUP_CASES = [
     (SMALLM, 1, 136, 512, 128, True),
     (SMALLM, 5, 300, 1024, 64, False),
     (SMALLM, 16, 128, 2048, 128, True),
+    (XS, 1, 136, 512, 128, True),
+    (XS, 5, 300, 1024, 64, False),
+    (XS, 16, 128, 2048, 128, True),
     (TC, 17, 136, 512, 64, False),
     (TC, 64, 300, 1024, 64, False),
     (TC, 120, 136, 512, 128, True),
@@ -171,17 +185,19 @@ ARGMAX_CASES = [
 ]
 
 
+@pytest.mark.parametrize("which", [w4.KERNEL_AUTO, XS])
 @pytest.mark.parametrize("M,N,K,group,sym", ARGMAX_CASES)
-def test_gemm_argmax_matches_first_max_of_y(M, N, K, group, sym):
+def test_gemm_argmax_matches_first_max_of_y(M, N, K, group, sym, which):
     """Fused argmax = numpy's first maximum of the bf16 row that w4a16_gemm
     writes (which is torch.argmax's choice), with and without stored logits."""
     p = synth.make_problem(M, N, K, group, sym, seed=70 + M + N)
     d = upload(p)
     packed = packed_of(p, d)
-    y = bf16_f64(run_gemm(p, d=d, packed=packed))
+    y = bf16_f64(run_gemm(p, which, d=d, packed=packed))
     want = np.argmax(y, axis=1)
-    a1, y1 = w4.gemm_argmax(d["x"], packed, N, K, group, sym, logits=True)
-    a2, y2 = w4.gemm_argmax(d["x"], packed, N, K, group, sym)
+    with kernel(which):
+        a1, y1 = w4.gemm_argmax(d["x"], packed, N, K, group, sym, logits=True)
+        a2, y2 = w4.gemm_argmax(d["x"], packed, N, K, group, sym)
     torch().cuda.synchronize()
     assert w4.kernel_status() == 0
     np.testing.assert_array_equal(a1.cpu().numpy(), want)
@@ -214,7 +230,7 @@ def test_gemm_argmax_ties_pick_the_first_column(M):
     assert (got == 40).all()
 
 
-DEGENERATE_KERNELS = [(GEMV, 1), (SMALLM, 1), (SMALLM, 7), (SMALLM, 16), (TC, 20), (TC, 300)]
+DEGENERATE_KERNELS = [(GEMV, 1), (SMALLM, 1), (SMALLM, 7), (SMALLM, 16), (XS, 2), (XS, 16), (TC, 20), (TC, 300)]
 
 
 @pytest.mark.parametrize("which,M", DEGENERATE_KERNELS)

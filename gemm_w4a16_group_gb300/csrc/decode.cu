@@ -550,9 +550,18 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
 // fragment loads of a warp touch 32 distinct banks. K is split only across
 // the CTAs of a cluster.
 // ---------------------------------------------------------------------------
-constexpr int kXsWarps = 4;  // compute warps; warp kXsWarps issues the copies
+#ifndef W4A16_XS_WARPS
+#define W4A16_XS_WARPS 4
+#endif
+constexpr int kXsWarps = W4A16_XS_WARPS;  // compute warps; warp kXsWarps issues the copies
 constexpr int kXsThreads = (kXsWarps + 1) * 32;
-constexpr int kXsSlots = 2;
+#ifndef W4A16_XS_SLOTS
+#define W4A16_XS_SLOTS 2
+#endif
+#ifndef W4A16_XS_TPW
+#define W4A16_XS_TPW 2
+#endif
+constexpr int kXsSlots = W4A16_XS_SLOTS;
 constexpr int kXRowStride = kUnitChunks * 128 + 16;
 
 template <int MT, int TPW, int QF>
@@ -1166,8 +1175,8 @@ cudaError_t run_xs(const DecodeParams &p, int sm_count, cudaStream_t s, bool onl
 
 template <int QF, int CPG, bool GATEUP>
 cudaError_t run_xs_m(const DecodeParams &p, int sm_count, cudaStream_t s, bool only_full, bool *launched) {
-  if (p.M <= 8) return run_xs<1, 2, QF, CPG, GATEUP>(p, sm_count, s, only_full, launched);
-  return run_xs<2, 2, QF, CPG, GATEUP>(p, sm_count, s, only_full, launched);
+  if (p.M <= 8) return run_xs<1, W4A16_XS_TPW, QF, CPG, GATEUP>(p, sm_count, s, only_full, launched);
+  return run_xs<2, W4A16_XS_TPW, QF, CPG, GATEUP>(p, sm_count, s, only_full, launched);
 }
 
 template <int QF, bool GATEUP>

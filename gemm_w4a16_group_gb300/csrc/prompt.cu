@@ -35,9 +35,11 @@
 //   warp 1       TMEM allocation (both CTAs); in the even CTA the single thread
 //                issuing D[b] (+)= W . X^T for the pair, b = group parity
 //   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
-//                128-byte-swizzled K-major W tile
+//                128-byte-swizzled K-major W tile (warps 4-11 for tiles of
+//                64 or 128 x rows)
 //   warps 8-15   epilogue: per group, TMEM -> registers, acc += scale * D[b];
-//                per tile, the bf16 store (or SiLU(gate) * up)
+//                per tile, the bf16 store (or SiLU(gate) * up) (warps 12-15
+//                for tiles of 64 or 128 x rows)
 // The odd CTA signals the even CTA's barriers with remote arrivals (W half
 // written, TMEM buffer drained); the MMA thread's commits arrive on the
 // barriers of both CTAs. Every wait is bounded; a wait that gives up sets the
@@ -71,17 +73,28 @@ constexpr int Q_BYTES = HW * BK / 2;  // 4096
 constexpr int RS_BYTES = NT16 * kScaleBlockBytes;  // 1024
 constexpr int RZ_BYTES = NT16 * kZeroBlockBytes;   // 256
 // barriers: full_L, empty_L [SL]; full_W, (unused) [SW]; full_S, empty_S [SS];
-// tfull, tempty [2]; mma_done [1]
-constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * 2 + 1;
+// tfull, tempty [up to 4 TMEM buffers]; mma_done [1]
+constexpr int kMaxTBuf = 4;
+constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * kMaxTBuf + 1;
 
 // Everything that depends on the pair's x rows per tile, BX = 256 for long
 // prompts, 128 or 64 for a few dozen rows: a short M then issues MMAs of
 // N = BX instead of computing 256 columns of which most are padding; and on
 // the weight form QF (a scale-block slot holds zeros, or biases and the x
 // group sums of the tile, [4 groups][BX] float32).
+//
+// Warp roles by tile width: at 256 x rows, 4 dequantising warps and 8
+// epilogue warps (two per TMEM lane quarter, each on half the columns) and
+// two TMEM buffers; at 64 or 128 x rows a 64-wide K stage carries a quarter
+// or half of the MMAs and the dequantisers set the pace, so 8 of them, 4
+// epilogue warps on all the columns of their lanes, and four TMEM buffers.
 template <int BXT, int QF>
 struct XGeo {
   static constexpr int BX = BXT, HX = BX / 2;  // x rows of the pair, of one CTA
+  static constexpr int DQW = BX == 256 ? 4 : 8;  // dequantising warps: 4 .. 4 + DQW - 1
+  static constexpr int EPW = 12 - DQW;           // epilogue warps: the rest of the 16
+  static constexpr int EC = BX * 4 / EPW;        // D columns per epilogue thread
+  static constexpr int NB = BX == 256 ? 2 : 4;   // TMEM accumulators (groups in flight)
   static constexpr int X_BYTES = HX * BK * 2;
   static constexpr int RZS = QF == kFormAffine ? RS_BYTES : RZ_BYTES;  // zero or bias block slot
   static constexpr int XS_BYTES = QF == kFormAffine ? 4 * BX * 4 : 0;
@@ -96,7 +109,8 @@ struct XGeo {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t kIdesc = idesc_bf16_f32(BW, BX);
-  static constexpr uint32_t kTmemCols = 2 * BX;  // two buffers of BX fp32 columns (a power of two)
+  static constexpr uint32_t kTmemCols = NB * BX;  // NB buffers of BX fp32 columns (a power of two)
+  static_assert(NB <= kMaxTBuf && kTmemCols <= 512 && EC % 32 == 0, "TMEM budget");
   static_assert(BX == 64 || BX == 128 || BX == 256, "pair x rows");
   static_assert(OFF_W % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(OFF_RZ % 128 == 0 && OFF_XS % 128 == 0, "TMA destinations");
@@ -123,8 +137,8 @@ struct Bars {
   __device__ uint32_t full_S(int i) const { return base + 8 * (2 * SL + 2 * SW + i); }
   __device__ uint32_t empty_S(int i) const { return base + 8 * (2 * SL + 2 * SW + SS + i); }
   __device__ uint32_t tfull(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + i); }
-  __device__ uint32_t tempty(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + 2 + i); }
-  __device__ uint32_t mma_done() const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + 4); }
+  __device__ uint32_t tempty(int i) const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + kMaxTBuf + i); }
+  __device__ uint32_t mma_done() const { return base + 8 * (2 * SL + 2 * SW + 2 * SS + 2 * kMaxTBuf); }
 };
 
 // this CTA's abort flag and the peer's (remote store), then the error word
@@ -174,14 +188,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.full_L(i), 1);
       mbar_init(bars.empty_L(i), 1);  // the MMA commit (multicast to both CTAs)
     }
-    for (int i = 0; i < SW; ++i) mbar_init(bars.full_W(i), 8);  // even CTA: 4 local + 4 remote dequant warps
+    for (int i = 0; i < SW; ++i) mbar_init(bars.full_W(i), 2 * G::DQW);  // even CTA: local + remote dequant warps
     for (int i = 0; i < SS; ++i) {
       mbar_init(bars.full_S(i), 1);
-      mbar_init(bars.empty_S(i), ZP ? 8 + 4 : 8);  // epilogue warps (+ dequantisers reading zeros)
+      mbar_init(bars.empty_S(i), ZP ? G::EPW + G::DQW : G::EPW);  // epilogue warps (+ dequantisers reading zeros)
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < G::NB; ++i) {
       mbar_init(bars.tfull(i), 1);
-      mbar_init(bars.tempty(i), 16);  // even CTA: 8 local + 8 remote epilogue warps
+      mbar_init(bars.tempty(i), 2 * G::EPW);  // even CTA: local + remote epilogue warps
     }
     mbar_init(bars.mma_done(), 1);
     *abort_flag = 0;
@@ -199,8 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   // Register split (launched with 128 per thread = 65536): warpgroup 0 gives
-  // back to 40, warpgroup 1 to 96, warpgroups 2-3 take 184:
-  // 128*40 + 128*96 + 256*184 = 64512 <= 65536.
+  // back to 40, the dequantising warpgroups to 96, the epilogue warpgroups
+  // take 184: 128*40 + 128*96 + 256*184 = 64512 (4 dequantising warps) or
+  // 128*40 + 256*96 + 128*184 = 53248 (8) <= 65536.
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
     if (warp == 0) {
@@ -264,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
         for (int gi = 0; ok && gi < p.ng; ++gi) {
-          const int b = gc & 1;
-          if (!mbar_wait(bars.tempty(b), ((gc >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          const int b = gc % G::NB;
+          if (!mbar_wait(bars.tempty(b), ((gc / G::NB) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(b * G::BX);
           // One wait per group, on the W barrier of the group's last stage.
@@ -302,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bars.mma_done(), 0);
     }
     }
-  } else if (warp < 8) {
+  } else if (warp < 4 + G::DQW) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
     // ------------------------------------------------------------------ dequantisers
     const int dw = warp - 4;
@@ -326,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qs = sbase + G::OFF_Q + sl * Q_BYTES;
         const uint32_t wt = sbase + G::OFF_W + sw * W_BYTES;
 #pragma unroll
-        for (int r = 0; r < NT16 / 4; ++r) {
-          const int i = dw + 4 * r;  // 16-row tile within the CTA's 128 rows
+        for (int r = 0; r < NT16 / G::DQW; ++r) {
+          const int i = dw + G::DQW * r;  // 16-row tile within the CTA's 128 rows
           uint32_t zg, zg8;
           if (!ZP) {
             zg = zg8 = zero_pair(SYM ? 8 : 0);  // affine: the code q itself
@@ -371,19 +386,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;           // TMEM lanes 32q .. 32q+31: this CTA's weight rows
-    const int ch2 = (warp - 8) >> 2;  // D columns 128*ch2 .. +127: x rows of CTA ch2
+    constexpr int EC = G::EC;
+    const int q = warp & 3;                    // TMEM lanes 32q .. 32q+31: this CTA's weight rows
+    const int ch2 = (warp - 4 - G::DQW) >> 2;  // D columns EC*ch2 .. +EC-1 (x rows mt*BX + EC*ch2 ..)
     const int wr = 32 * q + lane;     // weight row within the CTA's 128
     // this row's scale in a scale block: tile wr/16, g = wr%8, half (wr/8)%2
     const uint32_t soff = (uint32_t)((wr >> 4) * kScaleBlockBytes + (wr & 7) * 16 + ((wr >> 3) & 1) * 2);
-    float acc[G::HX];
+    float acc[EC];
     uint32_t gc = 0, sc = 0;
     int cur = 0;
     bool ok = true;
     for (int tile = pair; ok && tile < ntot; tile += npairs) {
       const int mt = tile % p.mtiles, nt = tile / p.mtiles;
 #pragma unroll
-      for (int c = 0; c < G::HX; ++c) acc[c] = 0.f;
+      for (int c = 0; c < EC; ++c) acc[c] = 0.f;
       for (int gi = 0; gi < p.ng; ++gi) {
         if ((gi & 3) == 0) {
           cur = sc % SS;
@@ -394,12 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // affine: this row's bias, and the group's x sums of the tile's x rows
         const float bias = AFF ? __uint_as_float(lds16(sbase + G::OFF_RZ + cur * G::RZS + soff + (gi & 3) * 4) << 16)
                                : 0.f;
-        const uint32_t xs_row = sbase + G::OFF_XS + cur * G::XS_BYTES + ((gi & 3) * G::BX + ch2 * G::HX) * 4;
+        const uint32_t xs_row = sbase + G::OFF_XS + cur * G::XS_BYTES + ((gi & 3) * G::BX + ch2 * EC) * 4;
         if (AFF) {
           // acc += bias * X_g needs no MMA result: done before the TMEM wait
           const float2 b2 = make_float2(bias, bias);
 #pragma unroll
-          for (int c = 0; c < G::HX; c += 4) {
+          for (int c = 0; c < EC; c += 4) {
             const float4 xv = lds128f(xs_row + c * 4);  // the same address in every lane
             float2 a = make_float2(acc[c], acc[c + 1]);
             float2 a2 = make_float2(acc[c + 2], acc[c + 3]);
@@ -411,14 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[c + 3] = a2.y;
           }
         }
-        const int b = gc & 1;
-        if (!mbar_wait(bars.tfull(b), (gc >> 1) & 1, abort_flag)) { ok = false; break; }
+        const int b = gc % G::NB;
+        if (!mbar_wait(bars.tfull(b), (gc / G::NB) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const float2 s2 = make_float2(s, s);
 #pragma unroll
-        for (int ch = 0; ch < G::HX / 32; ++ch) {
+        for (int ch = 0; ch < EC / 32; ++ch) {
           float d[32];
-          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * G::BX + ch2 * G::HX + ch * 32), d);
+          tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * G::BX + ch2 * EC + ch * 32), d);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float2 a = make_float2(acc[ch * 32 + c], acc[ch * 32 + c + 1]);
@@ -437,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gc;
       }
       if (!ok) break;
-      // thread = one weight row, HX x rows m0 + c
-      const int m0 = mt * G::BX + ch2 * G::HX;
+      // thread = one weight row, EC x rows m0 + c
+      const int m0 = mt * G::BX + ch2 * EC;
       if (GATEUP) {
         // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows (16-row
-        // tiles alternate); lanes 0-15 form h for x rows c < HX/2, lanes 16-31
-        // for c >= HX/2, each taking the other operand from its partner lane
-        constexpr int H2 = G::HX / 2;
+        // tiles alternate); lanes 0-15 form h for x rows c < EC/2, lanes 16-31
+        // for c >= EC/2, each taking the other operand from its partner lane
+        constexpr int H2 = EC / 2;
         const bool gate = lane < 16;
         const int n = 16 * (nt * (BW / 32) + (int)rank * (NT16 / 2) + q) + (lane & 15);
 #pragma unroll
@@ -458,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = nt * BW + (int)rank * HW + wr;
         if (n < p.N) {
 #pragma unroll
-          for (int c = 0; c < G::HX; ++c)
+          for (int c = 0; c < EC; ++c)
             if (m0 + c < p.M) p.y[(size_t)(m0 + c) * p.ld + n] = bf16_bits(acc[c]);
         }
       }

@@ -243,7 +243,7 @@ def run_cuda(args, rank, world):
         pt["x"] = up(p["x"])
         pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
         # affine form on the tcgen05 GEMM: the group sums of x, formed every call
-        pt["xs"] = (torch.empty(w4.xsum_bytes(w["M"], w["K"], w["group"]) // 4, dtype=torch.float32, device=dev)
+        pt["xs"] = (torch.empty(w4.xsum_bytes(w["M"], w["K"], w["group"]) // 2, dtype=torch.bfloat16, device=dev)
                     if p["affine"] and (w["M"] > 16 or args.kernel == "tc") else None)
         pt["idx"] = torch.empty(w["M"], dtype=torch.int64, device=dev)
         pt["idx_host"] = torch.empty(w["M"], dtype=torch.int64).pin_memory()

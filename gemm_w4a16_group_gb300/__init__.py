@@ -277,7 +277,8 @@ def xsum_bytes(M: int, K: int, group: int) -> int:
 
 
 def xsum(x, K, group, out=None, stream=None):
-    """float32 [K/G, ld]: column m < M holds the sums of x[m] over each group (ld >= M)."""
+    """bf16 [M, kb3]: the sum of x[m] over each group g as three bf16 parts
+    (hi, mid, lo at columns 3g .. 3g+2) that add up to the float32 sum exactly."""
     torch = _torch()
     M = x.shape[0]
     if x.dim() != 2 or x.shape[1] != K:
@@ -286,18 +287,17 @@ def xsum(x, K, group, out=None, stream=None):
     if nbytes == 0:
         raise W4A16Error("xsum: unsupported sizes")
     if out is None:
-        out = torch.empty((K // group, nbytes // 4 // (K // group)), dtype=torch.float32, device=x.device)
-    elif out.numel() * 4 < nbytes:
-        raise ValueError(f"xsum: out holds {out.numel() * 4} bytes, needs {nbytes}")
-    rc = lib().w4a16_xsum(_ptr(x, _bf16_types(), "x"), M, K, group, _ptr(out, (torch.float32,), "out"),
+        out = torch.empty((M, nbytes // 2 // M), dtype=torch.bfloat16, device=x.device)
+    elif out.numel() * out.element_size() < nbytes:
+        raise ValueError(f"xsum: out holds {out.numel() * out.element_size()} bytes, needs {nbytes}")
+    rc = lib().w4a16_xsum(_ptr(x, _bf16_types(), "x"), M, K, group, _ptr(out, _bf16_types(), "out"),
                           _stream(stream))
     _check(rc, "w4a16_xsum")
     return out
 
 
 def _xs_ptr(xs):
-    torch = _torch()
-    return _ptr(xs, (torch.float32,), "xsum")
+    return _ptr(xs, _bf16_types(), "xsum")
 
 
 def gemm_affine(x, packed, N, K, group, xs=None, out=None, stream=None):

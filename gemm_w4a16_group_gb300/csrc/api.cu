@@ -23,7 +23,7 @@ __device__ int g_kernel_error;
 // Fixed table of x group sums for w4a16_gemm_affine_noalloc (4 MiB per device,
 // part of the module image: nothing is allocated at run time).
 constexpr size_t kNoAllocXsumBytes = size_t(4) << 20;
-static __device__ __align__(256) float g_noalloc_xsum[kNoAllocXsumBytes / sizeof(float)];
+static __device__ __align__(256) uint16_t g_noalloc_xsum[kNoAllocXsumBytes / sizeof(uint16_t)];
 
 struct DeviceInfo {
   int device = 0;
@@ -31,7 +31,7 @@ struct DeviceInfo {
   int status = W4A16_OK;
   int sm_count = 0;
   int *err = nullptr;
-  float *noalloc_xsum = nullptr;  // this device's copy of g_noalloc_xsum
+  uint16_t *noalloc_xsum = nullptr;  // this device's copy of g_noalloc_xsum
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -62,7 +62,7 @@ int current_device(DeviceInfo &out) {
       if ((e = cudaGetSymbolAddress(&p, g_kernel_error)) != cudaSuccess) return cuda_fail(e);
       d.err = static_cast<int *>(p);
       if ((e = cudaGetSymbolAddress(&p, g_noalloc_xsum)) != cudaSuccess) return cuda_fail(e);
-      d.noalloc_xsum = static_cast<float *>(p);
+      d.noalloc_xsum = static_cast<uint16_t *>(p);
       d.sm_count = sms;
       d.status = W4A16_OK;
     }
@@ -100,10 +100,9 @@ bool zero_form(int form) { return form == kFormZero || form == kFormSym; }
 // itself), else the tcgen05 GEMM, which reads them from `xsum`.
 bool affine_uses_tc(int M) { return M > 16 || g_override.load() == 3; }
 
-int launch_affine(GemmCall &c, const float *xsum, const DeviceInfo &d) {
+int launch_affine(GemmCall &c, const uint16_t *xsum, const DeviceInfo &d) {
   if (!affine_uses_tc(c.M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
   c.xsum = xsum;
-  c.xsum_ld = xsum_ld(c.M);
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
@@ -257,10 +256,10 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
 
 size_t w4a16_xsum_bytes(int M, int K, int group) {
   if (!sizes_ok(M, 1, K, group)) return 0;
-  return (size_t)(K / group) * (size_t)xsum_ld(M) * sizeof(float);
+  return (size_t)M * (size_t)affine_kb3(K / group) * sizeof(uint16_t);
 }
 
-int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_stream_t stream) {
+int w4a16_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xsum, w4a16_stream_t stream) {
   if (!x || !xsum) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, 1, K, group)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(xsum, 16)) return W4A16_ERR_MISALIGNED;
@@ -270,7 +269,7 @@ int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_st
   return finish_launch(launch_xsum(x, M, K, group, xsum, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, int M, int N, int K, int group,
+int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packed, int M, int N, int K, int group,
                       uint16_t *y, w4a16_stream_t stream) {
   if (!x || !packed || !y || (!xsum && affine_uses_tc(M))) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
@@ -304,7 +303,7 @@ int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int 
   return launch_affine(c, d.noalloc_xsum, d);
 }
 
-int w4a16_gateup_silu_affine(const uint16_t *x, const float *xsum, const void *packed_gateup, int M, int N_each,
+int w4a16_gateup_silu_affine(const uint16_t *x, const uint16_t *xsum, const void *packed_gateup, int M, int N_each,
                              int K, int group, uint16_t *h, w4a16_stream_t stream) {
   if (!x || !packed_gateup || !h || (!xsum && affine_uses_tc(M))) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, N_each, K, group) || w4a16_gateup_repacked_bytes(N_each, K, group, kFormAffine) == 0)

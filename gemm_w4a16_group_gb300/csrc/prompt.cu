@@ -6,10 +6,12 @@
 // in float32, so the tensor core sums one group's products into a TMEM tile
 // (fp32), and CUDA cores fold it into a register accumulator with the group's
 // scale in float32. The affine form w = scale * q + bias (the MLX affine 4-bit
-// checkpoints of TensorFold PR #859) runs the same MMAs on the exact codes q
-// and adds bias * X_g per group, X_g = sum_{k in g} x[m][k] read from a
-// float32 table of group sums (w4a16_xsum) that TMA brings in beside the
-// scales. Rounding a dequantised (q - z) * scale to bf16 before the
+// checkpoints of TensorFold PR #859) runs the same MMAs on the exact codes q,
+// and each tile ends with one more group whose operands TMA loads as they
+// are: the weight's bias operand (each bias at three K columns) against the
+// x group sums X_g = sum_{k in g} x[m][k] split into three bf16 parts
+// (w4a16_xsum). Its accumulator is sum_g bias * X_g (exact products, float32
+// sums) and the epilogue adds it with scale 1. Rounding a dequantised (q - z) * scale to bf16 before the
 // MMA, as the TensorFold PR #859 prompt GEMM does ("each weight rounded once to
 // bf16"), would cost up to 2^-9 per weight; this split keeps every weight
 // exact. The feed-forward gate is fused as in the GRIMOIRE v1.8 release notes
@@ -31,7 +33,8 @@
 // One persistent CTA pair per two SMs, 512 threads per CTA, warp-specialised:
 //   warp 0       TMA producer: the CTA's x rows [128 x 64] (128-byte swizzle), the
 //                packed codes of its 128 weight rows x 64 k, and per four groups
-//                their scale (+ zero, or + bias and the tile's x group sums) block
+//                their scale (+ zero) block; affine: then the bias operand and
+//                x group sums of the closing group
 //   warp 1       TMEM allocation (both CTAs); in the even CTA the single thread
 //                issuing D[b] (+)= W . X^T for the pair, b = group parity
 //   warps 4-7    dequantisers: codes -> bf16 (q - z) written straight into the
@@ -80,8 +83,8 @@ constexpr int NBARS = 2 * SL + 2 * SW + 2 * SS + 2 * kMaxTBuf + 1;
 // Everything that depends on the pair's x rows per tile, BX = 256 for long
 // prompts, 128 or 64 for a few dozen rows: a short M then issues MMAs of
 // N = BX instead of computing 256 columns of which most are padding; and on
-// the weight form QF (a scale-block slot holds zeros, or biases and the x
-// group sums of the tile, [4 groups][BX] float32).
+// the weight form QF (a scale-block slot holds the scales, and the zeros of
+// the zero-point form).
 //
 // Warp roles by tile width: at 256 x rows, 4 dequantising warps and 8
 // epilogue warps (two per TMEM lane quarter, each on half the columns) and
@@ -96,15 +99,13 @@ struct XGeo {
   static constexpr int EC = BX * 4 / EPW;        // D columns per epilogue thread
   static constexpr int NB = BX == 256 ? 2 : 4;   // TMEM accumulators (groups in flight)
   static constexpr int X_BYTES = HX * BK * 2;
-  static constexpr int RZS = QF == kFormAffine ? RS_BYTES : RZ_BYTES;  // zero or bias block slot
-  static constexpr int XS_BYTES = QF == kFormAffine ? 4 * BX * 4 : 0;
+  static constexpr int RZS = RZ_BYTES;  // zero block slot
   static constexpr int OFF_X = 0;
   static constexpr int OFF_W = OFF_X + SL * X_BYTES;
   static constexpr int OFF_Q = OFF_W + SW * W_BYTES;
   static constexpr int OFF_RS = OFF_Q + SL * Q_BYTES;
   static constexpr int OFF_RZ = OFF_RS + SS * RS_BYTES;
-  static constexpr int OFF_XS = OFF_RZ + SS * RZS;
-  static constexpr int OFF_BAR = OFF_XS + SS * XS_BYTES;
+  static constexpr int OFF_BAR = OFF_RZ + SS * RZS;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -113,7 +114,7 @@ struct XGeo {
   static_assert(NB <= kMaxTBuf && kTmemCols <= 512 && EC % 32 == 0, "TMEM budget");
   static_assert(BX == 64 || BX == 128 || BX == 256, "pair x rows");
   static_assert(OFF_W % 1024 == 0 && OFF_Q % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static_assert(OFF_RZ % 128 == 0 && OFF_XS % 128 == 0, "TMA destinations");
+  static_assert(OFF_RZ % 128 == 0, "TMA destinations");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -125,6 +126,7 @@ struct PromptParams {
   int nk;          // K / 64
   int ng;          // K / group
   int spg;         // 64-wide stages per group (1 or 2)
+  int nkb;         // affine: 64-wide stages of the closing bias group (0 otherwise)
   int *err;
   UnpackConsts uc;
 };
@@ -161,8 +163,8 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return *reinterpret_cast<uint16_t *>(&b);
 }
 
-// tm_z: the zero blocks (zero-point form) or the bias blocks (affine form);
-// tm_xs: the x group sums (affine form)
+// tm_z: the zero blocks (zero-point form) or the bias operand (affine form);
+// tm_xs: the x group sums, in bf16 parts (affine form)
 template <int QF, bool GATEUP, int BXT>
 __global__ void __launch_bounds__(kThreads, 1)
     prompt_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
@@ -236,18 +238,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
         const int mt = tile % p.mtiles, nt = tile / p.mtiles;
         const int qt = nt * (BW / 16) + (int)rank * NT16;  // first 16-row tile of this CTA's weights
-        for (int kb = 0; kb < p.nk; ++kb) {
+        const int nkt = AFF ? p.nk + p.nkb : p.nk;  // stages of a tile
+        for (int kb = 0; kb < nkt; ++kb) {
+          if (AFF && kb >= p.nk) {
+            // affine closing group: x group sums into the x slot, the bias
+            // operand straight into the W slot
+            const int slot = ls % SL;
+            if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            mbar_arrive_expect_tx(bars.full_L(slot), G::X_BYTES + W_BYTES);
+            tma_load_2d_hint(sbase + G::OFF_X + slot * G::X_BYTES, &tm_xs, (kb - p.nk) * BK,
+                             mt * G::BX + (int)rank * G::HX, bars.full_L(slot), pol_keep);
+            tma_load_2d_hint(sbase + G::OFF_W + slot * W_BYTES, &tm_z, (kb - p.nk) * BK, qt * 16, bars.full_L(slot),
+                             pol_stream);
+            ++ls;
+            continue;
+          }
           if (kb % (4 * p.spg) == 0) {
             const int slot = sc % SS;
             if (!mbar_wait(bars.empty_S(slot), ((sc / SS) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (SYM ? 0 : G::RZS) + G::XS_BYTES);
+            mbar_arrive_expect_tx(bars.full_S(slot), RS_BYTES + (ZP ? G::RZS : 0));
             const int blk = kb / (4 * p.spg);
             tma_load_2d(sbase + G::OFF_RS + slot * RS_BYTES, &tm_s, blk * 32, qt, bars.full_S(slot));
             if (ZP) tma_load_2d(sbase + G::OFF_RZ + slot * G::RZS, &tm_z, blk * 8, qt, bars.full_S(slot));
-            if (AFF) {
-              tma_load_2d(sbase + G::OFF_RZ + slot * G::RZS, &tm_z, blk * 32, qt, bars.full_S(slot));
-              tma_load_2d(sbase + G::OFF_XS + slot * G::XS_BYTES, &tm_xs, mt * G::BX, 4 * blk, bars.full_S(slot));
-            }
             ++sc;
           }
           const int slot = ls % SL;
@@ -278,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ls = 0, ws = 0, gc = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
-        for (int gi = 0; ok && gi < p.ng; ++gi) {
+        const int ngt = AFF ? p.ng + 1 : p.ng;  // groups of a tile (affine: + the bias group)
+        for (int gi = 0; ok && gi < ngt; ++gi) {
+          const int nst = (AFF && gi == p.ng) ? p.nkb : p.spg;  // stages of this group
           const int b = gc % G::NB;
           if (!mbar_wait(bars.tempty(b), ((gc / G::NB) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -289,11 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // a stage, and arrives on the group's stages in order. (Every barrier
           // operation costs this single issuing thread a few hundred cycles.)
           {
-            const uint32_t wl = ws + (uint32_t)p.spg - 1;
+            const uint32_t wl = ws + (uint32_t)nst - 1;
             if (!mbar_wait(bars.full_W(wl % SW), (wl / SW) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
           }
-          for (int ks = 0; ks < p.spg; ++ks) {
+          for (int ks = 0; ks < nst; ++ks) {
             const int sl = ls % SL, sw = ws % SW;
             const uint64_t wdesc = sw128_desc(sbase + G::OFF_W + sw * W_BYTES);
             const uint64_t xdesc = sw128_desc(sbase + G::OFF_X + sl * G::X_BYTES);
@@ -326,7 +340,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur = 0;
     bool ok = true;
     for (int tile = pair; ok && tile < ntot; tile += npairs) {
-      for (int kb = 0; kb < p.nk; ++kb) {
+      const int nkt = AFF ? p.nk + p.nkb : p.nk;
+      for (int kb = 0; kb < nkt; ++kb) {
+        if (AFF && kb >= p.nk) {
+          // affine closing group: TMA filled the W slot; pass it on
+          const int sl = ls % SL, sw = ws % SW;
+          if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
+          __syncwarp();
+          if (lane == 0) arrive_even(bars.full_W(sw), rank);
+          ++ls;
+          ++ws;
+          continue;
+        }
         const int gi = kb / p.spg;
         if (ZP && kb % (4 * p.spg) == 0) {
           cur = sc % SS;
@@ -400,33 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = tile % p.mtiles, nt = tile / p.mtiles;
 #pragma unroll
       for (int c = 0; c < EC; ++c) acc[c] = 0.f;
-      for (int gi = 0; gi < p.ng; ++gi) {
-        if ((gi & 3) == 0) {
+      for (int gi = 0; gi < p.ng + (AFF ? 1 : 0); ++gi) {
+        const bool real = !AFF || gi < p.ng;  // not the affine closing group (scale 1)
+        if (real && (gi & 3) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
           ++sc;
         }
-        const float s = __uint_as_float(lds16(sbase + G::OFF_RS + cur * RS_BYTES + soff + (gi & 3) * 4) << 16);
-        // affine: this row's bias, and the group's x sums of the tile's x rows
-        const float bias = AFF ? __uint_as_float(lds16(sbase + G::OFF_RZ + cur * G::RZS + soff + (gi & 3) * 4) << 16)
-                               : 0.f;
-        const uint32_t xs_row = sbase + G::OFF_XS + cur * G::XS_BYTES + ((gi & 3) * G::BX + ch2 * EC) * 4;
-        if (AFF) {
-          // acc += bias * X_g needs no MMA result: done before the TMEM wait
-          const float2 b2 = make_float2(bias, bias);
-#pragma unroll
-          for (int c = 0; c < EC; c += 4) {
-            const float4 xv = lds128f(xs_row + c * 4);  // the same address in every lane
-            float2 a = make_float2(acc[c], acc[c + 1]);
-            float2 a2 = make_float2(acc[c + 2], acc[c + 3]);
-            a = __ffma2_rn(b2, make_float2(xv.x, xv.y), a);
-            a2 = __ffma2_rn(b2, make_float2(xv.z, xv.w), a2);
-            acc[c] = a.x;
-            acc[c + 1] = a.y;
-            acc[c + 2] = a2.x;
-            acc[c + 3] = a2.y;
-          }
-        }
+        const float s =
+            real ? __uint_as_float(lds16(sbase + G::OFF_RS + cur * RS_BYTES + soff + (gi & 3) * 4) << 16) : 1.0f;
         const int b = gc % G::NB;
         if (!mbar_wait(bars.tfull(b), (gc / G::NB) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           arrive_even(bars.tempty(b), rank);
-          if ((gi & 3) == 3 || gi == p.ng - 1) mbar_arrive(bars.empty_S(cur));
+          if (real && ((gi & 3) == 3 || gi == p.ng - 1)) mbar_arrive(bars.empty_S(cur));
         }
         ++gc;
       }
@@ -582,13 +589,12 @@ cudaError_t launch_bx(const GemmCall &c) {
                          CU_TENSOR_MAP_SWIZZLE_NONE);
   } else if (c.sym == kFormAffine) {
     if (!c.xsum) return cudaErrorInvalidValue;
-    ok = ok && encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT32, c.packed + L.biases_off, (uint64_t)L.gblocks * 32,
-                         (uint64_t)L.tiles, (uint64_t)L.gblocks * kScaleBlockBytes, 32, NT16,
-                         CU_TENSOR_MAP_SWIZZLE_NONE);
-    // xsum [groups][ld] float32, ld a multiple of 256 >= M: the box of BX x
-    // rows and four groups never starts past the row (x coordinate mt * BX)
-    ok = ok && encode_2d(&txs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c.xsum, (uint64_t)c.xsum_ld,
-                         (uint64_t)(c.K / c.group), (uint64_t)c.xsum_ld * 4, G::BX, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
+    // the bias operand [rows][kb3] and the x group sums [M][kb3], both bf16
+    // and K-major like x, in 64-wide boxes with the 128-byte swizzle
+    ok = ok && encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.packed + L.bops_off, (uint64_t)L.kb3,
+                         (uint64_t)L.tiles * 16, (uint64_t)L.kb3 * 2, BK, HW, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&txs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.xsum, (uint64_t)L.kb3, (uint64_t)c.M,
+                         (uint64_t)L.kb3 * 2, BK, G::HX, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return cudaErrorInvalidValue;
   PromptParams p;
@@ -602,6 +608,7 @@ cudaError_t launch_bx(const GemmCall &c) {
   p.nk = c.K / BK;
   p.ng = c.K / c.group;
   p.spg = c.group / BK;
+  p.nkb = c.sym == kFormAffine ? L.kb3 / BK : 0;
   p.err = c.err;
   p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;

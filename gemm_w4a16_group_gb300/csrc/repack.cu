@@ -111,6 +111,22 @@ __global__ void repack_zeros_kernel(RepackSrc s, Layout L, uint8_t *out) {
   }
 }
 
+// affine bias operand: row r (packed order), column j = bias(r, j / 3) for
+// j < 3 * groups, else 0
+__global__ void repack_bias_operand_kernel(RepackSrc s, Layout L, uint16_t *out) {
+  const size_t total = (size_t)L.tiles * 16 * L.kb3;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int j = (int)(idx % L.kb3);
+    const size_t r = idx / L.kb3;
+    const int T = (int)(r / 16), rr = (int)(r % 16);
+    const int gi = j / 3;
+    int which;
+    const int row = src_row(s, T, rr, which);
+    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0 : s.b[which][(size_t)row * L.groups + gi];
+  }
+}
+
 // w[n][k] = (q - z) * scale (exact), or scale * q + bias rounded once to
 // float32 (affine), through the same unpack as the GEMM kernels
 __global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float *w, UnpackConsts uc) {
@@ -203,9 +219,13 @@ cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t
   size_t ns = (size_t)L.tiles * L.gblocks * 64;
   repack_scales_kernel<<<grid_for(ns, th), th, 0, stream>>>(
       s, L, false, reinterpret_cast<uint16_t *>(packed + L.scales_off));
-  if (L.sym == kFormAffine)
+  if (L.sym == kFormAffine) {
     repack_scales_kernel<<<grid_for(ns, th), th, 0, stream>>>(
         s, L, true, reinterpret_cast<uint16_t *>(packed + L.biases_off));
+    const size_t nb = (size_t)L.tiles * 16 * L.kb3;
+    repack_bias_operand_kernel<<<grid_for(nb, th), th, 0, stream>>>(
+        s, L, reinterpret_cast<uint16_t *>(packed + L.bops_off));
+  }
   if (L.sym == kFormZero) {
     size_t nz = (size_t)L.tiles * L.gblocks * 32;
     repack_zeros_kernel<<<grid_for(nz, th), th, 0, stream>>>(s, L, packed + L.zeros_off);

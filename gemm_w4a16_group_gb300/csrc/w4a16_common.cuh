@@ -30,6 +30,11 @@ namespace w4a16 {
 //  Zeros (zero-point form only): per tile and block, [g][j] bytes holding
 //  zero(row g) | zero(row g+8) << 4: 32 bytes per block.
 //  Biases (affine form only): the scales' layout with bias for scale.
+//  Bias operand (affine form only): bf16 [16 * tiles][kb3], kb3 = 3 * groups
+//  rounded up to 64; row r holds bias(r, g) at columns 3g, 3g+1, 3g+2 and 0
+//  beyond. Against the group sums of x split into three bf16 parts (hi, mid,
+//  lo at the same columns), one K-major MMA operand pair gives
+//  sum_g bias * X_g on the tensor cores.
 // ---------------------------------------------------------------------------
 constexpr int kTileRows = 16;
 constexpr int kChunkK = 64;
@@ -49,8 +54,12 @@ struct Layout {
   int chunks;      // K / 64
   int groups;      // K / group
   int gblocks;     // ceil(groups / 4)
-  size_t codes_off, scales_off, zeros_off, biases_off, total;
+  int kb3;         // affine: columns of the bias operand (3 * groups rounded up to 64)
+  size_t codes_off, scales_off, zeros_off, biases_off, bops_off, total;
 };
+
+// columns of the affine bias operand and of the split x group sums
+__host__ __device__ inline int affine_kb3(int groups) { return (3 * groups + 63) / 64 * 64; }
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -65,7 +74,9 @@ __host__ __device__ inline Layout make_layout(int N, int K, int group, int form)
   L.scales_off = align_up((size_t)L.tiles * L.chunks * kChunkBytes, 256);
   L.zeros_off = align_up(L.scales_off + (size_t)L.tiles * L.gblocks * kScaleBlockBytes, 256);
   L.biases_off = align_up(L.zeros_off + (form == kFormZero ? (size_t)L.tiles * L.gblocks * kZeroBlockBytes : 0), 256);
-  L.total = align_up(L.biases_off + (form == kFormAffine ? (size_t)L.tiles * L.gblocks * kScaleBlockBytes : 0), 256);
+  L.bops_off = align_up(L.biases_off + (form == kFormAffine ? (size_t)L.tiles * L.gblocks * kScaleBlockBytes : 0), 256);
+  L.kb3 = affine_kb3(L.groups);
+  L.total = align_up(L.bops_off + (form == kFormAffine ? (size_t)L.tiles * 16 * L.kb3 * 2 : 0), 256);
   return L;
 }
 

@@ -33,8 +33,7 @@ struct GemmCall {
   int device;  // current device ordinal, < kMaxDevices
   bool overlap;  // programmatic overlap with the previous kernel (M <= 16 kernels)
   int64_t *amax = nullptr;  // argmax keys per x row (M <= 16 plain GEMM), or null
-  const float *xsum = nullptr;  // affine form, tcgen05 GEMM: x group sums [K/G][xsum_ld]
-  int xsum_ld = 0;
+  const uint16_t *xsum = nullptr;  // affine form, tcgen05 GEMM: x group sums, bf16 parts [M][kb3]
   int xs_mode = 1;  // M <= 16, the kernel that stages x once per CTA: 0 never, 1 when it fits, 2 always
 };
 
@@ -59,9 +58,9 @@ cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count);   // any M
 // y already written, the keys of every row
 cudaError_t launch_argmax_init(int64_t *amax, int M, bool overlap, cudaStream_t stream);
 cudaError_t launch_argmax_finalize(int64_t *amax, int M, bool overlap, cudaStream_t stream);
-// affine form: X[g][m] = sum of x[m][k] over group g, float32 [K/G][xsum_ld(M)]
-int xsum_ld(int M);
-cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, float *xs, cudaStream_t stream);
+// affine form: X[m][g] = sum of x[m][k] over group g, as three bf16 parts per
+// group, bf16 [M][affine_kb3(K / group)]
+cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xs, cudaStream_t stream);
 cudaError_t launch_row_argmax(const uint16_t *y, int M, int N, int64_t *amax, cudaStream_t stream);
 
 }  // namespace w4a16

@@ -1,13 +1,17 @@
 // Group sums of the activations for the affine weight form w = scale * q + bias
 // (the MLX affine 4-bit checkpoints of TensorFold PR #859):
 //
-//   y[m][n] = sum_g scale[n][g] * sum_{k in g} q[n][k] x[m][k] + sum_g bias[n][g] * X[g][m],
-//   X[g][m] = sum_{k in g} x[m][k]
+//   y[m][n] = sum_g scale[n][g] * sum_{k in g} q[n][k] x[m][k] + sum_g bias[n][g] * X[m][g],
+//   X[m][g] = sum_{k in g} x[m][k]
 //
 // X depends on x alone, so one table serves every weight that reads the same
-// x with the same group size. Layout: float32 [K/G][ld], ld = M rounded up to a
-// multiple of 256 (the tcgen05 GEMM loads boxes of up to 256 x rows by four
-// groups); entries m >= M are zero.
+// x with the same group size. Each X (a float32 sum) is stored as three bf16
+// parts hi + mid + lo that add up to it exactly (hi = bf16(X), mid =
+// bf16(X - hi), lo = X - hi - mid; every residual is exact in float32 and the
+// last fits in bf16), so that the tcgen05 GEMM forms sum_g bias * X[m][g] with
+// exact bf16 products against the bias operand of the packed weight.
+// Layout: bf16 [M][kb3], kb3 = 3 * K/G rounded up to 64, X[m][g]'s parts at
+// columns 3g, 3g+1, 3g+2, zeros beyond 3 * K/G.
 #include "w4a16_internal.h"
 
 namespace w4a16 {
@@ -15,19 +19,23 @@ namespace {
 
 constexpr int kXsThreads = 256;
 
+__device__ __forceinline__ uint16_t bf16_rn(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t *>(&b);
+}
+
 // One warp per x row: each lane sums 8 consecutive k of a 256-wide slab, then
-// the G/8 lanes of a group meet by shuffles and one of them writes X[g][m].
-__global__ void __launch_bounds__(kXsThreads) xsum_kernel(const uint16_t *x, int M, int K, int group, int ld,
-                                                          float *xs) {
+// the G/8 lanes of a group meet by shuffles and one of them writes the parts.
+__global__ void __launch_bounds__(kXsThreads) xsum_kernel(const uint16_t *x, int M, int K, int group, int kb3,
+                                                          uint16_t *xs) {
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (kXsThreads / 32);
   const int lpg = group / 8;  // lanes per group: 8 or 16
-  for (int m = blockIdx.x * (kXsThreads / 32) + (threadIdx.x >> 5); m < ld; m += warps) {
-    if (m >= M) {  // padding columns: zero (warp-uniform branch)
-      for (int g = lane; g < K / group; g += 32) xs[(size_t)g * ld + m] = 0.f;
-      continue;
-    }
+  const int groups = K / group;
+  for (int m = blockIdx.x * (kXsThreads / 32) + (threadIdx.x >> 5); m < M; m += warps) {
     const uint16_t *row = x + (size_t)m * K;
+    uint16_t *out = xs + (size_t)m * kb3;
+    for (int j = 3 * groups + lane; j < kb3; j += 32) out[j] = 0;
     for (int k0 = 0; k0 < K; k0 += 256) {
       const int k = k0 + 8 * lane;
       float v = 0.f;
@@ -38,20 +46,26 @@ __global__ void __launch_bounds__(kXsThreads) xsum_kernel(const uint16_t *x, int
         for (int i = 0; i < 4; ++i) v += bf16lo_to_f32(ws[i]) + bf16hi_to_f32(ws[i]);
       }
       for (int o = 1; o < lpg; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-      if (k < K && (lane & (lpg - 1)) == 0) xs[(size_t)(k / group) * ld + m] = v;
+      if (k < K && (lane & (lpg - 1)) == 0) {
+        const int gi = k / group;
+        const uint16_t hi = bf16_rn(v);
+        const float r1 = v - __uint_as_float((uint32_t)hi << 16);
+        const uint16_t mid = bf16_rn(r1);
+        const float r2 = r1 - __uint_as_float((uint32_t)mid << 16);
+        out[3 * gi] = hi;
+        out[3 * gi + 1] = mid;
+        out[3 * gi + 2] = bf16_rn(r2);
+      }
     }
   }
 }
 
 }  // namespace
 
-int xsum_ld(int M) { return (M + 255) / 256 * 256; }
-
-cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, float *xs, cudaStream_t stream) {
-  const int ld = xsum_ld(M);
-  int blocks = (ld + kXsThreads / 32 - 1) / (kXsThreads / 32);
+cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xs, cudaStream_t stream) {
+  int blocks = (M + kXsThreads / 32 - 1) / (kXsThreads / 32);
   if (blocks > 4096) blocks = 4096;
-  xsum_kernel<<<blocks, kXsThreads, 0, stream>>>(x, M, K, group, ld, xs);
+  xsum_kernel<<<blocks, kXsThreads, 0, stream>>>(x, M, K, group, affine_kb3(K / group), xs);
   return cudaGetLastError();
 }
 

@@ -182,7 +182,9 @@ int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float
 
 /*
  * Offline repack of an affine weight: qweight as above, scales and biases
- * bf16 [N][K/G]. The biases sit in the scales' tiled layout. Writes
+ * bf16 [N][K/G]. The biases sit in the scales' tiled layout, and once more as
+ * the tcgen05 GEMM's bias operand: bf16 [rows][kb3] with each bias at three
+ * consecutive columns (against the three parts of the x group sums). Writes
  * w4a16_repacked_bytes(N, K, group, W4A16_AFFINE) bytes; padding rows get
  * code 0, scale 0 and bias 0.
  */
@@ -195,15 +197,19 @@ int w4a16_repack_affine_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, 
                                int K, int group, void *packed, w4a16_stream_t stream);
 
 /*
- * Group sums of the activations: xsum[g][m] = sum_{k in group g} x[m][k]
- * (float32, summed in float32), rows of ld = M rounded up to a multiple of
- * 256 floats; entries m >= M are written as 0. They depend on x alone, so one
- * table serves every affine weight that reads the same x with the same group
- * size. `xsum` is caller-owned device memory of w4a16_xsum_bytes(M, K, group)
- * bytes, 16-byte aligned; w4a16_xsum_bytes returns 0 for unsupported sizes.
+ * Group sums of the activations, X[m][g] = sum_{k in group g} x[m][k] summed
+ * in float32, each stored as three bf16 parts that add up to it exactly
+ * (hi = bf16(X), mid = bf16(X - hi), lo = X - hi - mid): bf16 [M][kb3],
+ * kb3 = 3 * K/G rounded up to 64, the parts of X[m][g] at columns 3g .. 3g+2,
+ * zeros beyond 3 * K/G. The tcgen05 GEMM multiplies them by the weight's
+ * biases on the tensor cores (exact bf16 products, float32 sums). They depend
+ * on x alone, so one table serves every affine weight that reads the same x
+ * with the same group size. `xsum` is caller-owned device memory of
+ * w4a16_xsum_bytes(M, K, group) bytes, 16-byte aligned; w4a16_xsum_bytes
+ * returns 0 for unsupported sizes.
  */
 size_t w4a16_xsum_bytes(int M, int K, int group);
-int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_stream_t stream);
+int w4a16_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xsum, w4a16_stream_t stream);
 
 /*
  * y[M][N] (bf16) = x . (scale * q + bias)^T, W from w4a16_repack_affine.
@@ -212,7 +218,7 @@ int w4a16_xsum(const uint16_t *x, int M, int K, int group, float *xsum, w4a16_st
  * when M <= 16, where the decode kernel forms the group sums itself with one
  * more tensor-core product per 16 k (then it is not read).
  */
-int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, int M, int N, int K, int group,
+int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packed, int M, int N, int K, int group,
                       uint16_t *y, w4a16_stream_t stream);
 
 /*
@@ -222,7 +228,7 @@ int w4a16_gemm_affine(const uint16_t *x, const float *xsum, const void *packed, 
  * module image (one per device, found once with cudaGetSymbolAddress), so the
  * call allocates nothing and needs no workspace argument; sizes whose table
  * (w4a16_xsum_bytes) exceeds 4 MiB are W4A16_ERR_INVALID_ARG (at K = 5120 and
- * group 64, M up to 13,056). Every entry the GEMM reads, the zero padding
+ * group 64, M up to 8,192). Every entry the GEMM reads, the zero padding
  * included, is written by the call itself before the GEMM reads it, so
  * nothing has to start at zero. The array is shared: calls in flight at the
  * same time on one device (other streams, other host threads) race on it and
@@ -234,7 +240,7 @@ int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int 
 
 /* h = SiLU(x Wg^T) * (x Wu^T) as w4a16_gateup_silu, affine weights from
  * w4a16_repack_affine_gateup; `xsum` as for w4a16_gemm_affine. */
-int w4a16_gateup_silu_affine(const uint16_t *x, const float *xsum, const void *packed_gateup, int M, int N_each,
+int w4a16_gateup_silu_affine(const uint16_t *x, const uint16_t *xsum, const void *packed_gateup, int M, int N_each,
                              int K, int group, uint16_t *h, w4a16_stream_t stream);
 
 /*

@@ -121,13 +121,15 @@ def test_argmax_entry_point_argument_checks(L):
 
 def test_affine_layout_and_argument_checks(L):
     P = ctypes.c_void_p
-    # the bias section is the scales' size: N=256, K=512, G=128 -> 2048 B
-    assert w4.repacked_bytes(256, 512, 128, w4.AFFINE) == 65536 + 2048 + 2048
+    # the bias section is the scales' size (N=256, K=512, G=128 -> 2048 B), then
+    # the bias operand: 256 rows of 3 * 4 columns rounded up to 64, bf16
+    assert w4.repacked_bytes(256, 512, 128, w4.AFFINE) == 65536 + 2048 + 2048 + 256 * 64 * 2
     assert w4.gateup_repacked_bytes(100, 512, 128, w4.AFFINE) == w4.repacked_bytes(256, 512, 128, w4.AFFINE)
     assert w4.repacked_bytes(256, 512, 128, 3) == 0  # no such form
-    # group sums: K/G rows of M rounded up to 256 floats
-    assert w4.xsum_bytes(17, 512, 64) == 8 * 256 * 4
-    assert w4.xsum_bytes(300, 5120, 128) == 40 * 512 * 4
+    # group sums: M rows of 3 * K/G bf16 parts rounded up to 64
+    assert w4.xsum_bytes(17, 512, 64) == 17 * 64 * 2
+    assert w4.xsum_bytes(300, 5120, 128) == 300 * 128 * 2
+    assert w4.xsum_bytes(4, 5120, 64) == 4 * 256 * 2
     assert w4.xsum_bytes(0, 512, 64) == 0 and w4.xsum_bytes(4, 100, 64) == 0
     # the zero-point calls reject the affine form, and the affine repack needs biases
     assert _gemm(L, sym=2) == INVALID

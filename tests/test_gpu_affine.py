@@ -49,17 +49,22 @@ def test_dequantize_affine(N, K, group):
 
 @pytest.mark.parametrize("M,K,group", [(1, 512, 64), (17, 640, 128), (300, 1024, 64), (256, 256, 128)])
 def test_xsum_parity(M, K, group):
+    """Three bf16 parts per group whose sum is a float32 sum of the group's x
+    (within its summation bound of the exact sum); zeros past 3 * K/G."""
     x = synth.make_x(M, K, seed=M + K)
     xs = w4.xsum(dev(x), K, group)
     _finish()
-    got = xs.cpu().numpy().astype(np.float64)
-    ld = got.shape[1]
-    assert ld % 256 == 0 and ld >= M
-    ref = oracle.group_sums(x, M, K, group)
-    absx = oracle.group_sums(x & np.uint16(0x7FFF), M, K, group)  # sums of |x|
-    bound = group * 2.0 ** -24 * absx
-    assert np.all(np.abs(got[:, :M] - ref) <= bound)
-    assert np.all(got[:, M:] == 0.0)
+    parts = synth.bf16_bits_to_f32(host_bits(xs)).astype(np.float64)
+    G3 = 3 * (K // group)
+    assert parts.shape == (M, (G3 + 63) // 64 * 64)
+    assert np.all(parts[:, G3:] == 0.0)
+    hi, mid, lo = parts[:, 0:G3:3], parts[:, 1:G3:3], parts[:, 2:G3:3]
+    got = hi + mid + lo                                   # exact in float64
+    assert np.all(got.astype(np.float32).astype(np.float64) == got)  # a float32 value
+    assert np.all(synth.f32_to_bf16_bits(got.astype(np.float32)) == host_bits(xs)[:, 0:G3:3])  # hi = bf16(X)
+    ref = oracle.group_sums(x, M, K, group).T              # [M, groups]
+    absx = oracle.group_sums(x & np.uint16(0x7FFF), M, K, group).T  # sums of |x|
+    assert np.all(np.abs(got - ref) <= group * 2.0 ** -24 * absx)
 
 
 GEMM_CASES = [

@@ -22,9 +22,9 @@ def test_noalloc_rejects_tables_over_4_mib():
     L = w4.lib()
     P = ctypes.c_void_p
     fake = 1 << 20
-    # K = 5120, group 64: 80 rows of round_up(M, 256) floats; 4 MiB holds M <= 13,056
-    assert w4.xsum_bytes(13056, 5120, 64) <= 4 << 20 < w4.xsum_bytes(13057, 5120, 64)
-    assert L.w4a16_gemm_affine_noalloc(P(fake), P(fake), 13057, 64, 5120, 64, P(fake), None) == -1
+    # K = 5120, group 64: M rows of 256 bf16 parts; 4 MiB holds M <= 8,192
+    assert w4.xsum_bytes(8192, 5120, 64) <= 4 << 20 < w4.xsum_bytes(8193, 5120, 64)
+    assert L.w4a16_gemm_affine_noalloc(P(fake), P(fake), 8193, 64, 5120, 64, P(fake), None) == -1
     assert L.w4a16_gemm_affine_noalloc(None, P(fake), 17, 64, 128, 64, P(fake), None) == -1
     assert L.w4a16_gemm_affine_noalloc(P(fake + 8), P(fake), 17, 64, 128, 64, P(fake), None) == -2
 

@@ -86,13 +86,13 @@ def step_parts(workload: str):
 
 def part_units(w):
     """(units per call, metric unit, is_flops): FLOPs for the prompt regime
-    (M > 16, tensor-bound), algorithmic bytes for decode (M <= 16, HBM-bound)."""
+    (M > 32, tensor-bound), algorithmic bytes for decode (M <= 32, HBM-bound)."""
     aff = w.get("affine", False)
     if w["kind"] == "gateup":
-        if w["M"] > 16:
+        if w["M"] > 32:
             return gemm_flops(w["M"], 2 * w["N"], w["K"]), "TFLOP/s", True
         return gateup_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"], aff), "GB/s", False
-    if w["M"] > 16:
+    if w["M"] > 32:
         return gemm_flops(w["M"], w["N"], w["K"]), "TFLOP/s", True
     return algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"], aff), "GB/s", False
 
@@ -102,7 +102,7 @@ def metric_name(workload):
     if part_units(parts[0][1])[2]:
         if parts[0][1]["kind"] == "gateup":
             return "W4A16 fused gate/up GEMM TFLOP/s (M=4096, K=5120, 2x17408)"
-        return "W4A16 GEMM TFLOP/s (M>16)"
+        return "W4A16 GEMM TFLOP/s (M>32)"
     return "W4A16 GEMM eff. HBM GB/s (M=1..16)"
 
 
@@ -244,7 +244,7 @@ def run_cuda(args, rank, world):
         pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
         # affine form on the tcgen05 GEMM: the group sums of x, formed every call
         pt["xs"] = (torch.empty(w4.xsum_bytes(w["M"], w["K"], w["group"]) // 2, dtype=torch.bfloat16, device=dev)
-                    if p["affine"] and (w["M"] > 16 or args.kernel == "tc") else None)
+                    if p["affine"] and (w["M"] > 32 or args.kernel == "tc") else None)
         pt["idx"] = torch.empty(w["M"], dtype=torch.int64, device=dev)
         pt["idx_host"] = torch.empty(w["M"], dtype=torch.int64).pin_memory()
         pt["x_host"] = torch.from_numpy(p["x"].view(np.int16)).pin_memory()

@@ -210,14 +210,14 @@ def gemm(x, packed, N, K, group, sym, out=None, stream=None):
 
 def gemm_argmax(x, packed, N, K, group, sym, out=None, logits=False, stream=None, index_out=None):
     """int64 [M]: the first column of each row of y = x . dequant(W)^T (bf16)
-    at which y is largest (torch.argmax over the bf16 row). For M <= 16 the
+    at which y is largest (torch.argmax over the bf16 row). For M <= 32 the
     logits are stored only when `logits` is true or `out` is given; returns
     (argmax, y or None)."""
     torch = _torch()
     M = x.shape[0]
     if x.dim() != 2 or x.shape[1] != K:
         raise ValueError("x must be [M, K]")
-    if out is None and (logits or M > 16):
+    if out is None and (logits or M > 32):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     idx = index_out if index_out is not None else torch.empty(M, dtype=torch.int64, device=x.device)
     rc = lib().w4a16_gemm_argmax(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), M, N, K,
@@ -302,7 +302,7 @@ def _xs_ptr(xs):
 
 def gemm_affine(x, packed, N, K, group, xs=None, out=None, stream=None):
     """y[M, N] (bf16) = x . (scale * q + bias)^T. `xs` (from xsum) is needed
-    for M > 16; None lets the M <= 16 kernel form the group sums itself."""
+    for M > 32; None lets the M <= 32 kernels form the group sums themselves."""
     torch = _torch()
     M = x.shape[0]
     if x.dim() != 2 or x.shape[1] != K:
@@ -366,7 +366,7 @@ def set_kernel_override(which: int) -> int:
 
 
 def set_programmatic_overlap(on: bool) -> bool:
-    """Let each M <= 16 call start streaming its weights while the previous
+    """Let each M <= 32 call start streaming its weights while the previous
     kernel on the stream finishes (x and y are touched only after it has).
     Only while packed weights are read-only and complete; returns the previous
     setting."""

@@ -84,7 +84,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int finish_launch(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : cuda_fail(e); }
 
-// The M <= 16 kernels: override 2 keeps the per-warp-ring kernel, override 4
+// The decode kernels (M <= 32): override 2 keeps the per-warp-ring kernel, override 4
 // forces the x-staged one, otherwise the x-staged kernel takes M <= 8 calls
 // whose grid fills a wave
 cudaError_t launch_decode_kernel(GemmCall &c, int sm_count) {
@@ -93,12 +93,19 @@ cudaError_t launch_decode_kernel(GemmCall &c, int sm_count) {
   return launch_smallm_mma(c, sm_count);
 }
 
+// Rows that go to a decode kernel rather than the tcgen05 GEMM: M <= 32
+// (graph-timed at N = 34816, K = 5120: M = 17-24 36.5 us against 66.8 on the
+// tcgen05 GEMM, M = 32 47.6 against 66.8; 3.7-4.9x at N = 5120, where the
+// GEMM has few tiles), unless the tcgen05 GEMM is forced (override 3)
+constexpr int kDecodeMaxM = 32;
+bool use_decode(int M) { return M <= kDecodeMaxM && g_override.load() != 3; }
+
 bool form_ok(int form) { return form == kFormZero || form == kFormSym || form == kFormAffine; }
 bool zero_form(int form) { return form == kFormZero || form == kFormSym; }
 
-// The affine calls: the decode kernel for M <= 16 (it forms the x group sums
+// The affine calls: the decode kernel for M <= 32 (it forms the x group sums
 // itself), else the tcgen05 GEMM, which reads them from `xsum`.
-bool affine_uses_tc(int M) { return M > 16 || g_override.load() == 3; }
+bool affine_uses_tc(int M) { return !use_decode(M); }
 
 int launch_affine(GemmCall &c, const uint16_t *xsum, const DeviceInfo &d) {
   if (!affine_uses_tc(c.M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
@@ -206,11 +213,11 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym, false,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
-  // M <= 16: the tensor-core decode kernel (measured faster than the CUDA-core
+  // M <= 32: a tensor-core decode kernel (measured faster than the CUDA-core
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
   const int ov = g_override.load();
   if (M == 1 && ov == 1) return finish_launch(launch_gemv_m1(c, d.sm_count));
-  if (M <= 16 && ov != 3) return finish_launch(launch_decode_kernel(c, d.sm_count));
+  if (use_decode(M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
@@ -225,14 +232,14 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym, true,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
-  if (M <= 16 && g_override.load() != 3) return finish_launch(launch_decode_kernel(c, d.sm_count));
+  if (use_decode(M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
 int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym,
                       uint16_t *y, int64_t *argmax, w4a16_stream_t stream) {
   if (!x || !packed || !argmax) return W4A16_ERR_INVALID_ARG;
-  if (!sizes_ok(M, N, K, group) || !zero_form(sym) || (M > 16 && !y)) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group) || !zero_form(sym) || (!use_decode(M) && !y)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(argmax, 8))
     return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
@@ -243,7 +250,7 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
   cudaError_t e = launch_argmax_init(argmax, M, overlap, s);
   if (e != cudaSuccess) return cuda_fail(e);
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym, false, s, d.err, d.device, overlap};
-  if (M <= 16 && g_override.load() != 3) {
+  if (use_decode(M)) {
     c.amax = argmax;  // keys from the decode kernel's epilogue; y may be NULL
     e = launch_decode_kernel(c, d.sm_count);
   } else {

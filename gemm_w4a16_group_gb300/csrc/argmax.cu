@@ -5,7 +5,7 @@
 // Keys (w4a16_common.cuh, argmax_key) order the bf16 values and break ties
 // toward the lower index; every producer folds its keys into keys[m] with
 // 64-bit atomicMax on a buffer zeroed before, and the finalize step rewrites
-// each key as its index in place. The M <= 16 decode kernel produces keys in
+// each key as its index in place. The M <= 32 decode kernels produce keys in
 // its epilogue (fused); for y already in memory, row_argmax_kernel does.
 #include "w4a16_internal.h"
 

@@ -1,4 +1,4 @@
-// Decode-regime kernels, M <= 16 rows of x against the whole weight.
+// Decode-regime kernels, M <= 32 rows of x against the whole weight.
 //
 // Both kernels stream the repacked weight exactly once per call (HBM-bound)
 // and are built around the integer-ALU cost of the nibble unpack, which is
@@ -301,8 +301,8 @@ struct DecodeSmem {
   static constexpr int kRingOff = 0;
   static constexpr int kBarOff = kWarps * R::kWarpBytes;
   static constexpr int kRedOff = kBarOff + kWarps * SLOTS * 8;
-  static constexpr int kBestOff = kRedOff + kWarps * E * 4;  // 16 argmax keys, one per x row
-  static constexpr int kFlagOff = kBestOff + 16 * 8;
+  static constexpr int kBestOff = kRedOff + kWarps * E * 4;  // argmax keys, one per x row (<= 32)
+  static constexpr int kFlagOff = kBestOff + 32 * 8;
   static constexpr int kBytes = kFlagOff + 16;
 };
 
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
   const int tile0 = blockIdx.x * TPW;
   unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + SM::kBestOff);
   if (threadIdx.x == 0) *abort_flag = 0;
-  if (threadIdx.x < 16) best[threadIdx.x] = 0;
+  if (threadIdx.x < 32) best[threadIdx.x] = 0;
   __syncthreads();
   int ub, ue;
   k_slice(p.units, ub, ue);
@@ -1105,10 +1105,13 @@ cudaError_t run_mma(const DecodeParams &p, int sm_count, cudaStream_t s) {
 
 // Two 16-row tiles per warp at every N (measured faster than four at the
 // 248,320-row head: more resident warps per SM).
+// n8 tiles of x rows by M (up to 32 rows)
 template <int QF, int CPG, bool GATEUP>
 cudaError_t run_mma_m(const DecodeParams &p, int sm_count, cudaStream_t s) {
   if (p.M <= 8) return run_mma<1, 2, QF, CPG, GATEUP>(p, sm_count, s);
-  return run_mma<2, 2, QF, CPG, GATEUP>(p, sm_count, s);
+  if (p.M <= 16) return run_mma<2, 2, QF, CPG, GATEUP>(p, sm_count, s);
+  if (p.M <= 24) return run_mma<3, 2, QF, CPG, GATEUP>(p, sm_count, s);
+  return run_mma<4, 2, QF, CPG, GATEUP>(p, sm_count, s);
 }
 
 template <int QF, bool GATEUP>
@@ -1211,7 +1214,7 @@ cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(packed_rows(c), c.K, c.group, c.sym);
   DecodeParams p = make_params(c, L);
   // the x-staged kernel: forced, or chosen for M <= 8 when its grid fills a wave
-  if (c.xs_mode == 2 || (c.xs_mode == 1 && c.M <= 8)) {
+  if (c.M <= 16 && (c.xs_mode == 2 || (c.xs_mode == 1 && c.M <= 8))) {
     bool launched = false;
     const bool only_full = c.xs_mode == 1;
     const cudaError_t e = c.gateup ? run_xs_all<true>(p, sm_count, c.sym, c.group, c.stream, only_full, &launched)

@@ -31,8 +31,8 @@ struct GemmCall {
   cudaStream_t stream;
   int *err;    // device error word (bounded waits that gave up)
   int device;  // current device ordinal, < kMaxDevices
-  bool overlap;  // programmatic overlap with the previous kernel (M <= 16 kernels)
-  int64_t *amax = nullptr;  // argmax keys per x row (M <= 16 plain GEMM), or null
+  bool overlap;  // programmatic overlap with the previous kernel (M <= 32 kernels)
+  int64_t *amax = nullptr;  // argmax keys per x row (M <= 32 plain GEMM), or null
   const uint16_t *xsum = nullptr;  // affine form, tcgen05 GEMM: x group sums, bf16 parts [M][kb3]
   int xs_mode = 1;  // M <= 16, the kernel that stages x once per CTA: 0 never, 1 when it fits, 2 always
 };

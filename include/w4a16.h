@@ -119,10 +119,10 @@ int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const i
  * float32 accumulation; each group's partial sum is scaled in float32.
  * `scales` and `zeros` are reserved: scales and zero points travel inside
  * `packed`, and both must be NULL (else W4A16_ERR_INVALID_ARG).
- * Kernel choice: M <= 16 -> a decode kernel (each weight read and unpacked
+ * Kernel choice: M <= 32 -> a decode kernel (each weight read and unpacked
  * once for all rows, multiply-adds on the tensor core): the one that stages x
  * once per CTA when M <= 8 and its grid fills the GPU, else the one with a
- * weight ring per warp; M > 16 -> the tcgen05 GEMM. A CUDA-core one-row GEMV
+ * weight ring per warp; M > 32 -> the tcgen05 GEMM. A CUDA-core one-row GEMV
  * is selectable (w4a16_set_kernel_override).
  * Results are bitwise reproducible run to run (no atomics in any sum).
  */
@@ -140,9 +140,9 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales,
  * the GRIMOIRE v1.8 release notes, "INT4 verify faster").
  *
  *   argmax  int64 [M], device, 8-byte aligned; written by this call
- *   y       bf16 [M][N] or NULL. M <= 16: the decode kernel forms the argmax
+ *   y       bf16 [M][N] or NULL. M <= 32: the decode kernel forms the argmax
  *           in its epilogue and stores y only when y is not NULL (the logits
- *           need not exist). M > 16: required; the tcgen05 GEMM writes y and
+ *           need not exist). M > 32: required; the tcgen05 GEMM writes y and
  *           a second kernel reads it back.
  *
  * Launches three kernels on `stream` (zero the keys, the GEMM, turn keys
@@ -214,8 +214,8 @@ int w4a16_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xsum, w4a16
 /*
  * y[M][N] (bf16) = x . (scale * q + bias)^T, W from w4a16_repack_affine.
  * `xsum` (w4a16_xsum of the same x, K and group, complete when the stream
- * reaches this call) is read by the tcgen05 GEMM (M > 16); it may be NULL
- * when M <= 16, where the decode kernel forms the group sums itself with one
+ * reaches this call) is read by the tcgen05 GEMM (M > 32); it may be NULL
+ * when M <= 32, where the decode kernel forms the group sums itself with one
  * more tensor-core product per 16 k (then it is not read).
  */
 int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packed, int M, int N, int K, int group,
@@ -224,7 +224,7 @@ int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packe
 /*
  * w4a16_gemm_affine without the caller's group-sum table: this library's own
  * addition, with no counterpart on the pages the method comes from. For
- * M > 16 the group sums go to a fixed 4 MiB device array inside the library's
+ * M > 32 the group sums go to a fixed 4 MiB device array inside the library's
  * module image (one per device, found once with cudaGetSymbolAddress), so the
  * call allocates nothing and needs no workspace argument; sizes whose table
  * (w4a16_xsum_bytes) exceeds 4 MiB are W4A16_ERR_INVALID_ARG (at K = 5120 and
@@ -232,7 +232,7 @@ int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packe
  * included, is written by the call itself before the GEMM reads it, so
  * nothing has to start at zero. The array is shared: calls in flight at the
  * same time on one device (other streams, other host threads) race on it and
- * may compute wrong results; calls in order on one stream are safe. M <= 16
+ * may compute wrong results; calls in order on one stream are safe. M <= 32
  * uses no table and behaves exactly as w4a16_gemm_affine.
  */
 int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int group, uint16_t *y,
@@ -260,7 +260,7 @@ int w4a16_last_cuda_error(void);
 /*
  * Kernel selection override for A/B measurement: 0 = automatic (default),
  * 1 = force the CUDA-core one-row GEMV for M = 1 (zero-point forms), 2 = force
- * the small-M tensor-core kernel with per-warp weight rings for M <= 16, 3 =
+ * the small-M tensor-core kernel with per-warp weight rings for M <= 32, 3 =
  * force the tcgen05 GEMM for any M, 4 = force the small-M kernel that stages x
  * once per CTA for M <= 16 (automatic choice: M <= 8 calls whose grid of
  * 128-row CTAs fills the GPU, e.g. the output-vocabulary head).
@@ -270,8 +270,8 @@ int w4a16_last_cuda_error(void);
 int w4a16_set_kernel_override(int which);
 
 /*
- * Programmatic overlap of consecutive decode calls (M <= 16), off by default.
- * When on, the M <= 16 kernels are launched with programmatic stream
+ * Programmatic overlap of consecutive decode calls (M <= 32), off by default.
+ * When on, the M <= 32 kernels are launched with programmatic stream
  * serialization: a call may start while the previous kernel on its stream is
  * still running, begin streaming its packed weights (and scales and zeros)
  * at once, and wait for that kernel to finish (and its writes to become

@@ -113,7 +113,7 @@ def test_argmax_entry_point_argument_checks(L):
     g = L.w4a16_gemm_argmax
     assert g(None, P(FAKE), 4, 64, 128, 64, 1, P(FAKE), P(FAKE), None) == INVALID
     assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, P(FAKE), None, None) == INVALID     # no output
-    assert g(P(FAKE), P(FAKE), 17, 64, 128, 64, 1, None, P(FAKE), None) == INVALID    # M > 16 needs y
+    assert g(P(FAKE), P(FAKE), 33, 64, 128, 64, 1, None, P(FAKE), None) == INVALID    # M > 32 needs y
     assert g(P(FAKE), P(FAKE), 4, 64, 96, 64, 1, None, P(FAKE), None) == INVALID      # K % G
     assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, None, P(FAKE + 4), None) == MISALIGNED
     assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, P(FAKE + 2), P(FAKE), None) == MISALIGNED
@@ -140,11 +140,11 @@ def test_affine_layout_and_argument_checks(L):
     assert L.w4a16_repack_affine(P(FAKE), P(FAKE), P(FAKE + 1), 64, 128, 64, P(FAKE), None) == MISALIGNED
     assert L.w4a16_repack_affine_gateup(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, 64, 128, 64,
                                         P(FAKE), None) == INVALID
-    # M > 16 runs the tcgen05 GEMM, which reads the group sums: they are required
+    # M > 32 runs the tcgen05 GEMM, which reads the group sums: they are required
     ga = L.w4a16_gemm_affine
-    assert ga(P(FAKE), None, P(FAKE), 17, 64, 128, 64, P(FAKE), None) == INVALID
-    assert ga(P(FAKE), P(FAKE + 4), P(FAKE), 17, 64, 128, 64, P(FAKE), None) == MISALIGNED
-    assert ga(P(FAKE), P(FAKE), P(FAKE), 17, 64, 96, 64, P(FAKE), None) == INVALID
+    assert ga(P(FAKE), None, P(FAKE), 33, 64, 128, 64, P(FAKE), None) == INVALID
+    assert ga(P(FAKE), P(FAKE + 4), P(FAKE), 33, 64, 128, 64, P(FAKE), None) == MISALIGNED
+    assert ga(P(FAKE), P(FAKE), P(FAKE), 33, 64, 96, 64, P(FAKE), None) == INVALID
     assert L.w4a16_gateup_silu_affine(P(FAKE), None, P(FAKE), 300, 64, 128, 64, P(FAKE), None) == INVALID
     assert L.w4a16_xsum(P(FAKE), 4, 128, 64, None, None) == INVALID
     assert L.w4a16_xsum(P(FAKE), 4, 128, 64, P(FAKE + 8), None) == MISALIGNED

@@ -4,7 +4,7 @@ oracle: the dequantised read-back is scale * q + bias rounded once to float32,
 the group sums of x are float32 sums within their summation bound, and every
 matmul output lies within |y - ref| <= 2^-7 |ref| + 1e-5 sum_k |x_k w_nk|
 (the fused gate/up output within oracle.silu_bound). Sizes span several tiles
-with ragged tails in M, N and K, on the decode kernel (M <= 16, group sums
+with ragged tails in M, N and K, on the decode kernels (M <= 32, group sums
 formed in the kernel) and the tcgen05 GEMM (group sums from w4a16_xsum)."""
 import numpy as np
 import pytest
@@ -77,6 +77,8 @@ GEMM_CASES = [
     (AUTO, 13, 250, 512, 64),
     (AUTO, 16, 520, 2048, 128),
     (AUTO, 16, 32, 5120, 64),       # short N: split K across a cluster
+    (SMALLM, 24, 250, 512, 64),
+    (SMALLM, 32, 520, 1024, 128),
     (XS, 1, 250, 512, 64),
     (XS, 5, 250, 1024, 128),
     (XS, 16, 520, 2048, 128),
@@ -99,7 +101,7 @@ def test_gemm_affine_parity(which, M, N, K, group):
     x = dev(p["x"])
     packed = _packed(p)
     with kernel(which):
-        xs = w4.xsum(x, K, group) if (M > 16 or which == TC) else None
+        xs = w4.xsum(x, K, group) if (M > 32 or which == TC) else None
         y = w4.gemm_affine(x, packed, N, K, group, xs)
     _finish()
     ref, sa = oracle.gemm_affine(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, group)
@@ -115,7 +117,7 @@ def test_affine_one_hot_x_gives_rounded_weight(M):
     x = np.zeros((M, K), np.uint16)
     x[np.arange(M), ks] = 0x3F80
     xd = dev(x)
-    xs = w4.xsum(xd, K, group) if M > 16 else None
+    xs = w4.xsum(xd, K, group) if M > 32 else None
     y = w4.gemm_affine(xd, _packed(p), N, K, group, xs)
     _finish()
     w = oracle.dequant_affine(p["qweight"], p["scales"], p["biases"], N, K, group)
@@ -132,7 +134,7 @@ def test_gateup_affine_parity(which, M, N, K, group):
     x = dev(p["x"])
     packed = _packed(p, gateup=True)
     with kernel(which):
-        xs = w4.xsum(x, K, group) if (M > 16 or which == TC) else None
+        xs = w4.xsum(x, K, group) if (M > 32 or which == TC) else None
         h = w4.gateup_silu_affine(x, packed, N, K, group, xs)
     _finish()
     mi, ni = np.repeat(np.arange(M), N), np.tile(np.arange(N), M)

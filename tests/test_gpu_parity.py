@@ -47,6 +47,12 @@ CASES = [
     (SMALLM, 13, 250, 512, 64, False),
     (SMALLM, 16, 1040, 1024, 128, True),
     (SMALLM, 16, 32, 5120, 64, False),
+    # 17-32 rows on the small-M kernel (three and four n8 tiles of x rows)
+    (SMALLM, 17, 520, 1024, 64, False),
+    (SMALLM, 24, 250, 512, 128, True),
+    (SMALLM, 25, 1040, 2048, 64, False),
+    (SMALLM, 32, 300, 640, 128, True),
+    (SMALLM, 32, 32, 5120, 64, False),
     # the small-M kernel that stages x once per CTA: one CTA (8 tiles), ragged
     # N, cluster split-K on short N, a ragged last K unit (K = 640, 1088)
     (XS, 1, 250, 512, 128, True),
@@ -137,6 +143,8 @@ GATEUP_CASES = [
     (SMALLM, 1, 136, 512, 128, True),
     (SMALLM, 5, 300, 1024, 64, False),
     (SMALLM, 16, 128, 2048, 128, True),
+    (SMALLM, 20, 136, 512, 128, True),
+    (SMALLM, 32, 300, 1024, 64, False),
     (XS, 1, 136, 512, 128, True),
     (XS, 5, 300, 1024, 64, False),
     (XS, 16, 128, 2048, 128, True),
@@ -182,6 +190,7 @@ ARGMAX_CASES = [
     (16, 520, 5120, 64, False),
     (1, 96, 17408, 128, True),
     (24, 300, 640, 128, True),
+    (40, 300, 640, 128, True),
 ]
 
 
@@ -203,7 +212,7 @@ def test_gemm_argmax_matches_first_max_of_y(M, N, K, group, sym, which):
     np.testing.assert_array_equal(a1.cpu().numpy(), want)
     np.testing.assert_array_equal(a2.cpu().numpy(), want)
     np.testing.assert_array_equal(bf16_f64(host_bits(y1)), y)
-    assert (y2 is None) == (M <= 16)
+    assert (y2 is None) == (M <= 32)
 
 
 @pytest.mark.parametrize("M", [1, 7, 30])
@@ -223,7 +232,7 @@ def test_gemm_argmax_ties_pick_the_first_column(M):
     d = upload(pp)
     packed = packed_of(pp, d)
     y = bf16_f64(run_gemm(pp, d=d, packed=packed))
-    a, _ = w4.gemm_argmax(d["x"], packed, N, K, group, True, logits=M > 16)
+    a, _ = w4.gemm_argmax(d["x"], packed, N, K, group, True, logits=M > 32)
     torch().cuda.synchronize()
     got = a.cpu().numpy()
     np.testing.assert_array_equal(got, np.argmax(y, axis=1))

@@ -69,7 +69,6 @@ constexpr int SL = W4A16_PROMPT_SL;
 constexpr int SW = SL;
 constexpr int SS = 2;                // scale-block ring (4 groups each)
 constexpr int kThreads = 512;
-constexpr uint16_t kPairMask = 0x3;
 
 constexpr int W_BYTES = HW * BK * 2;  // 16384
 constexpr int Q_BYTES = HW * BK / 2;  // 4096
@@ -127,6 +126,8 @@ struct PromptParams {
   int ng;          // K / group
   int spg;         // 64-wide stages per group (1 or 2)
   int nkb;         // affine: 64-wide stages of the closing bias group (0 otherwise)
+  int kc;          // pairs per cluster: 1 = persistent pairs; > 1 = split K, one tile per cluster
+  int gblk;        // blocks of four groups (K split at block boundaries)
   int *err;
   UnpackConsts uc;
 };
@@ -150,12 +151,13 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, uint32_t peer_
   atomicExch(err, kErrTimeout);
 }
 
-// arrive on the even CTA's copy of a barrier: locally there, remotely from the odd CTA
-__device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t rank) {
+// arrive on the even CTA's copy of a barrier: locally there, remotely from the
+// odd CTA (pbase: the even CTA's rank in the cluster)
+__device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t rank, uint32_t pbase) {
   if (rank == 0)
     mbar_arrive(bar);
   else
-    mbar_arrive_remote(mapa_shared(bar, 0));
+    mbar_arrive_remote(mapa_shared(bar, pbase));
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
@@ -180,10 +182,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::OFF_MISC + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: odd
-  const uint32_t peer_abort = mapa_shared(smem_u32(smem + G::OFF_MISC + 4), rank ^ 1u);
+  // A cluster holds p.kc pairs (ranks 2j, 2j+1). With kc = 1 the pairs are
+  // persistent and walk the tiles; with kc > 1 a cluster owns one tile and
+  // pair j takes part j of its K range (whole blocks of four groups).
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;    // 0: even CTA of the pair (issues the MMAs), 1: odd
+  const uint32_t pbase = crank & ~1u;  // the even CTA's rank in the cluster
+  const int kpart = (int)(crank >> 1);
+  const uint16_t pair_mask = (uint16_t)(3u << pbase);
+  const uint32_t peer_abort = mapa_shared(smem_u32(smem + G::OFF_MISC + 4), crank ^ 1u);
   const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
   const int ntot = p.mtiles * p.ntiles;
+  const int g0 = 4 * (int)((long long)p.gblk * kpart / p.kc);
+  const int g1 = min(4 * (int)((long long)p.gblk * (kpart + 1) / p.kc), p.ng);  // this pair's groups [g0, g1)
+  const int kb0 = g0 * p.spg, kb1 = g1 * p.spg;                                  // and 64-wide stages
+  const bool bias_group = AFF && kpart == 0;  // affine: the closing bias group, once per tile
 
   if (tid == 0) {
     for (int i = 0; i < SL; ++i) {
@@ -238,17 +251,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
         const int mt = tile % p.mtiles, nt = tile / p.mtiles;
         const int qt = nt * (BW / 16) + (int)rank * NT16;  // first 16-row tile of this CTA's weights
-        const int nkt = AFF ? p.nk + p.nkb : p.nk;  // stages of a tile
-        for (int kb = 0; kb < nkt; ++kb) {
-          if (AFF && kb >= p.nk) {
+        const int kbe = bias_group ? kb1 + p.nkb : kb1;  // this pair's stages of a tile
+        for (int kb = kb0; kb < kbe; ++kb) {
+          if (AFF && kb >= kb1) {
             // affine closing group: x group sums into the x slot, the bias
             // operand straight into the W slot
             const int slot = ls % SL;
             if (!mbar_wait(bars.empty_L(slot), ((ls / SL) & 1) ^ 1, abort_flag)) { ok = false; break; }
             mbar_arrive_expect_tx(bars.full_L(slot), G::X_BYTES + W_BYTES);
-            tma_load_2d_hint(sbase + G::OFF_X + slot * G::X_BYTES, &tm_xs, (kb - p.nk) * BK,
+            tma_load_2d_hint(sbase + G::OFF_X + slot * G::X_BYTES, &tm_xs, (kb - kb1) * BK,
                              mt * G::BX + (int)rank * G::HX, bars.full_L(slot), pol_keep);
-            tma_load_2d_hint(sbase + G::OFF_W + slot * W_BYTES, &tm_z, (kb - p.nk) * BK, qt * 16, bars.full_L(slot),
+            tma_load_2d_hint(sbase + G::OFF_W + slot * W_BYTES, &tm_z, (kb - kb1) * BK, qt * 16, bars.full_L(slot),
                              pol_stream);
             ++ls;
             continue;
@@ -290,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ls = 0, ws = 0, gc = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < ntot; tile += npairs) {
-        const int ngt = AFF ? p.ng + 1 : p.ng;  // groups of a tile (affine: + the bias group)
-        for (int gi = 0; ok && gi < ngt; ++gi) {
-          const int nst = (AFF && gi == p.ng) ? p.nkb : p.spg;  // stages of this group
+        const int ge = bias_group ? g1 + 1 : g1;  // this pair's groups of a tile (+ the bias group)
+        for (int gi = g0; ok && gi < ge; ++gi) {
+          const int nst = (AFF && gi == g1) ? p.nkb : p.spg;  // stages of this group
           const int b = gc % G::NB;
           if (!mbar_wait(bars.tempty(b), ((gc / G::NB) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -316,12 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the address field
               tc_mma2_f16(d_tmem, wdesc + 2 * kk, xdesc + 2 * kk, G::kIdesc, (ks | kk) != 0);
             }
-            tc_commit2_mc(bars.empty_L(sl), kPairMask);  // frees x, codes and W of the stage
+            tc_commit2_mc(bars.empty_L(sl), pair_mask);  // frees x, codes and W of the stage
             ++ls;
             ++ws;
           }
           if (!ok) break;
-          tc_commit2_mc(bars.tfull(b), kPairMask);
+          tc_commit2_mc(bars.tfull(b), pair_mask);
           ++gc;
         }
       }
@@ -340,14 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int cur = 0;
     bool ok = true;
     for (int tile = pair; ok && tile < ntot; tile += npairs) {
-      const int nkt = AFF ? p.nk + p.nkb : p.nk;
-      for (int kb = 0; kb < nkt; ++kb) {
-        if (AFF && kb >= p.nk) {
+      const int kbe = bias_group ? kb1 + p.nkb : kb1;
+      for (int kb = kb0; kb < kbe; ++kb) {
+        if (AFF && kb >= kb1) {
           // affine closing group: TMA filled the W slot; pass it on
           const int sl = ls % SL, sw = ws % SW;
           if (!mbar_wait(bars.full_L(sl), (ls / SL) & 1, abort_flag)) { ok = false; break; }
           __syncwarp();
-          if (lane == 0) arrive_even(bars.full_W(sw), rank);
+          if (lane == 0) arrive_even(bars.full_W(sw), rank, pbase);
           ++ls;
           ++ws;
           continue;
@@ -400,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          arrive_even(bars.full_W(sw), rank);
-          if (ZP && ((kb + 1) % (4 * p.spg) == 0 || kb + 1 == p.nk)) mbar_arrive(bars.empty_S(cur));
+          arrive_even(bars.full_W(sw), rank, pbase);
+          if (ZP && ((kb + 1) % (4 * p.spg) == 0 || kb + 1 == kb1)) mbar_arrive(bars.empty_S(cur));
         }
         ++ls;
         ++ws;
@@ -425,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = tile % p.mtiles, nt = tile / p.mtiles;
 #pragma unroll
       for (int c = 0; c < EC; ++c) acc[c] = 0.f;
-      for (int gi = 0; gi < p.ng + (AFF ? 1 : 0); ++gi) {
-        const bool real = !AFF || gi < p.ng;  // not the affine closing group (scale 1)
+      for (int gi = g0; gi < (bias_group ? g1 + 1 : g1); ++gi) {
+        const bool real = !AFF || gi < g1;  // not the affine closing group (scale 1)
         if (real && (gi & 3) == 0) {
           cur = sc % SS;
           if (!mbar_wait(bars.full_S(cur), (sc / SS) & 1, abort_flag)) { ok = false; break; }
@@ -454,12 +467,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          arrive_even(bars.tempty(b), rank);
-          if (real && ((gi & 3) == 3 || gi == p.ng - 1)) mbar_arrive(bars.empty_S(cur));
+          arrive_even(bars.tempty(b), rank, pbase);
+          if (real && ((gi & 3) == 3 || gi == g1 - 1)) mbar_arrive(bars.empty_S(cur));
         }
         ++gc;
       }
       if (!ok) break;
+      if (p.kc > 1) {
+        // split K: the partial sums go to the (now idle) ring, [column][row]
+        // float32, for the cluster's first pair to add up
+        float *part = reinterpret_cast<float *>(smem + G::OFF_X);
+#pragma unroll
+        for (int c = 0; c < EC; ++c) part[(ch2 * EC + c) * HW + wr] = acc[c];
+        continue;
+      }
       // thread = one weight row, EC x rows m0 + c
       const int m0 = mt * G::BX + ch2 * EC;
       if (GATEUP) {
@@ -496,6 +517,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc2(tmem_base, G::kTmemCols);
   }
+  if (p.kc > 1) {
+    // split K: the first pair adds the other pairs' partial sums (same parity
+    // CTA, ranks 2j + rank), in pair order, and stores the tile
+    if (kpart == 0 && !*abort_flag) {
+      const float *part = reinterpret_cast<const float *>(smem + G::OFF_X);
+      const uint32_t part_s = smem_u32(smem + G::OFF_X);
+      const int mt = pair % p.mtiles, nt = pair / p.mtiles;
+      auto sum_at = [&](int idx) {
+        float v = part[idx];
+        for (int j = 1; j < p.kc; ++j) v += ld_cluster_f32(mapa_shared(part_s + 4u * (uint32_t)idx, crank + 2u * j));
+        return v;
+      };
+      if (GATEUP) {
+        // gate row 32q + l and its up row 32q + 16 + l (16-row tiles alternate)
+        for (int e = tid; e < G::BX * HW / 2; e += kThreads) {
+          const int col = e / (HW / 2), rr = e % (HW / 2), q = rr >> 4, l = rr & 15;
+          const float gv = sum_at(col * HW + 32 * q + l), uv = sum_at(col * HW + 32 * q + 16 + l);
+          const int n = 16 * (nt * (BW / 32) + (int)rank * (NT16 / 2) + q) + l;
+          const int m = mt * G::BX + col;
+          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(silu_f32(gv) * uv);
+        }
+      } else {
+        for (int e = tid; e < G::BX * HW; e += kThreads) {
+          const int col = e / HW, row = e % HW;
+          const int n = nt * BW + (int)rank * HW + row, m = mt * G::BX + col;
+          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(sum_at(e));
+        }
+      }
+    }
+    // the other pairs keep their partials until the first pair has read them
+    cluster_sync_all();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -529,7 +582,7 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 
 // Launch as clusters of two CTAs: one pair per tile, as many pairs as fit at
 // once (found once per instantiation and device), each walking the tiles with
-// a stride.
+// a stride; or, split K (p.kc > 1), one cluster of p.kc pairs per tile.
 template <int QF, bool GATEUP, int BXT>
 cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
                            const CUtensorMap &tz, const CUtensorMap &txs, const PromptParams &p, int ntot,
@@ -558,8 +611,13 @@ cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const C
     if (np < 1) return cudaErrorInvalidConfiguration;
     max_pairs.v[device].store(np, std::memory_order_relaxed);
   }
-  const int pairs = ntot < np ? ntot : np;
-  lc.gridDim = dim3(2 * pairs, 1, 1);
+  if (p.kc > 1) {
+    attr[0].val.clusterDim.x = 2 * p.kc;
+    lc.gridDim = dim3(2 * p.kc * ntot, 1, 1);
+  } else {
+    const int pairs = ntot < np ? ntot : np;
+    lc.gridDim = dim3(2 * pairs, 1, 1);
+  }
   return cudaLaunchKernelEx(&lc, kern, tx, tq, ts, tz, txs, p);
 }
 
@@ -570,7 +628,7 @@ cudaError_t launch_form(const CUtensorMap &tx, const CUtensorMap &tq, const CUte
 }
 
 template <int BXT>
-cudaError_t launch_bx(const GemmCall &c) {
+cudaError_t launch_bx(const GemmCall &c, int sm_count) {
   using G = XGeo<BXT, kFormSym>;
   const int rows = packed_rows(c);
   const Layout L = make_layout(rows, c.K, c.group, c.sym);
@@ -609,6 +667,17 @@ cudaError_t launch_bx(const GemmCall &c) {
   p.ng = c.K / c.group;
   p.spg = c.group / BK;
   p.nkb = c.sym == kFormAffine ? L.kb3 / BK : 0;
+  p.gblk = (p.ng + 3) / 4;
+  // Split K when the tiles leave most pairs idle (few weight tiles, short M):
+  // up to 4 pairs per tile, each with at least two blocks of four groups.
+  p.kc = 1;
+  {
+    const int ntiles_all = p.mtiles * p.ntiles, pairs = sm_count / 2;
+    if (ntiles_all * 2 <= pairs) {
+      p.kc = pairs / ntiles_all < 4 ? pairs / ntiles_all : 4;
+      while (p.kc > 1 && p.gblk < 2 * p.kc) --p.kc;
+    }
+  }
   p.err = c.err;
   p.uc = host_unpack_consts();
   const int ntot = p.mtiles * p.ntiles;
@@ -625,11 +694,10 @@ cudaError_t launch_bx(const GemmCall &c) {
 }  // namespace
 
 cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count) {
-  (void)sm_count;  // the pair count comes from the cluster occupancy query
   // x-row tile: the smallest that holds M (a tile of 256 otherwise)
-  if (c.M <= 64) return launch_bx<64>(c);
-  if (c.M <= 128) return launch_bx<128>(c);
-  return launch_bx<256>(c);
+  if (c.M <= 64) return launch_bx<64>(c, sm_count);
+  if (c.M <= 128) return launch_bx<128>(c, sm_count);
+  return launch_bx<256>(c, sm_count);
 }
 
 }  // namespace w4a16

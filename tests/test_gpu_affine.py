@@ -92,6 +92,8 @@ GEMM_CASES = [
     (AUTO, 200, 520, 1024, 64),
     (AUTO, 513, 1040, 768, 128),
     (AUTO, 600, 700, 1024, 64),
+    (AUTO, 48, 300, 2048, 64),      # split K: the bias group on the first pair only
+    (AUTO, 256, 250, 4096, 128),
 ]
 
 

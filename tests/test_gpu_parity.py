@@ -77,6 +77,12 @@ CASES = [
     # several 256 x 256 pair tiles in both directions, ragged in M and N
     (TC, 600, 700, 1024, 64, True),
     (TC, 513, 1040, 768, 128, False),
+    # few tiles: K split across 2, 3 or 4 pairs of a cluster (blocks of four
+    # groups each), the partial sums added over distributed shared memory
+    (TC, 64, 300, 2048, 64, False),
+    (TC, 100, 1040, 1536, 64, True),
+    (TC, 300, 250, 4096, 128, False),
+    (TC, 40, 5120, 1024, 64, True),
 ]
 
 
@@ -145,6 +151,8 @@ GATEUP_CASES = [
     (SMALLM, 16, 128, 2048, 128, True),
     (SMALLM, 20, 136, 512, 128, True),
     (SMALLM, 32, 300, 1024, 64, False),
+    (TC, 40, 136, 2048, 64, False),
+    (TC, 200, 300, 3072, 128, True),
     (XS, 1, 136, 512, 128, True),
     (XS, 5, 300, 1024, 64, False),
     (XS, 16, 128, 2048, 128, True),

@@ -37,6 +37,10 @@ _add("decode_down_m1_k17408_n5120", M=1, K=FFN, N=HIDDEN, group=128, sym=True)
 for _M in (2, 4, 5, 8, 16):
     for _K, _N in ((HIDDEN, HIDDEN), (HIDDEN, 2 * FFN), (FFN, HIDDEN)):
         _add(f"smallm_m{_M}_k{_K}_n{_N}", M=_M, K=_K, N=_N, group=64, sym=False)
+# 17-32 rows (a longer verify window) on the decode kernel, and a 256-row
+# prompt chunk through the down projection (few output tiles: split K)
+_add("verify_m32_k5120_n34816", M=32, K=HIDDEN, N=2 * FFN, group=64, sym=False)
+_add("chunk_m256_k17408_n5120", M=256, K=FFN, N=HIDDEN, group=128, sym=True)
 # single-user decode through the fused gate/up: h = SiLU(x Wg^T) * (x Wu^T),
 # both weights read once (the same 34,816 weight rows as above)
 _add("decode_gateup_silu_m1_k5120_n17408", M=1, K=HIDDEN, N=FFN, group=128, sym=True, kind="gateup")

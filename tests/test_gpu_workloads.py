@@ -1,7 +1,8 @@
 """Every measured workload at full size, in the launch configuration bench.py
 times (automatic kernel choice), checked against the oracle on sampled
-outputs it computes one by one; the output-vocabulary head also on its
-argmax over all 248,320 columns."""
+outputs it computes one by one (the affine workloads through the affine
+entry points and oracle); the output-vocabulary head also on its argmax over
+all 248,320 columns."""
 import numpy as np
 import pytest
 
@@ -11,7 +12,8 @@ from synth.workloads import WORKLOADS
 
 import gemm_w4a16_group_gb300 as w4
 
-from gpu_helpers import assert_within, bf16_f64, packed_of, run_gateup, run_gemm, sample_pairs, torch, upload
+from gpu_helpers import (assert_within, bf16_f64, dev, host_bits, packed_of, run_gateup, run_gemm, sample_pairs, torch,
+                         upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,8 +26,25 @@ def problem(name):
         _cache.clear()  # keep one full-size problem in host memory at a time
         _cache[name] = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"],
                                           scale_range=w["scale_range"], x_scale=w["x_scale"], seed=0,
-                                          gateup=w["kind"] == "gateup")
+                                          gateup=w["kind"] == "gateup", affine=w["affine"])
     return _cache[name]
+
+
+def run_affine(p, gateup):
+    """The affine workload through its public calls, as bench.py makes them
+    (group sums from w4a16_xsum above 32 rows)."""
+    x = dev(p["x"])
+    xs = w4.xsum(x, p["K"], p["group"]) if p["M"] > 32 else None
+    if gateup:
+        packed = w4.repack_affine_gateup(dev(p["qweight"]), dev(p["scales"]), dev(p["biases"]), dev(p["qweight_up"]),
+                                         dev(p["scales_up"]), dev(p["biases_up"]), p["N"], p["K"], p["group"])
+        out = w4.gateup_silu_affine(x, packed, p["N"], p["K"], p["group"], xs)
+    else:
+        packed = w4.repack_affine(dev(p["qweight"]), dev(p["scales"]), dev(p["biases"]), p["N"], p["K"], p["group"])
+        out = w4.gemm_affine(x, packed, p["N"], p["K"], p["group"], xs)
+    torch().cuda.synchronize()
+    assert w4.kernel_status() == 0
+    return host_bits(out)
 
 
 GEMM_NAMES = [n for n, w in WORKLOADS.items() if w["kind"] in ("gemm", "lm_head")]
@@ -34,10 +53,15 @@ GEMM_NAMES = [n for n, w in WORKLOADS.items() if w["kind"] in ("gemm", "lm_head"
 @pytest.mark.parametrize("name", GEMM_NAMES)
 def test_workload_sampled(name):
     p = problem(name)
-    y = run_gemm(p)
     mi, ni = sample_pairs(p["M"], p["N"], 1500, seed=len(name))
-    ref, sa = oracle.gemm_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["M"], p["N"], p["K"],
-                             p["group"], p["sym"], mi, ni)
+    if p["affine"]:
+        y = run_affine(p, gateup=False)
+        ref, sa = oracle.gemm_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], p["M"], p["N"], p["K"],
+                                        p["group"], mi, ni)
+    else:
+        y = run_gemm(p)
+        ref, sa = oracle.gemm_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["M"], p["N"], p["K"],
+                                 p["group"], p["sym"], mi, ni)
     assert_within(y[mi, ni], ref, oracle.gemm_bound(ref, sa), name)
     assert np.isfinite(bf16_f64(y)).all()
 
@@ -76,10 +100,16 @@ GATEUP_NAMES = [n for n, w in WORKLOADS.items() if w["kind"] == "gateup"]
 @pytest.mark.parametrize("name", GATEUP_NAMES)
 def test_gateup_workload_sampled(name):
     p = problem(name)
-    h = run_gateup(p)
     mi, ni = sample_pairs(p["M"], p["N"], 2000, seed=1)
-    ref, g, u, ga, ua = oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"],
-                                              p["qweight_up"], p["scales_up"], p["zeros_up"], p["M"],
-                                              p["N"], p["K"], p["group"], p["sym"], mi, ni)
+    if p["affine"]:
+        h = run_affine(p, gateup=True)
+        ref, g, u, ga, ua = oracle.gateup_silu_affine_at(p["x"], p["qweight"], p["scales"], p["biases"],
+                                                         p["qweight_up"], p["scales_up"], p["biases_up"], p["M"],
+                                                         p["N"], p["K"], p["group"], mi, ni)
+    else:
+        h = run_gateup(p)
+        ref, g, u, ga, ua = oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"],
+                                                  p["qweight_up"], p["scales_up"], p["zeros_up"], p["M"],
+                                                  p["N"], p["K"], p["group"], p["sym"], mi, ni)
     assert_within(h[mi, ni], ref, oracle.silu_bound(ref, g, u, ga, ua), name)
     assert np.isfinite(bf16_f64(h)).all()

@@ -167,7 +167,10 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 
 // tm_z: the zero blocks (zero-point form) or the bias operand (affine form);
 // tm_xs: the x group sums, in bf16 parts (affine form)
-template <int QF, bool GATEUP, int BXT>
+// SPLIT: clusters of p.kc pairs that split one tile's K (a separate
+// instantiation, so that the persistent form keeps its loop bounds and pair
+// constants out of the registers of the single MMA- and TMA-issuing threads)
+template <int QF, bool GATEUP, int BXT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prompt_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
@@ -186,17 +189,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // persistent and walk the tiles; with kc > 1 a cluster owns one tile and
   // pair j takes part j of its K range (whole blocks of four groups).
   const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;    // 0: even CTA of the pair (issues the MMAs), 1: odd
-  const uint32_t pbase = crank & ~1u;  // the even CTA's rank in the cluster
-  const int kpart = (int)(crank >> 1);
-  const uint16_t pair_mask = (uint16_t)(3u << pbase);
+  const uint32_t rank = crank & 1u;                   // 0: even CTA of the pair (issues the MMAs), 1: odd
+  const uint32_t pbase = SPLIT ? crank & ~1u : 0u;    // the even CTA's rank in the cluster
+  const int kpart = SPLIT ? (int)(crank >> 1) : 0;
+  const uint16_t pair_mask = SPLIT ? (uint16_t)(3u << pbase) : (uint16_t)3u;
   const uint32_t peer_abort = mapa_shared(smem_u32(smem + G::OFF_MISC + 4), crank ^ 1u);
   const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
   const int ntot = p.mtiles * p.ntiles;
-  const int g0 = 4 * (int)((long long)p.gblk * kpart / p.kc);
-  const int g1 = min(4 * (int)((long long)p.gblk * (kpart + 1) / p.kc), p.ng);  // this pair's groups [g0, g1)
-  const int kb0 = g0 * p.spg, kb1 = g1 * p.spg;                                  // and 64-wide stages
-  const bool bias_group = AFF && kpart == 0;  // affine: the closing bias group, once per tile
+  const int g0 = SPLIT ? 4 * (int)((long long)p.gblk * kpart / p.kc) : 0;
+  const int g1 = SPLIT ? min(4 * (int)((long long)p.gblk * (kpart + 1) / p.kc), p.ng) : p.ng;  // groups [g0, g1)
+  const int kb0 = SPLIT ? g0 * p.spg : 0, kb1 = SPLIT ? g1 * p.spg : p.nk;                       // and stages
+  const bool bias_group = AFF && (!SPLIT || kpart == 0);  // affine: the closing bias group, once per tile
 
   if (tid == 0) {
     for (int i = 0; i < SL; ++i) {
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gc;
       }
       if (!ok) break;
-      if (p.kc > 1) {
+      if (SPLIT) {
         // split K: the partial sums go to the (now idle) ring, [column][row]
         // float32, for the cluster's first pair to add up
         float *part = reinterpret_cast<float *>(smem + G::OFF_X);
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc2(tmem_base, G::kTmemCols);
   }
-  if (p.kc > 1) {
+  if (SPLIT) {
     // split K: the first pair adds the other pairs' partial sums (same parity
     // CTA, ranks 2j + rank), in pair order, and stores the tile
     if (kpart == 0 && !*abort_flag) {
@@ -583,12 +586,12 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 // Launch as clusters of two CTAs: one pair per tile, as many pairs as fit at
 // once (found once per instantiation and device), each walking the tiles with
 // a stride; or, split K (p.kc > 1), one cluster of p.kc pairs per tile.
-template <int QF, bool GATEUP, int BXT>
+template <int QF, bool GATEUP, int BXT, bool SPLIT>
 cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts,
                            const CUtensorMap &tz, const CUtensorMap &txs, const PromptParams &p, int ntot,
                            int device, cudaStream_t s) {
   using G = XGeo<BXT, QF>;
-  auto kern = prompt_tc_kernel<QF, GATEUP, BXT>;
+  auto kern = prompt_tc_kernel<QF, GATEUP, BXT, SPLIT>;
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = G::SMEM_ALLOC;
@@ -624,7 +627,8 @@ cudaError_t launch_variant(const CUtensorMap &tx, const CUtensorMap &tq, const C
 template <int QF, bool GATEUP, int BXT>
 cudaError_t launch_form(const CUtensorMap &tx, const CUtensorMap &tq, const CUtensorMap &ts, const CUtensorMap &tz,
                         const CUtensorMap &txs, const PromptParams &p, int ntot, const GemmCall &c) {
-  return launch_variant<QF, GATEUP, BXT>(tx, tq, ts, tz, txs, p, ntot, c.device, c.stream);
+  if (p.kc > 1) return launch_variant<QF, GATEUP, BXT, true>(tx, tq, ts, tz, txs, p, ntot, c.device, c.stream);
+  return launch_variant<QF, GATEUP, BXT, false>(tx, tq, ts, tz, txs, p, ntot, c.device, c.stream);
 }
 
 template <int BXT>

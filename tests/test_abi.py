@@ -148,3 +148,24 @@ def test_affine_layout_and_argument_checks(L):
     assert L.w4a16_gateup_silu_affine(P(FAKE), None, P(FAKE), 300, 64, 128, 64, P(FAKE), None) == INVALID
     assert L.w4a16_xsum(P(FAKE), 4, 128, 64, None, None) == INVALID
     assert L.w4a16_xsum(P(FAKE), 4, 128, 64, P(FAKE + 8), None) == MISALIGNED
+
+
+def test_noalloc_entry_point_argument_checks(L):
+    # the no-alloc affine GEMM keeps its group sums in a fixed 4 MiB device
+    # array: at K = 5120, group 64 a row of sums is 256 bf16 (512 B), so
+    # M = 8192 fills it exactly and M = 8193 is refused before any CUDA call
+    P = ctypes.c_void_p
+    na = L.w4a16_gemm_affine_noalloc
+    assert w4.xsum_bytes(8192, 5120, 64) == 4 << 20
+    assert w4.xsum_bytes(8193, 5120, 64) > 4 << 20
+    assert na(P(FAKE), P(FAKE), 8193, 64, 5120, 64, P(FAKE), None) == INVALID
+    assert na(P(FAKE), P(FAKE), 16385, 64, 5120, 128, P(FAKE), None) == INVALID
+    assert na(None, P(FAKE), 4, 64, 128, 64, P(FAKE), None) == INVALID
+    assert na(P(FAKE), None, 4, 64, 128, 64, P(FAKE), None) == INVALID
+    assert na(P(FAKE), P(FAKE), 4, 64, 128, 64, None, None) == INVALID
+    assert na(P(FAKE), P(FAKE), 0, 64, 128, 64, P(FAKE), None) == INVALID
+    assert na(P(FAKE), P(FAKE), 4, 64, 96, 64, P(FAKE), None) == INVALID     # K % G
+    assert na(P(FAKE), P(FAKE), 4, 64, 128, 32, P(FAKE), None) == INVALID    # group
+    assert na(P(FAKE + 8), P(FAKE), 4, 64, 128, 64, P(FAKE), None) == MISALIGNED
+    assert na(P(FAKE), P(FAKE + 128), 4, 64, 128, 64, P(FAKE), None) == MISALIGNED
+    assert na(P(FAKE), P(FAKE), 40, 64, 128, 64, P(FAKE + 2), None) == MISALIGNED

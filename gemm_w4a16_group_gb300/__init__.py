@@ -19,6 +19,7 @@ Affine form w = scale * q + bias (MLX affine 4-bit checkpoints):
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 
 from . import build as _build
@@ -132,28 +133,79 @@ def _torch():
     return torch
 
 
-def _stream(stream):
+@functools.lru_cache(maxsize=1)
+def _device_count() -> int:
+    return _torch().cuda.device_count()
+
+
+def _stream(stream, device=None):
+    """The call's stream handle. The library launches on the current CUDA
+    device, so the call's tensors (on `device`) must live there; with one
+    visible device they always do."""
     torch = _torch()
+    if device is not None and _device_count() > 1 and device.index != torch.cuda.current_device():
+        raise ValueError(f"the tensors are on {device} but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}: the library launches on the current device")
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _ptr(t, dtypes, name):
+def _is_device_tensor(t) -> bool:
+    return t.is_cuda
+
+
+def _ptr(t, dtypes, name, nbytes=0, device=None):
+    """Data pointer of `t` after the checks a plain C pointer cannot carry:
+    dtype, residency on the call's device, contiguity, and room for the
+    `nbytes` bytes the call reads or writes through it."""
     if t is None:
         return None
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
-    if not t.is_cuda:
+    if not _is_device_tensor(t):
         raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the call's other tensors on {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if t.nbytes < nbytes:
+        raise ValueError(f"{name} holds {t.nbytes} bytes, the call needs {nbytes}")
     return ctypes.c_void_p(t.data_ptr())
 
 
+_BF16 = None
+
+
 def _bf16_types():
-    torch = _torch()
-    return (torch.bfloat16, torch.int16, torch.uint16)
+    global _BF16
+    if _BF16 is None:
+        torch = _torch()
+        _BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+    return _BF16
+
+
+@functools.lru_cache(maxsize=1024)
+def _packed_bytes(N: int, K: int, group: int, form: int, gateup: bool) -> int:
+    L = lib()
+    f = L.w4a16_gateup_repacked_bytes if gateup else L.w4a16_repacked_bytes
+    return int(f(N, K, group, form))
+
+
+def _canonical_bytes(N: int, K: int, group: int):
+    """Bytes of a canonical weight's qweight (int32 [N, K/8]), scales or
+    biases (bf16 [N, K/G]) and zeros (int32 [N, ceil(K/G/8)])."""
+    groups = K // group if group > 0 else 0
+    return N * K // 2, N * groups * 2, N * ((groups + 7) // 8) * 4
+
+
+def _x_rows(x, K) -> int:
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M, k = x.shape
+    if k != K:
+        raise ValueError("x must be [M, K]")
+    return M
 
 
 def repacked_bytes(N: int, K: int, group: int, sym: bool) -> int:
@@ -170,11 +222,14 @@ def repack(qweight, scales, zeros, N, K, group, sym, stream=None, out=None):
     nbytes = repacked_bytes(N, K, group, sym)
     if nbytes == 0:
         raise W4A16Error("repack: unsupported sizes")
+    d = qweight.device
     if out is None:
-        out = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
-    rc = lib().w4a16_repack(_ptr(qweight, (torch.int32,), "qweight"), _ptr(scales, _bf16_types(), "scales"),
-                            _ptr(zeros, (torch.int32,), "zeros"), N, K, group, int(sym),
-                            ctypes.c_void_p(out.data_ptr()), _stream(stream))
+        out = torch.empty(nbytes, dtype=torch.uint8, device=d)
+    bq, bs, bz = _canonical_bytes(N, K, group)
+    rc = lib().w4a16_repack(_ptr(qweight, (torch.int32,), "qweight", bq, d),
+                            _ptr(scales, _bf16_types(), "scales", bs, d),
+                            _ptr(zeros, (torch.int32,), "zeros", bz, d), N, K, group, int(sym),
+                            _ptr(out, (torch.uint8,), "out", nbytes, d), _stream(stream, d))
     _check(rc, "w4a16_repack")
     return out
 
@@ -184,12 +239,14 @@ def repack_gateup(qw_gate, sc_gate, z_gate, qw_up, sc_up, z_up, N_each, K, group
     nbytes = gateup_repacked_bytes(N_each, K, group, sym)
     if nbytes == 0:
         raise W4A16Error("repack_gateup: unsupported sizes")
-    out = torch.empty(nbytes, dtype=torch.uint8, device=qw_gate.device)
+    d = qw_gate.device
+    out = torch.empty(nbytes, dtype=torch.uint8, device=d)
     i32, b16 = (torch.int32,), _bf16_types()
-    rc = lib().w4a16_repack_gateup(_ptr(qw_gate, i32, "qw_gate"), _ptr(sc_gate, b16, "sc_gate"),
-                                   _ptr(z_gate, i32, "z_gate"), _ptr(qw_up, i32, "qw_up"),
-                                   _ptr(sc_up, b16, "sc_up"), _ptr(z_up, i32, "z_up"), N_each, K, group,
-                                   int(sym), ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    bq, bs, bz = _canonical_bytes(N_each, K, group)
+    rc = lib().w4a16_repack_gateup(_ptr(qw_gate, i32, "qw_gate", bq, d), _ptr(sc_gate, b16, "sc_gate", bs, d),
+                                   _ptr(z_gate, i32, "z_gate", bz, d), _ptr(qw_up, i32, "qw_up", bq, d),
+                                   _ptr(sc_up, b16, "sc_up", bs, d), _ptr(z_up, i32, "z_up", bz, d), N_each, K,
+                                   group, int(sym), ctypes.c_void_p(out.data_ptr()), _stream(stream, d))
     _check(rc, "w4a16_repack_gateup")
     return out
 
@@ -197,13 +254,14 @@ def repack_gateup(qw_gate, sc_gate, z_gate, qw_up, sc_up, z_up, N_each, K, group
 def gemm(x, packed, N, K, group, sym, out=None, stream=None):
     """y[M, N] (bf16) = x[M, K] (bf16) . dequant(W)^T."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
+    d = x.device
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    rc = lib().w4a16_gemm(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), None, None,
-                          M, N, K, group, int(sym), _ptr(out, _bf16_types(), "out"), _stream(stream))
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_gemm(_ptr(x, _bf16_types(), "x", 0, d),
+                          _ptr(packed, (torch.uint8,), "packed", _packed_bytes(N, K, group, int(sym), False), d),
+                          None, None, M, N, K, group, int(sym), _ptr(out, _bf16_types(), "out", 2 * M * N, d),
+                          _stream(stream, d))
     _check(rc, "w4a16_gemm")
     return out
 
@@ -214,15 +272,16 @@ def gemm_argmax(x, packed, N, K, group, sym, out=None, logits=False, stream=None
     logits are stored only when `logits` is true or `out` is given; returns
     (argmax, y or None)."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
+    d = x.device
     if out is None and (logits or M > 32):
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    idx = index_out if index_out is not None else torch.empty(M, dtype=torch.int64, device=x.device)
-    rc = lib().w4a16_gemm_argmax(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), M, N, K,
-                                 group, int(sym), _ptr(out, _bf16_types(), "out"),
-                                 ctypes.c_void_p(idx.data_ptr()), _stream(stream))
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    idx = index_out if index_out is not None else torch.empty(M, dtype=torch.int64, device=d)
+    rc = lib().w4a16_gemm_argmax(_ptr(x, _bf16_types(), "x", 0, d),
+                                 _ptr(packed, (torch.uint8,), "packed", _packed_bytes(N, K, group, int(sym), False),
+                                      d),
+                                 M, N, K, group, int(sym), _ptr(out, _bf16_types(), "out", 2 * M * N, d),
+                                 _ptr(idx, (torch.int64,), "index_out", 8 * M, d), _stream(stream, d))
     _check(rc, "w4a16_gemm_argmax")
     return idx, out
 
@@ -230,14 +289,15 @@ def gemm_argmax(x, packed, N, K, group, sym, out=None, logits=False, stream=None
 def gateup_silu(x, packed_gateup, N_each, K, group, sym, out=None, stream=None):
     """h[M, N_each] (bf16) = SiLU(x Wg^T) * (x Wu^T)."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
+    d = x.device
     if out is None:
-        out = torch.empty((M, N_each), dtype=torch.bfloat16, device=x.device)
-    rc = lib().w4a16_gateup_silu(_ptr(x, _bf16_types(), "x"), _ptr(packed_gateup, (torch.uint8,), "packed"),
-                                 M, N_each, K, group, int(sym), _ptr(out, _bf16_types(), "out"),
-                                 _stream(stream))
+        out = torch.empty((M, N_each), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_gateup_silu(_ptr(x, _bf16_types(), "x", 0, d),
+                                 _ptr(packed_gateup, (torch.uint8,), "packed",
+                                      _packed_bytes(N_each, K, group, int(sym), True), d),
+                                 M, N_each, K, group, int(sym), _ptr(out, _bf16_types(), "out", 2 * M * N_each, d),
+                                 _stream(stream, d))
     _check(rc, "w4a16_gateup_silu")
     return out
 
@@ -248,11 +308,13 @@ def repack_affine(qweight, scales, biases, N, K, group, stream=None):
     nbytes = repacked_bytes(N, K, group, AFFINE)
     if nbytes == 0:
         raise W4A16Error("repack_affine: unsupported sizes")
-    out = torch.empty(nbytes, dtype=torch.uint8, device=qweight.device)
+    d = qweight.device
+    out = torch.empty(nbytes, dtype=torch.uint8, device=d)
     b16 = _bf16_types()
-    rc = lib().w4a16_repack_affine(_ptr(qweight, (torch.int32,), "qweight"), _ptr(scales, b16, "scales"),
-                                   _ptr(biases, b16, "biases"), N, K, group, ctypes.c_void_p(out.data_ptr()),
-                                   _stream(stream))
+    bq, bs, _ = _canonical_bytes(N, K, group)
+    rc = lib().w4a16_repack_affine(_ptr(qweight, (torch.int32,), "qweight", bq, d),
+                                   _ptr(scales, b16, "scales", bs, d), _ptr(biases, b16, "biases", bs, d), N, K,
+                                   group, ctypes.c_void_p(out.data_ptr()), _stream(stream, d))
     _check(rc, "w4a16_repack_affine")
     return out
 
@@ -262,12 +324,14 @@ def repack_affine_gateup(qw_gate, sc_gate, b_gate, qw_up, sc_up, b_up, N_each, K
     nbytes = gateup_repacked_bytes(N_each, K, group, AFFINE)
     if nbytes == 0:
         raise W4A16Error("repack_affine_gateup: unsupported sizes")
-    out = torch.empty(nbytes, dtype=torch.uint8, device=qw_gate.device)
+    d = qw_gate.device
+    out = torch.empty(nbytes, dtype=torch.uint8, device=d)
     i32, b16 = (torch.int32,), _bf16_types()
-    rc = lib().w4a16_repack_affine_gateup(_ptr(qw_gate, i32, "qw_gate"), _ptr(sc_gate, b16, "sc_gate"),
-                                          _ptr(b_gate, b16, "b_gate"), _ptr(qw_up, i32, "qw_up"),
-                                          _ptr(sc_up, b16, "sc_up"), _ptr(b_up, b16, "b_up"), N_each, K, group,
-                                          ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    bq, bs, _ = _canonical_bytes(N_each, K, group)
+    rc = lib().w4a16_repack_affine_gateup(_ptr(qw_gate, i32, "qw_gate", bq, d), _ptr(sc_gate, b16, "sc_gate", bs, d),
+                                          _ptr(b_gate, b16, "b_gate", bs, d), _ptr(qw_up, i32, "qw_up", bq, d),
+                                          _ptr(sc_up, b16, "sc_up", bs, d), _ptr(b_up, b16, "b_up", bs, d), N_each,
+                                          K, group, ctypes.c_void_p(out.data_ptr()), _stream(stream, d))
     _check(rc, "w4a16_repack_affine_gateup")
     return out
 
@@ -280,37 +344,36 @@ def xsum(x, K, group, out=None, stream=None):
     """bf16 [M, kb3]: the sum of x[m] over each group g as three bf16 parts
     (hi, mid, lo at columns 3g .. 3g+2) that add up to the float32 sum exactly."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
     nbytes = xsum_bytes(M, K, group)
     if nbytes == 0:
         raise W4A16Error("xsum: unsupported sizes")
+    d = x.device
     if out is None:
-        out = torch.empty((M, nbytes // 2 // M), dtype=torch.bfloat16, device=x.device)
-    elif out.numel() * out.element_size() < nbytes:
-        raise ValueError(f"xsum: out holds {out.numel() * out.element_size()} bytes, needs {nbytes}")
-    rc = lib().w4a16_xsum(_ptr(x, _bf16_types(), "x"), M, K, group, _ptr(out, _bf16_types(), "out"),
-                          _stream(stream))
+        out = torch.empty((M, nbytes // 2 // M), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_xsum(_ptr(x, _bf16_types(), "x", 0, d), M, K, group,
+                          _ptr(out, _bf16_types(), "out", nbytes, d), _stream(stream, d))
     _check(rc, "w4a16_xsum")
     return out
 
 
-def _xs_ptr(xs):
-    return _ptr(xs, _bf16_types(), "xsum")
+def _xs_ptr(xs, M, K, group, d):
+    # the table is read only by the tcgen05 GEMM (M > 32), but whenever one is
+    # passed it must be whole
+    return None if xs is None else _ptr(xs, _bf16_types(), "xsum", xsum_bytes(M, K, group), d)
 
 
 def gemm_affine(x, packed, N, K, group, xs=None, out=None, stream=None):
     """y[M, N] (bf16) = x . (scale * q + bias)^T. `xs` (from xsum) is needed
     for M > 32; None lets the M <= 32 kernels form the group sums themselves."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
+    d = x.device
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    rc = lib().w4a16_gemm_affine(_ptr(x, _bf16_types(), "x"), _xs_ptr(xs), _ptr(packed, (torch.uint8,), "packed"),
-                                 M, N, K, group, _ptr(out, _bf16_types(), "out"), _stream(stream))
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_gemm_affine(_ptr(x, _bf16_types(), "x", 0, d), _xs_ptr(xs, M, K, group, d),
+                                 _ptr(packed, (torch.uint8,), "packed", _packed_bytes(N, K, group, AFFINE, False), d),
+                                 M, N, K, group, _ptr(out, _bf16_types(), "out", 2 * M * N, d), _stream(stream, d))
     _check(rc, "w4a16_gemm_affine")
     return out
 
@@ -319,13 +382,15 @@ def gemm_affine_noalloc(x, packed, N, K, group, out=None, stream=None):
     """gemm_affine with the group sums in the library's fixed device array (no
     table argument; calls in flight at once on one device race on it)."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
+    d = x.device
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    rc = lib().w4a16_gemm_affine_noalloc(_ptr(x, _bf16_types(), "x"), _ptr(packed, (torch.uint8,), "packed"), M, N,
-                                         K, group, _ptr(out, _bf16_types(), "out"), _stream(stream))
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_gemm_affine_noalloc(_ptr(x, _bf16_types(), "x", 0, d),
+                                         _ptr(packed, (torch.uint8,), "packed",
+                                              _packed_bytes(N, K, group, AFFINE, False), d),
+                                         M, N, K, group, _ptr(out, _bf16_types(), "out", 2 * M * N, d),
+                                         _stream(stream, d))
     _check(rc, "w4a16_gemm_affine_noalloc")
     return out
 
@@ -333,14 +398,15 @@ def gemm_affine_noalloc(x, packed, N, K, group, out=None, stream=None):
 def gateup_silu_affine(x, packed_gateup, N_each, K, group, xs=None, out=None, stream=None):
     """h[M, N_each] (bf16) = SiLU(x Wg^T) * (x Wu^T), affine weights."""
     torch = _torch()
-    M = x.shape[0]
-    if x.dim() != 2 or x.shape[1] != K:
-        raise ValueError("x must be [M, K]")
+    M = _x_rows(x, K)
+    d = x.device
     if out is None:
-        out = torch.empty((M, N_each), dtype=torch.bfloat16, device=x.device)
-    rc = lib().w4a16_gateup_silu_affine(_ptr(x, _bf16_types(), "x"), _xs_ptr(xs),
-                                        _ptr(packed_gateup, (torch.uint8,), "packed"), M, N_each, K, group,
-                                        _ptr(out, _bf16_types(), "out"), _stream(stream))
+        out = torch.empty((M, N_each), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_gateup_silu_affine(_ptr(x, _bf16_types(), "x", 0, d), _xs_ptr(xs, M, K, group, d),
+                                        _ptr(packed_gateup, (torch.uint8,), "packed",
+                                             _packed_bytes(N_each, K, group, AFFINE, True), d),
+                                        M, N_each, K, group, _ptr(out, _bf16_types(), "out", 2 * M * N_each, d),
+                                        _stream(stream, d))
     _check(rc, "w4a16_gateup_silu_affine")
     return out
 
@@ -349,9 +415,11 @@ def dequantize(packed, N, K, group, sym, stream=None):
     """float32 [N, K] = (q - z) * scale (exact), or scale * q + bias rounded once
     to float32 for sym = AFFINE, read back through the kernels' unpack."""
     torch = _torch()
-    out = torch.empty((N, K), dtype=torch.float32, device=packed.device)
-    rc = lib().w4a16_dequantize(_ptr(packed, (torch.uint8,), "packed"), N, K, group, int(sym),
-                                ctypes.c_void_p(out.data_ptr()), _stream(stream))
+    d = packed.device
+    need = _packed_bytes(N, K, group, int(sym), False)
+    p = _ptr(packed, (torch.uint8,), "packed", need, d)
+    out = torch.empty((N, K), dtype=torch.float32, device=d)
+    rc = lib().w4a16_dequantize(p, N, K, group, int(sym), ctypes.c_void_p(out.data_ptr()), _stream(stream, d))
     _check(rc, "w4a16_dequantize")
     return out
 

@@ -87,10 +87,14 @@ def _brute(codes, zeros_mat, scales, x, G):
     return y, a
 
 
+# (False, 8, 2, 3, 80) and (False, 16, 1, 5, 272): 10 and 17 groups per row,
+# so each row's zero points span two and three int32 words, the last one part
+# used (a wrong word stride or nibble index shows up only past 8 groups)
 @pytest.mark.parametrize("sym,G,M,N,K", [(True, 8, 3, 5, 32), (False, 8, 2, 4, 64),
-                                         (False, 16, 3, 3, 48), (True, 64, 1, 2, 128)])
-def test_bruteforce_exact(sym, G, M, N, K):
-    seed = 11 + K + N
+                                         (False, 16, 3, 3, 48), (True, 64, 1, 2, 128),
+                                         (False, 8, 2, 3, 80), (False, 16, 1, 5, 272)])
+def test_bruteforce_exact(sym, G, M, N, K, seed=None):
+    seed = 11 + K + N if seed is None else seed
     codes = synth.make_codes(N, K, seed, 2)
     Kg = K // G
     zmat = (np.full((N, Kg), 8, dtype=np.uint8) if sym
@@ -107,6 +111,21 @@ def test_bruteforce_exact(sym, G, M, N, K):
             err = abs(Fraction(y[m, n]) - ye[m][n])
             assert err <= gamma * ae[m][n], (m, n, float(err))
             assert abs(Fraction(a[m, n]) - ae[m][n]) <= gamma * ae[m][n]
+
+
+def test_bruteforce_random_shapes():
+    """The same exact comparison over random shapes (1-20 groups of 8 or 16,
+    so zero points in one to three int32 words per row), forms and seeds."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=120, deadline=None, derandomize=True)
+    @hyp.given(sym=st.booleans(), G=st.sampled_from([8, 16]), M=st.integers(1, 3), N=st.integers(2, 4),
+               Kg=st.integers(1, 20), seed=st.integers(0, 2**31 - 1))
+    def run(sym, G, M, N, Kg, seed):
+        test_bruteforce_exact(sym, G, M, N, G * Kg, seed=seed)
+
+    run()
 
 
 def test_bruteforce_detects_transposed_weight():

@@ -332,9 +332,9 @@ def _brute_affine(codes, scales, biases, x, G):
     return y, a
 
 
-@pytest.mark.parametrize("G,M,N,K", [(8, 3, 5, 32), (16, 2, 4, 64), (64, 1, 3, 128)])
-def test_affine_bruteforce_exact(G, M, N, K):
-    seed = 31 + K + N
+@pytest.mark.parametrize("G,M,N,K", [(8, 3, 5, 32), (16, 2, 4, 64), (64, 1, 3, 128), (8, 2, 3, 88)])
+def test_affine_bruteforce_exact(G, M, N, K, seed=None):
+    seed = 31 + K + N if seed is None else seed
     Kg = K // G
     codes = synth.make_codes(N, K, seed, 2)
     s = synth.make_scales(N, Kg, 0.005, 0.02, seed)
@@ -347,6 +347,21 @@ def test_affine_bruteforce_exact(G, M, N, K):
         for n in range(N):
             assert abs(Fraction(y[m, n]) - ye[m][n]) <= gamma * ae[m][n], (m, n)
             assert abs(Fraction(a[m, n]) - ae[m][n]) <= gamma * ae[m][n]
+
+
+def test_affine_bruteforce_random_shapes():
+    """The affine exact comparison over random shapes (1-20 groups of 8 or
+    16) and seeds."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=60, deadline=None, derandomize=True)
+    @hyp.given(G=st.sampled_from([8, 16]), M=st.integers(1, 3), N=st.integers(2, 4), Kg=st.integers(1, 20),
+               seed=st.integers(0, 2**31 - 1))
+    def run(G, M, N, Kg, seed):
+        test_affine_bruteforce_exact(G, M, N, G * Kg, seed=seed)
+
+    run()
 
 
 def test_affine_zero_codes_leave_bias_times_group_sums():

@@ -403,70 +403,103 @@ def run_cuda(args, rank, world):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # ---------------------------------------------------------------------------
-def cpu_baseline(workload, budget_s=10.0, steps=None):
-    """The float64 oracle as it stands, on every host core, over a bounded
-    sample of the workload; returns value in the workload's unit."""
-    import oracle
+def _oracle_problems(workload):
     parts = step_parts(workload)
-    probs = []
-    for name, w in parts:
-        probs.append((name, w, new_problem(w)))
-    is_flops = part_units(parts[0][1])[2]
-    units_done, t_total, reps, desc = 0.0, 0.0, 0, ""
-    while True:
-        for name, w, p in probs:
-            if w["kind"] == "gateup":
-                rows = min(16, w["M"])  # sample of M rows x every output column
-                mi = np.repeat(np.arange(rows), w["N"])
-                ni = np.tile(np.arange(w["N"]), rows)
-                t0 = time.perf_counter()
-                if p["affine"]:
-                    oracle.gateup_silu_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], p["qweight_up"],
-                                                 p["scales_up"], p["biases_up"], w["M"], w["N"], w["K"],
-                                                 w["group"], mi, ni)
-                else:
-                    oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["qweight_up"],
-                                          p["scales_up"], p["zeros_up"], w["M"], w["N"], w["K"], w["group"],
-                                          w["sym"], mi, ni)
-                t_total += time.perf_counter() - t0
-                units_done += (gemm_flops(rows, 2 * w["N"], w["K"]) if is_flops else
-                               gateup_bytes(rows, w["N"], w["K"], w["group"], w["sym"], p["affine"]))
-                desc = f"{rows} of {w['M']} rows x all {2 * w['N']} gate/up columns"
-            else:
-                rows = w["M"] if not is_flops else min(16, w["M"])  # M > 16: a sample of rows
-                t0 = time.perf_counter()
-                if p["affine"]:
-                    oracle.gemm_affine(p["x"][:rows], p["qweight"], p["scales"], p["biases"], rows, w["N"], w["K"],
-                                       w["group"])
-                else:
-                    oracle.gemm(p["x"][:rows], p["qweight"], p["scales"], p["zeros"], rows, w["N"], w["K"],
-                                w["group"], w["sym"])
-                t_total += time.perf_counter() - t0
-                units_done += (gemm_flops(rows, w["N"], w["K"]) if is_flops else
-                               algorithmic_bytes(w["M"], w["N"], w["K"], w["group"], w["sym"], p["affine"]))
-                desc = "whole step" if rows == w["M"] else f"{rows} of {w['M']} rows x all {w['N']} columns"
-        reps += 1
-        if (steps is not None and reps >= steps) or (steps is None and t_total >= budget_s):
-            break
+    return [(name, w, new_problem(w)) for name, w in parts], part_units(parts[0][1])[2]
+
+
+def _oracle_step(probs, is_flops, frac=1.0):
+    """One step of the float64 oracle over every part of the workload: M rows
+    (at most 16 for gate/up and where the unit is FLOP/s) by all output
+    columns, or with `frac` < 1 that share of the columns, evenly spaced,
+    through the oracle's sampled-output functions. Returns (seconds, units,
+    description)."""
+    import oracle
+    seconds, units, descs, whole = 0.0, 0.0, [], True
+    for name, w, p in probs:
+        gate = w["kind"] == "gateup"
+        M, N, K, G = w["M"], w["N"], w["K"], w["group"]
+        rows = min(16, M) if (gate or is_flops) else M
+        ncols = N if frac >= 1.0 else max(1, min(N, int(round(N * frac))))
+        cols = np.arange(N, dtype=np.int64) if ncols == N else (np.arange(ncols, dtype=np.int64) * N) // ncols
+        mi, ni = np.repeat(np.arange(rows, dtype=np.int64), ncols), np.tile(cols, rows)
+        t0 = time.perf_counter()
+        if gate and p["affine"]:
+            oracle.gateup_silu_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], p["qweight_up"],
+                                         p["scales_up"], p["biases_up"], M, N, K, G, mi, ni)
+        elif gate:
+            oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["qweight_up"], p["scales_up"],
+                                  p["zeros_up"], M, N, K, G, w["sym"], mi, ni)
+        elif ncols == N and p["affine"]:
+            oracle.gemm_affine(p["x"][:rows], p["qweight"], p["scales"], p["biases"], rows, N, K, G)
+        elif ncols == N:
+            oracle.gemm(p["x"][:rows], p["qweight"], p["scales"], p["zeros"], rows, N, K, G, w["sym"])
+        elif p["affine"]:
+            oracle.gemm_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, G, mi, ni)
+        else:
+            oracle.gemm_at(p["x"], p["qweight"], p["scales"], p["zeros"], M, N, K, G, w["sym"], mi, ni)
+        seconds += time.perf_counter() - t0
+        if is_flops:
+            units += gemm_flops(rows, (2 if gate else 1) * ncols, K)
+        elif gate:
+            units += gateup_bytes(rows, ncols, K, G, w["sym"], p["affine"])
+        else:
+            units += algorithmic_bytes(rows, ncols, K, G, w["sym"], p["affine"])
+        whole = whole and rows == M and ncols == N
+        what = "gate/up column pairs" if gate else "columns"
+        descs.append(f"{name}: {rows} of {M} rows x {ncols} of {N} {what}")
+    return seconds, units, "whole step" if whole else "; ".join(descs)
+
+
+def _oracle_result(units, seconds, reps, desc, is_flops):
+    import oracle
     scale = 1e-12 if is_flops else 1e-9
-    return {"value": units_done / t_total * scale, "unit": "TFLOP/s" if is_flops else "GB/s",
+    return {"value": units / seconds * scale, "unit": "TFLOP/s" if is_flops else "GB/s",
             "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{desc}, {reps} repetition(s), {t_total:.1f} s", "seconds": t_total, "reps": reps}
+            "sample": f"{desc}, {reps} repetition(s), {seconds:.1f} s", "seconds": seconds, "reps": reps}
 
 
-def run_reference(args, rank):
+def cpu_baseline(workload, budget_s=10.0):
+    """The float64 oracle as it stands, on every host core, over whole steps
+    of the workload's bounded sample until `budget_s` seconds of oracle work;
+    returns value in the workload's unit."""
+    probs, is_flops = _oracle_problems(workload)
+    seconds, units, reps = 0.0, 0.0, 0
+    while True:  # at least one step
+        s, u, desc = _oracle_step(probs, is_flops)
+        seconds, units, reps = seconds + s, units + u, reps + 1
+        if seconds >= budget_s:
+            return _oracle_result(units, seconds, reps, desc, is_flops)
+
+
+REFERENCE_BUDGET_S = 120.0  # the reference arm's warm-up and timed steps together
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle on rank 0's host cores (the other ranks
+    do no work), exactly --warmup untimed and --steps timed steps. When that
+    many whole steps of the bounded sample would take more than two minutes,
+    every step samples the same smaller share of the output columns."""
     if rank != 0:
         return None
+    probs, is_flops = _oracle_problems(args.workload)
+    probe, _, _ = _oracle_step(probs, is_flops)
+    est = (args.warmup + args.steps) * probe
+    frac = 1.0 if est <= REFERENCE_BUDGET_S else REFERENCE_BUDGET_S / est
     for _ in range(args.warmup):
-        cpu_baseline(args.workload, steps=1)
-    cb = cpu_baseline(args.workload, steps=max(1, args.steps if args.steps <= 20 else 20))
-    return {"impl": "reference", "metric": metric_name(args.workload), "value": round(cb["value"], 4),
-            "unit": cb["unit"], "n_gpus": 1, "steps": cb["reps"], "warmup": args.warmup,
-            "ms_per_step": cb["seconds"] * 1e3 / cb["reps"], "higher_is_better": True, "scaling": "weak",
+        _oracle_step(probs, is_flops, frac)
+    seconds, units, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        s, u, desc = _oracle_step(probs, is_flops, frac)
+        seconds, units = seconds + s, units + u
+    cb = _oracle_result(units, seconds, args.steps, desc, is_flops)
+    return {"impl": "reference", "metric": metric_name(args.workload), "value": cb["value"],
+            "unit": cb["unit"], "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": cb["seconds"] * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload},
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
-            "e2e": {"value": round(cb["value"], 4), "unit": cb["unit"], "h2d_bytes_per_step": 0,
+            "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
@@ -494,11 +527,13 @@ def main():
         print(kernel_source_hash())
         return
     args.warmup = max(3, args.warmup)
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
-        line = run_reference(args, rank)
+        line = run_reference(args, rank, world)
     else:
         if world > 1:
             import torch

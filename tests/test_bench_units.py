@@ -58,3 +58,36 @@ def test_metric_names():
     assert bench.metric_name("decode_ffn_m1") == "W4A16 GEMM eff. HBM GB/s (M=1..16)"
     assert bench.metric_name("prompt_gateup_m4096_k5120_n17408").startswith("W4A16 fused gate/up GEMM TFLOP/s")
     assert bench.metric_name("chunk_m256_k17408_n5120") == "W4A16 GEMM TFLOP/s (M>32)"
+
+
+def test_oracle_step_whole_and_sampled_columns():
+    probs, is_flops = bench._oracle_problems("tiny_gemv_m1_k512_n256")
+    assert not is_flops
+    s, units, desc = bench._oracle_step(probs, is_flops)
+    assert s > 0 and desc == "whole step"
+    assert units == workloads.algorithmic_bytes(1, 256, 512, 128, True)
+    # a quarter of the columns, evenly spaced, through the sampled-output path
+    s, units, desc = bench._oracle_step(probs, is_flops, frac=0.25)
+    assert units == workloads.algorithmic_bytes(1, 64, 512, 128, True)
+    assert "64 of 256 columns" in desc
+    # the FLOP unit counts 2 * rows * columns * K of the sample
+    probs, is_flops = bench._oracle_problems("shape:40,64,128,64,affine")
+    assert is_flops
+    _, units, desc = bench._oracle_step(probs, is_flops, frac=0.5)
+    assert units == 2 * 16 * 32 * 128 and "16 of 40 rows x 32 of 64 columns" in desc
+
+
+def test_reference_line_echoes_the_launch():
+    import argparse
+    args = argparse.Namespace(workload="tiny_gemv_m1_k512_n256", steps=2, warmup=3)
+    assert bench.run_reference(args, 1, 2) is None  # only rank 0 works and prints
+    line = bench.run_reference(args, 0, 2)
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["steps"] == 2 and line["warmup"] == 3
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["sample"].startswith("whole step, 2 repetition(s)")
+
+
+def test_cpu_baseline_runs_at_least_one_step():
+    cb = bench.cpu_baseline("tiny_gemv_m1_k512_n256", budget_s=0.0)
+    assert cb["reps"] == 1 and cb["value"] > 0 and cb["kind"] == "oracle"

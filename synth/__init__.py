@@ -26,6 +26,7 @@ __all__ = [
     "splitmix64_stream", "uniform01", "normal01", "f32_to_bf16_bits",
     "bf16_bits_to_f32", "pack_nibbles_rows", "make_codes", "make_qweight",
     "make_scales", "make_zeros", "make_biases", "make_x", "make_problem", "TENSOR_IDS",
+    "SCALE_SWEEP", "exhaustive_problem", "planted_max_problem",
 ]
 
 def _signed(c: int) -> np.int64:
@@ -40,7 +41,7 @@ _M2 = _signed(0x94D049BB133111EB)
 
 # stream id of every tensor a problem draws
 TENSOR_IDS = {"x": 1, "qweight": 2, "scales": 3, "zeros": 4,
-              "qweight_up": 5, "scales_up": 6, "zeros_up": 7, "biases": 8, "biases_up": 9}
+              "qweight_up": 5, "scales_up": 6, "zeros_up": 7, "biases": 8, "biases_up": 9, "x_signs": 10}
 
 
 _BLOCK = 1 << 20  # draws per in-place block (reused buffers keep page faults down)
@@ -220,4 +221,50 @@ def make_problem(M: int, N: int, K: int, group: int, sym: bool,
         p["zeros_up"] = None if (sym or affine) else make_zeros(N, Kg, seed, TENSOR_IDS["zeros_up"])
         if affine:
             p["biases_up"] = make_biases(N, Kg, bias_range[0], bias_range[1], seed, TENSOR_IDS["biases_up"])
+    return p
+
+
+# Scales of the exhaustive weight: normal float32 values that bf16 holds
+# exactly, from 2^-100 to 2^100, both signs; times any q - z (|q - z| <= 15)
+# each stays a normal float32.
+SCALE_SWEEP = (2.0 ** -100, 2.0 ** -40, 2.0 ** -20, 2.0 ** -7, 5 / 1024, 3 / 256, 0.5, 1.0,
+               1.5, 201 / 64, -0.25, -3.0, 7.75, 2.0 ** 10, 2.0 ** 40, 2.0 ** 100)
+
+
+def exhaustive_problem(sym: bool, N: int = 256, group: int = 64) -> dict:
+    """A weight in which every (code, zero point) pair meets every scale of
+    SCALE_SWEEP (with N = 256): K = 16 groups; row r holds code
+    (r + k + r // 16) % 16 at column k, zero point (r + g) % 16 in group g (8
+    for the symmetric form) and scale SCALE_SWEEP[(r // 16 + g) % 16].
+    Besides the problem's arrays it returns the codes, zero points and scale
+    bits it packed ("codes", "zero_points", "scale_bits")."""
+    K = 16 * group
+    r = np.arange(N)[:, None]
+    g = np.arange(16)[None, :]
+    codes = ((r + np.arange(K)[None, :] + r // 16) % 16).astype(np.uint8)
+    zpts = np.full((N, 16), 8, dtype=np.uint8) if sym else ((r + g) % 16).astype(np.uint8)
+    sweep_bits = (np.array(SCALE_SWEEP, dtype=np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    scales = sweep_bits[(r // 16 + g) % 16]
+    return {"M": 1, "N": N, "K": K, "group": group, "sym": bool(sym), "seed": 0, "affine": False,
+            "x": make_x(1, K, 0), "qweight": pack_nibbles_rows(codes), "scales": scales,
+            "zeros": None if sym else pack_nibbles_rows(zpts),
+            "codes": codes, "zero_points": zpts, "scale_bits": scales}
+
+
+def planted_max_problem(M: int, N: int, K: int, group: int, planted, seed: int = 0,
+                        scale_range=(0.002, 0.01)) -> dict:
+    """A symmetric weight of uniform random codes and x rows of +1 and -1
+    (signs from their own stream), in which row planted[m] of the weight is
+    recoded to 15 where x[m] is +1 and to 0 where it is -1. Every product
+    x[m][k] * (q - 8) of that row is then +7 or +8 times a positive scale, so
+    row m's output is largest at column planted[m] by a wide margin."""
+    planted = [int(n) for n in planted]
+    assert len(planted) == M and len(set(planted)) == M
+    p = make_problem(M, N, K, group, True, scale_range=scale_range, seed=seed)
+    pos = (make_codes(M, K, seed, TENSOR_IDS["x_signs"]) & 1).astype(bool)
+    p["x"] = np.where(pos, np.uint16(0x3F80), np.uint16(0xBF80)).astype(np.uint16)
+    q = p["qweight"].copy()
+    for m, n in enumerate(planted):
+        q[n] = pack_nibbles_rows(np.where(pos[m], 15, 0)[None, :])[0]
+    p["qweight"], p["planted"], p["x_positive"] = q, planted, pos
     return p

@@ -35,6 +35,16 @@ def test_dequantize_bit_exact(sym, group, N, K):
     np.testing.assert_array_equal(w, ref)
 
 
+
+@pytest.mark.parametrize("sym", [False, True])
+def test_dequantize_every_code_zero_point_and_scale(sym):
+    """Every (code, zero point) pair against every scale of a sweep from
+    2^-100 to 2^100 (both signs), read back bit for bit."""
+    e = synth.exhaustive_problem(sym)
+    N, K, G = e["N"], e["K"], e["group"]
+    w = w4.dequantize(packed_of(e, upload(e)), N, K, G, sym).cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(w, oracle.dequant(e["qweight"], e["scales"], e["zeros"], N, K, G, sym))
+
 CASES = [
     # (kernel, M, N, K, group, sym)
     (GEMV, 1, 250, 512, 128, True),
@@ -267,3 +277,20 @@ def test_smallest_shapes(which, M, N, K, group, sym):
     """One output row and/or one 64-wide K chunk (a single group)."""
     p = synth.make_problem(M, N, K, group, sym, seed=95 + N + K)
     check_gemm_full(p, run_gemm(p, which))
+
+
+
+@pytest.mark.parametrize("M,N", [(1, 248320), (5, 248320), (40, 4096)])
+def test_argmax_finds_a_planted_maximum(M, N):
+    """On the output-vocabulary head shape, x rows of +1 and -1 and one weight
+    row per x row recoded to agree with it in sign: the greedy pick of every
+    row is its planted column (decode epilogue for M <= 32; stored logits and
+    the row argmax for M = 40)."""
+    K, G = 5120, 128
+    planted = [(7919 * (m + 1)) % N for m in range(M)]
+    p = synth.planted_max_problem(M, N, K, G, planted, seed=M)
+    d = upload(p)
+    idx, _ = w4.gemm_argmax(d["x"], packed_of(p, d), N, K, G, True)
+    torch().cuda.synchronize()
+    assert w4.kernel_status() == 0
+    assert idx.cpu().numpy().tolist() == planted

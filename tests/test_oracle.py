@@ -438,3 +438,38 @@ def test_group_sums_closed_forms():
         for g in range(K // G):
             exact = sum((_fr_bf16(x[m, k]) for k in range(g * G, (g + 1) * G)), Fraction(0))
             assert xs[g, m] == float(exact)  # at most 128 bf16 terms: exact in float64
+
+
+# --------------------------------------------------------------------------
+# every code, zero point and scale; a planted maximum
+
+@pytest.mark.parametrize("sym", [False, True])
+def test_dequant_every_code_zero_point_and_scale(sym):
+    """Every (code, zero point) pair meets every scale of a sweep from 2^-100
+    to 2^100, both signs, in every nibble position of a word (codes 8-15 in
+    the top nibble make the int32 word negative). The oracle's unpack of the
+    packed words must give back exactly the q - z the input was built from,
+    times the scale."""
+    e = synth.exhaustive_problem(sym)
+    N, K, G = e["N"], e["K"], e["group"]
+    w = oracle.dequant(e["qweight"], e["scales"], e["zeros"], N, K, G, sym)
+    s = synth.bf16_bits_to_f32(e["scale_bits"]).astype(np.float64)
+    qz = e["codes"].astype(np.float64) - np.repeat(e["zero_points"], G, axis=1).astype(np.float64)
+    np.testing.assert_array_equal(w, qz * np.repeat(s, G, axis=1))
+
+
+def test_planted_maximum_is_the_argmax():
+    """A weight row recoded to agree in sign with x row m (code 15 where x is
+    +1, 0 where it is -1; z = 8) gives x[m] . w = sum_g s_g (7 P_g + 8 (G - P_g))
+    with P_g the +1 entries of x[m] in group g: exact in float64 (every term
+    is a short dyadic rational of nearby exponents), and the row's maximum."""
+    M, N, K, G = 3, 300, 512, 128
+    planted = [17, 250, 299]
+    p = synth.planted_max_problem(M, N, K, G, planted, seed=3)
+    y, _ = oracle.gemm(p["x"], p["qweight"], p["scales"], None, M, N, K, G, True)
+    for m, n in enumerate(planted):
+        P = p["x_positive"][m].reshape(K // G, G).sum(axis=1)
+        exact = sum((_fr_bf16(p["scales"][n, g]) * (7 * int(P[g]) + 8 * (G - int(P[g]))) for g in range(K // G)),
+                    Fraction(0))
+        assert Fraction(y[m, n]) == exact
+        assert int(np.argmax(y[m])) == n

@@ -257,3 +257,28 @@ def silu_bound(h_ref, g, u, gsum_abs, usum_abs):
     bu = ACC_TOL * np.asarray(usum_abs)
     return (REL_TOL * np.abs(h_ref) + np.abs(dsilu) * np.abs(u) * bg
             + np.abs(g * s) * bu + bg * bu)
+
+
+def _bf16_rank(bits) -> np.ndarray:
+    """Order key of bf16 bit patterns, larger key = larger value: sign and
+    magnitude as a signed integer (so -0 and +0 share the key 0), and every
+    NaN one step above +inf."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    key = np.where(b & 0x8000, -mag, mag)
+    return np.where(mag > 0x7F80, 0x7F81, key)
+
+
+def topk_bf16(y_bits, k: int):
+    """The k largest entries of every row of a bf16 matrix (bits [M, N]), the
+    greedy pick of the GPU-side token selection (lucebox PR #823, description)
+    widened from 1 to k: largest value first; equal values (-0 and +0 among
+    them) lowest column first; a NaN ranks above +inf. Returns (indices int64
+    [M, k], value bits uint16 [M, k]). A stable sort of the negated key keeps
+    equal keys in column order."""
+    y = np.atleast_2d(np.asarray(y_bits, dtype=np.uint16))
+    M, N = y.shape
+    if not 1 <= k <= N:
+        raise ValueError("topk_bf16: need 1 <= k <= N")
+    order = np.argsort(-_bf16_rank(y), axis=1, kind="stable")[:, :k]
+    return order.astype(np.int64), np.take_along_axis(y, order, axis=1)

@@ -473,3 +473,77 @@ def test_planted_maximum_is_the_argmax():
                     Fraction(0))
         assert Fraction(y[m, n]) == exact
         assert int(np.argmax(y[m])) == n
+
+
+# --------------------------------------------------------------------------
+# top-k selection of a bf16 row
+
+TOPK_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "topk_worked_example.txt")
+
+
+def test_topk_golden_worked_example():
+    d = {}
+    with open(TOPK_GOLDEN) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            key, v = line.split(":", 1)
+            d[key.strip()] = v.split()
+    row = np.array([int(h, 16) for h in d["row"]], dtype=np.uint16)
+    for key in ("k1", "k3", "k6", "k8", "k10"):
+        k = int(key[1:])
+        idx, vals = oracle.topk_bf16(row, k)
+        assert idx[0].tolist() == [int(v) for v in d[key]], key
+        np.testing.assert_array_equal(vals[0], row[idx[0]])
+
+
+def _rank_by_comparison(vals):
+    """Column order by repeated pairwise comparison of Python floats: a
+    before b when a > b, or a NaN against a number, or equal (or both NaN)
+    and a's column is lower."""
+    import functools
+
+    def cmp(i, j):
+        a, b = vals[i], vals[j]
+        an, bn = math.isnan(a), math.isnan(b)
+        if an != bn:
+            return -1 if an else 1
+        if not an and a != b:
+            return -1 if a > b else 1
+        return -1 if i < j else (1 if i > j else 0)
+
+    return sorted(range(len(vals)), key=functools.cmp_to_key(cmp))
+
+
+def test_topk_against_pairwise_comparison():
+    """Random rows mixing normal values, repeats, +-0, +-inf and NaNs, every
+    k: the oracle's order equals a sort by pairwise float comparison."""
+    rng = np.random.default_rng(7)
+    specials = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0xFFC1, 0x3F80, 0xBF80], dtype=np.uint16)
+    for trial in range(60):
+        N = int(rng.integers(1, 40))
+        row = rng.integers(0, 1 << 16, N).astype(np.uint16)
+        mask = rng.random(N) < 0.35
+        row[mask] = rng.choice(specials, int(mask.sum()))
+        vals = [float(v) for v in synth.bf16_bits_to_f32(row)]
+        want = _rank_by_comparison(vals)
+        for k in range(1, N + 1):
+            idx, _ = oracle.topk_bf16(row, k)
+            assert idx[0].tolist() == want[:k], (trial, k)
+
+
+def test_topk_k1_is_the_first_maximum_and_k_n_a_permutation():
+    """k = 1 is numpy's argmax of the float values (first maximum, first NaN
+    if any); k = N orders every column exactly once."""
+    rng = np.random.default_rng(11)
+    y = rng.integers(0, 1 << 16, (50, 300)).astype(np.uint16)
+    y[:, rng.integers(0, 300, 20)] = 0x4040  # repeated values
+    f = synth.bf16_bits_to_f32(y)
+    idx, vals = oracle.topk_bf16(y, 1)
+    np.testing.assert_array_equal(idx[:, 0], np.argmax(f, axis=1))
+    full, _ = oracle.topk_bf16(y, 300)
+    assert all(sorted(r) == list(range(300)) for r in full.tolist())
+    with pytest.raises(ValueError):
+        oracle.topk_bf16(y, 0)
+    with pytest.raises(ValueError):
+        oracle.topk_bf16(y, 301)

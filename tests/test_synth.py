@@ -75,3 +75,40 @@ def test_qweight_words_are_draw_halves_and_blocking_is_invisible():
                                   synth.make_qweight(37, 128, 5))
     np.testing.assert_array_equal(synth.splitmix64_stream(9, 10, offset=5),
                                   synth.splitmix64_stream(9, 15)[5:])
+
+
+@pytest.mark.parametrize("sym", [False, True])
+def test_exhaustive_problem_meets_every_code_zero_point_and_scale(sym):
+    e = synth.exhaustive_problem(sym)
+    G = e["group"]
+    c = e["codes"].reshape(e["N"], 16, G)
+    seen = set()
+    for r in range(e["N"]):
+        for g in range(16):
+            z, s = int(e["zero_points"][r, g]), int(e["scale_bits"][r, g])
+            seen.update((int(q), z, s) for q in np.unique(c[r, g]))
+    assert len(seen) == (16 * 16 * 16 if not sym else 16 * 16)
+    # the packed words hold the codes and zero points, nibble j of word c = column 8c + j
+    np.testing.assert_array_equal(e["qweight"], synth.pack_nibbles_rows(e["codes"]))
+    if not sym:
+        np.testing.assert_array_equal(e["zeros"], synth.pack_nibbles_rows(e["zero_points"]))
+    # every scale of the sweep, exactly, and normal in float32 times any |q - z| <= 15
+    vals = set(synth.bf16_bits_to_f32(e["scale_bits"]).astype(np.float64).ravel().tolist())
+    assert vals == set(synth.SCALE_SWEEP)
+    tiny = np.float32(min(abs(v) for v in synth.SCALE_SWEEP))
+    assert tiny >= np.finfo(np.float32).tiny and 15 * max(abs(v) for v in synth.SCALE_SWEEP) < np.finfo(np.float32).max
+
+
+def test_planted_max_problem_recodes_the_planted_rows():
+    M, N, K, G = 3, 64, 256, 128
+    p = synth.planted_max_problem(M, N, K, G, [5, 40, 63], seed=2)
+    assert p["x"].dtype == np.uint16 and set(np.unique(p["x"]).tolist()) <= {0x3F80, 0xBF80}
+    base = synth.make_problem(M, N, K, G, True, scale_range=(0.002, 0.01), seed=2)
+    for m, n in enumerate([5, 40, 63]):
+        want = np.where(p["x"][m] == 0x3F80, 15, 0)
+        np.testing.assert_array_equal(p["qweight"][n], synth.pack_nibbles_rows(want[None, :])[0])
+    others = [r for r in range(N) if r not in (5, 40, 63)]
+    np.testing.assert_array_equal(p["qweight"][others], base["qweight"][others])
+    np.testing.assert_array_equal(p["scales"], base["scales"])
+    with pytest.raises(AssertionError):
+        synth.planted_max_problem(2, N, K, G, [7, 7])

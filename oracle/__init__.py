@@ -99,6 +99,12 @@ def lib() -> ctypes.CDLL:
             L.oracle_group_sums.restype = i32
             L.oracle_threads.argtypes = [i32]
             L.oracle_threads.restype = i32
+            L.oracle_code_bits.argtypes = [P, i32, i32, i32, i32]
+            L.oracle_code_bits.restype = i32
+            L.oracle_dequant_affine_bits.argtypes = [P, P, P, i32, i32, i32, i32, P]
+            L.oracle_dequant_affine_bits.restype = i32
+            L.oracle_gemm_affine_bits.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P, i32]
+            L.oracle_gemm_affine_bits.restype = i32
             _lib = L
     return _lib
 
@@ -227,6 +233,33 @@ def gateup_silu_affine_at(x, qg, sg, bg, qu, su, bu, M, N, K, group, m_idx, n_id
         raise ValueError("oracle_gateup_silu_affine_at: bad arguments")
     return tuple(outs)
 
+
+
+def code_bits(qweight, K, bits, n, k) -> int:
+    """Code k of row n of a bits-wide weight (uint32 [N, ceil(K*bits/32)], one
+    little-endian bit stream per row)."""
+    q = _c(qweight, np.uint32)
+    return lib().oracle_code_bits(_p(q), K, bits, n, k)
+
+
+def dequant_affine_bits(qweight, scales, biases, N, K, group, bits) -> np.ndarray:
+    """float64 [N, K]: w = scale * q + bias of a bits-wide affine weight."""
+    q, s, b = _c(qweight, np.uint32), _c(scales, np.uint16), _c(biases, np.uint16)
+    w = np.empty((N, K), dtype=np.float64)
+    if lib().oracle_dequant_affine_bits(_p(q), _p(s), _p(b), N, K, group, bits, _p(w)):
+        raise ValueError("oracle_dequant_affine_bits: bad arguments")
+    return w
+
+
+def gemm_affine_bits(x, qweight, scales, biases, M, N, K, group, bits, nthreads: int = 0):
+    """(y, sum_abs), float64 [M, N] each, of a bits-wide affine weight."""
+    x, q, s, b = (_c(x, np.uint16), _c(qweight, np.uint32), _c(scales, np.uint16), _c(biases, np.uint16))
+    y = np.empty((M, N), dtype=np.float64)
+    a = np.empty((M, N), dtype=np.float64)
+    rc = lib().oracle_gemm_affine_bits(_p(x), _p(q), _p(s), _p(b), M, N, K, group, bits, _p(y), _p(a), nthreads)
+    if rc:
+        raise ValueError("oracle_gemm_affine_bits: bad arguments")
+    return y, a
 
 def group_sums(x, M, K, group) -> np.ndarray:
     """float64 [K/G, M]: the sum of x[m] over each group of K."""

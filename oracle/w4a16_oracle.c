@@ -278,3 +278,71 @@ int oracle_gateup_silu_affine_at(const uint16_t *x,
   for (int64_t i = 0; i < count; ++i) h[i] = oracle_silu_mul(g[i], u[i]);
   return 0;
 }
+
+/*
+ * Affine form at other code widths: TensorFold PR #859 loads modules of 2 to
+ * 8 bits, every code keeping its value, scale and bias ("What this changes";
+ * the native 2, 3, 5 and 6-bit tiles note), so w = scale * q + bias with q in
+ * 0 .. 2^bits - 1. The canonical layout is read as one little-endian bit
+ * stream per row: the row's K codes fill ceil(K * bits / 32) uint32 words and
+ * code k occupies bits [bits * k, bits * k + bits) of the stream, running
+ * into the next word where it does not fit. At 4 bits this is the nibble
+ * packing of oracle_code.
+ */
+static size_t row_words_bits(int K, int bits) { return ((size_t)K * (size_t)bits + 31) / 32; }
+
+int oracle_code_bits(const uint32_t *qweight, int K, int bits, int n, int k) {
+  const size_t words = row_words_bits(K, bits);
+  const uint32_t *row = qweight + (size_t)n * words;
+  const size_t bit = (size_t)k * (size_t)bits;
+  const size_t w = bit / 32;
+  uint64_t v = row[w];
+  if (w + 1 < words) v |= (uint64_t)row[w + 1] << 32;
+  return (int)((v >> (bit % 32)) & ((1u << bits) - 1u));
+}
+
+double oracle_weight_affine_bits(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                                 int K, int G, int bits, int n, int k) {
+  const size_t i = (size_t)n * (size_t)(K / G) + (size_t)(k / G);
+  return bf16_value(scales[i]) * (double)oracle_code_bits(qweight, K, bits, n, k) + bf16_value(biases[i]);
+}
+
+static int bits_args_ok(int M, int N, int K, int G, int bits) {
+  return M >= 0 && N >= 0 && K > 0 && G > 0 && K % G == 0 && bits >= 1 && bits <= 8;
+}
+
+/* float64 [N][K]: w = scale * q + bias of a bits-wide weight. Returns 0 or -1. */
+int oracle_dequant_affine_bits(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                               int N, int K, int G, int bits, double *w) {
+  if (!bits_args_ok(0, N, K, G, bits)) return -1;
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k)
+      w[(size_t)n * K + k] = oracle_weight_affine_bits(qweight, scales, biases, K, G, bits, n, k);
+  return 0;
+}
+
+/* y[m][n] and sum_k |x w| of a bits-wide affine weight, as oracle_gemm_affine. */
+int oracle_gemm_affine_bits(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                            const uint16_t *biases, int M, int N, int K, int G, int bits,
+                            double *y, double *ysum_abs, int nthreads) {
+  if (!bits_args_ok(M, N, K, G, bits)) return -1;
+  int bad = 0;
+  int nt = pick_threads(nthreads);
+#pragma omp parallel num_threads(nt)
+  {
+    double *wrow = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!wrow) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 8)
+      for (int n = 0; n < N; ++n) {
+        for (int k = 0; k < K; ++k) wrow[k] = oracle_weight_affine_bits(qweight, scales, biases, K, G, bits, n, k);
+        for (int m = 0; m < M; ++m)
+          dot_one(x, wrow, K, m, &y[(size_t)m * N + n], &ysum_abs[(size_t)m * N + n]);
+      }
+      free(wrow);
+    }
+  }
+  return bad ? -1 : 0;
+}

@@ -26,7 +26,7 @@ __all__ = [
     "splitmix64_stream", "uniform01", "normal01", "f32_to_bf16_bits",
     "bf16_bits_to_f32", "pack_nibbles_rows", "make_codes", "make_qweight",
     "make_scales", "make_zeros", "make_biases", "make_x", "make_problem", "TENSOR_IDS",
-    "SCALE_SWEEP", "exhaustive_problem", "planted_max_problem",
+    "SCALE_SWEEP", "exhaustive_problem", "planted_max_problem", "pack_bits_rows", "make_codes_bits",
 ]
 
 def _signed(c: int) -> np.int64:
@@ -141,6 +141,29 @@ def pack_nibbles_rows(vals: np.ndarray) -> np.ndarray:
         words |= padded[:, :, j] << np.uint32(4 * j)
     return words.view(np.int32)
 
+
+
+def pack_bits_rows(vals: np.ndarray, bits: int) -> np.ndarray:
+    """Pack a [R, C] array of bits-wide integers into uint32 [R, ceil(C*bits/32)]:
+    one little-endian bit stream per row, value c at bits [bits*c, bits*c + bits),
+    running into the next word where it does not fit; unused high bits zero."""
+    vals = np.asarray(vals, dtype=np.uint64) & np.uint64((1 << bits) - 1)
+    R, C = vals.shape
+    W = (C * bits + 31) // 32
+    pos = np.arange(C, dtype=np.uint64) * np.uint64(bits)
+    word, shift = (pos // np.uint64(32)).astype(np.int64), pos % np.uint64(32)
+    shifted = vals << shift[None, :]
+    out = np.zeros((R, W + 1), dtype=np.uint64)
+    rows = np.repeat(np.arange(R), C)
+    np.bitwise_or.at(out, (rows, np.tile(word, R)), (shifted & np.uint64(0xFFFFFFFF)).ravel())
+    np.bitwise_or.at(out, (rows, np.tile(word + 1, R)), (shifted >> np.uint64(32)).ravel())
+    return out[:, :W].astype(np.uint32)
+
+
+def make_codes_bits(N: int, K: int, bits: int, seed: int, tid: int = TENSOR_IDS["qweight"]) -> np.ndarray:
+    """Uniform bits-wide codes, uint8 [N, K] (the top `bits` bits of each draw)."""
+    draws = splitmix64_stream(_stream_state(seed, tid), N * K)
+    return (draws >> np.uint64(64 - bits)).astype(np.uint8).reshape(N, K)
 
 def make_codes(N: int, K: int, seed: int, tid: int) -> np.ndarray:
     """Uniform 4-bit codes q[n][k] in 0..15, uint8 [N, K] (top 4 bits of each draw)."""

@@ -547,3 +547,118 @@ def test_topk_k1_is_the_first_maximum_and_k_n_a_permutation():
         oracle.topk_bf16(y, 0)
     with pytest.raises(ValueError):
         oracle.topk_bf16(y, 301)
+
+
+# --------------------------------------------------------------------------
+# affine form at 2, 3, 5, 6 and 8 bits
+
+BITS_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "affine_bits_worked_example.txt")
+
+
+def _load_bits_golden():
+    d = {}
+    with open(BITS_GOLDEN) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            key, v = line.split(":", 1)
+            d[key.strip()] = v.split()
+    return d
+
+
+@pytest.mark.parametrize("bits,G,M", [(3, 8, 2), (6, 16, 1)])
+def test_affine_bits_golden_worked_example(bits, G, M):
+    d = _load_bits_golden()
+    pre = f"bits{bits}_"
+    codes = np.array([int(v) for v in d[pre + "codes"]], dtype=np.uint8)[None, :]
+    words = np.array([int(h, 16) for h in d[pre + "words"]], dtype=np.uint32)[None, :]
+    s = np.array([int(h, 16) for h in d[pre + "scales"]], dtype=np.uint16)[None, :]
+    b = np.array([int(h, 16) for h in d[pre + "biases"]], dtype=np.uint16)[None, :]
+    x = np.array([int(h, 16) for h in d[pre + "x"]], dtype=np.uint16).reshape(M, 16)
+    np.testing.assert_array_equal(synth.pack_bits_rows(codes, bits), words)
+    assert [oracle.code_bits(words, 16, bits, 0, k) for k in range(16)] == codes[0].tolist()
+    y, _ = oracle.gemm_affine_bits(x, words, s, b, M, 1, 16, G, bits)
+    np.testing.assert_array_equal(y[:, 0], [float(v) for v in d[pre + "y"]])
+
+
+def _pack_by_bigint(codes, bits):
+    """Reference packer: one Python integer per row, code k shifted to bit bits*k."""
+    R, C = codes.shape
+    W = (C * bits + 31) // 32
+    out = np.zeros((R, W), dtype=np.uint32)
+    for r in range(R):
+        v = 0
+        for k in range(C):
+            v |= int(codes[r, k]) << (bits * k)
+        for i in range(W):
+            out[r, i] = (v >> (32 * i)) & 0xFFFFFFFF
+    return out
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_bit_stream_packing(bits):
+    codes = synth.make_codes_bits(5, 77, bits, seed=bits)
+    assert codes.max() < (1 << bits)
+    np.testing.assert_array_equal(synth.pack_bits_rows(codes, bits), _pack_by_bigint(codes, bits))
+    q = synth.pack_bits_rows(codes, bits)
+    got = [[oracle.code_bits(q, 77, bits, n, k) for k in range(77)] for n in range(5)]
+    np.testing.assert_array_equal(np.array(got), codes)
+
+
+def test_affine_bits4_is_the_nibble_form():
+    """At 4 bits the stream is the nibble packing, and the b-bit GEMM equals
+    the 4-bit affine GEMM on the same words exactly."""
+    M, N, K, G = 3, 20, 256, 64
+    codes = synth.make_codes(N, K, 5, 2)
+    assert np.array_equal(synth.pack_bits_rows(codes, 4).view(np.int32), synth.pack_nibbles_rows(codes))
+    s = synth.make_scales(N, K // G, 0.005, 0.02, 5)
+    b = synth.make_biases(N, K // G, -0.16, -0.04, 5)
+    x = synth.make_x(M, K, 5)
+    y4, a4 = oracle.gemm_affine(x, synth.pack_nibbles_rows(codes), s, b, M, N, K, G)
+    yb, ab = oracle.gemm_affine_bits(x, synth.pack_bits_rows(codes, 4), s, b, M, N, K, G, 4)
+    np.testing.assert_array_equal(y4, yb)
+    np.testing.assert_array_equal(a4, ab)
+
+
+def _affine_bits_case(bits, M, N, K, G, seed):
+    codes = synth.make_codes_bits(N, K, bits, seed)
+    s = synth.make_scales(N, K // G, 0.005, 0.02, seed)
+    b = synth.make_biases(N, K // G, -0.16, -0.04, seed)
+    x = synth.make_x(M, K, seed)
+    return codes, synth.pack_bits_rows(codes, bits), s, b, x
+
+
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
+@pytest.mark.parametrize("G,M,N,K", [(8, 2, 3, 40), (16, 3, 2, 96), (64, 1, 3, 128)])
+def test_affine_bits_bruteforce_exact(bits, G, M, N, K):
+    """Exact rational sums from the codes the packer was given (not from the
+    packed words), within the float64 summation bound."""
+    codes, q, s, b, x = _affine_bits_case(bits, M, N, K, G, 40 + bits + K)
+    y, a = oracle.gemm_affine_bits(x, q, s, b, M, N, K, G, bits)
+    gamma = 1.01 * K * 2.0 ** -53
+    for n in range(N):
+        w = [_fr_bf16(s[n, k // G]) * int(codes[n, k]) + _fr_bf16(b[n, k // G]) for k in range(K)]
+        for m in range(M):
+            xs = [_fr_bf16(x[m, k]) for k in range(K)]
+            ye = sum((xs[k] * w[k] for k in range(K)), Fraction(0))
+            ae = sum((abs(xs[k] * w[k]) for k in range(K)), Fraction(0))
+            assert abs(Fraction(y[m, n]) - ye) <= gamma * ae, (bits, m, n)
+            assert abs(Fraction(a[m, n]) - ae) <= gamma * ae
+
+
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
+def test_affine_bits_one_hot_x_and_dequant(bits):
+    """One-hot x at column k gives s * q + b of that column exactly, and the
+    dequantised matrix holds the same values."""
+    N, K, G = 4, 64, 16
+    codes, q, s, b, _ = _affine_bits_case(bits, 1, N, K, G, 70 + bits)
+    w = oracle.dequant_affine_bits(q, s, b, N, K, G, bits)
+    for k in (0, 1, 31, 63):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = 0x3F80
+        y, _ = oracle.gemm_affine_bits(x, q, s, b, 1, N, K, G, bits)
+        for n in range(N):
+            exact = _fr_bf16(s[n, k // G]) * int(codes[n, k]) + _fr_bf16(b[n, k // G])
+            assert Fraction(y[0, n]) == exact and Fraction(w[n, k]) == exact
+    with pytest.raises(ValueError):
+        oracle.gemm_affine_bits(np.zeros((1, K), np.uint16), q, s, b, 1, N, K, G, 9)

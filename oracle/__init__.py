@@ -279,17 +279,28 @@ def gemm_bound(ref, sum_abs):
     return REL_TOL * np.abs(ref) + ACC_TOL * np.asarray(sum_abs)
 
 
+def sigmoid(g):
+    """The logistic function 1 / (1 + e^-g), float64 (0 where e^-g overflows)."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-g))
+
+
+def dsilu(g):
+    """SiLU'(g) = d/dg [g s(g)] = s (1 + g (1 - s)), s the logistic function."""
+    g = np.asarray(g, dtype=np.float64)
+    s = sigmoid(g)
+    return s * (1.0 + g * (1.0 - s))
+
+
 def silu_bound(h_ref, g, u, gsum_abs, usum_abs):
     """Allowed |h - ref| for the fused SiLU(g) * u output (first-order propagation)."""
     g = np.asarray(g, dtype=np.float64)
     u = np.asarray(u, dtype=np.float64)
-    with np.errstate(over="ignore"):
-        s = 1.0 / (1.0 + np.exp(-g))
-    dsilu = s * (1.0 + g * (1.0 - s))
     bg = ACC_TOL * np.asarray(gsum_abs)
     bu = ACC_TOL * np.asarray(usum_abs)
-    return (REL_TOL * np.abs(h_ref) + np.abs(dsilu) * np.abs(u) * bg
-            + np.abs(g * s) * bu + bg * bu)
+    return (REL_TOL * np.abs(h_ref) + np.abs(dsilu(g)) * np.abs(u) * bg
+            + np.abs(g * sigmoid(g)) * bu + bg * bu)
 
 
 def _bf16_rank(bits) -> np.ndarray:

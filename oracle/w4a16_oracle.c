@@ -308,7 +308,7 @@ double oracle_weight_affine_bits(const uint32_t *qweight, const uint16_t *scales
 }
 
 static int bits_args_ok(int M, int N, int K, int G, int bits) {
-  return M >= 0 && N >= 0 && K > 0 && G > 0 && K % G == 0 && bits >= 1 && bits <= 8;
+  return M >= 0 && N >= 0 && K > 0 && G > 0 && K % G == 0 && bits >= 2 && bits <= 8;
 }
 
 /* float64 [N][K]: w = scale * q + bias of a bits-wide weight. Returns 0 or -1. */

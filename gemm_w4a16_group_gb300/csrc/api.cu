@@ -84,11 +84,14 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int finish_launch(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : cuda_fail(e); }
 
+// The kernel override is read once per call (`ov`, from g_override) and that
+// value decides both the argument checks and the launch, so a concurrent
+// w4a16_set_kernel_override cannot send a call the checks did not accept.
+
 // The decode kernels (M <= 32): override 2 keeps the per-warp-ring kernel, override 4
 // forces the x-staged one, otherwise the x-staged kernel takes M <= 8 calls
 // whose grid fills a wave
-cudaError_t launch_decode_kernel(GemmCall &c, int sm_count) {
-  const int ov = g_override.load();
+cudaError_t launch_decode_kernel(GemmCall &c, int sm_count, int ov) {
   c.xs_mode = ov == 4 ? 2 : ov == 2 ? 0 : 1;
   return launch_smallm_mma(c, sm_count);
 }
@@ -98,17 +101,17 @@ cudaError_t launch_decode_kernel(GemmCall &c, int sm_count) {
 // tcgen05 GEMM, M = 32 47.6 against 66.8; 3.7-4.9x at N = 5120, where the
 // GEMM has few tiles), unless the tcgen05 GEMM is forced (override 3)
 constexpr int kDecodeMaxM = 32;
-bool use_decode(int M) { return M <= kDecodeMaxM && g_override.load() != 3; }
+bool use_decode(int M, int ov) { return M <= kDecodeMaxM && ov != 3; }
 
 bool form_ok(int form) { return form == kFormZero || form == kFormSym || form == kFormAffine; }
 bool zero_form(int form) { return form == kFormZero || form == kFormSym; }
 
 // The affine calls: the decode kernel for M <= 32 (it forms the x group sums
 // itself), else the tcgen05 GEMM, which reads them from `xsum`.
-bool affine_uses_tc(int M) { return !use_decode(M); }
+bool affine_uses_tc(int M, int ov) { return !use_decode(M, ov); }
 
-int launch_affine(GemmCall &c, const uint16_t *xsum, const DeviceInfo &d) {
-  if (!affine_uses_tc(c.M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
+int launch_affine(GemmCall &c, const uint16_t *xsum, const DeviceInfo &d, int ov) {
+  if (!affine_uses_tc(c.M, ov)) return finish_launch(launch_decode_kernel(c, d.sm_count, ov));
   c.xsum = xsum;
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
@@ -204,6 +207,7 @@ int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const i
 
 int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, const int32_t *zeros, int M,
                int N, int K, int group, int sym, uint16_t *y, w4a16_stream_t stream) {
+  const int ov = g_override.load();
   if (!x || !packed || !y) return W4A16_ERR_INVALID_ARG;
   if (scales || zeros) return W4A16_ERR_INVALID_ARG;  // reserved: they travel inside `packed`
   if (!sizes_ok(M, N, K, group) || !zero_form(sym)) return W4A16_ERR_INVALID_ARG;
@@ -215,14 +219,14 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
   // M <= 32: a tensor-core decode kernel (measured faster than the CUDA-core
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
-  const int ov = g_override.load();
   if (M == 1 && ov == 1) return finish_launch(launch_gemv_m1(c, d.sm_count));
-  if (use_decode(M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
+  if (use_decode(M, ov)) return finish_launch(launch_decode_kernel(c, d.sm_count, ov));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
 int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N_each, int K, int group,
                       int sym, uint16_t *h, w4a16_stream_t stream) {
+  const int ov = g_override.load();
   if (!x || !packed_gateup || !h) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, N_each, K, group) || !zero_form(sym) || w4a16_gateup_repacked_bytes(N_each, K, group, sym) == 0)
     return W4A16_ERR_INVALID_ARG;
@@ -232,14 +236,16 @@ int w4a16_gateup_silu(const uint16_t *x, const void *packed_gateup, int M, int N
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, sym, true,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
-  if (use_decode(M)) return finish_launch(launch_decode_kernel(c, d.sm_count));
+  if (use_decode(M, ov)) return finish_launch(launch_decode_kernel(c, d.sm_count, ov));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
 int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym,
                       uint16_t *y, int64_t *argmax, w4a16_stream_t stream) {
+  const int ov = g_override.load();
+  const bool decode = use_decode(M, ov);
   if (!x || !packed || !argmax) return W4A16_ERR_INVALID_ARG;
-  if (!sizes_ok(M, N, K, group) || !zero_form(sym) || (!use_decode(M) && !y)) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group) || !zero_form(sym) || (!decode && !y)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(argmax, 8))
     return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
@@ -250,9 +256,9 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
   cudaError_t e = launch_argmax_init(argmax, M, overlap, s);
   if (e != cudaSuccess) return cuda_fail(e);
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, sym, false, s, d.err, d.device, overlap};
-  if (use_decode(M)) {
+  if (decode) {
     c.amax = argmax;  // keys from the decode kernel's epilogue; y may be NULL
-    e = launch_decode_kernel(c, d.sm_count);
+    e = launch_decode_kernel(c, d.sm_count, ov);
   } else {
     e = launch_prompt_tc(c, d.sm_count);
     if (e == cudaSuccess) e = launch_row_argmax(y, M, N, argmax, s);
@@ -278,7 +284,8 @@ int w4a16_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xsum, w4a16
 
 int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packed, int M, int N, int K, int group,
                       uint16_t *y, w4a16_stream_t stream) {
-  if (!x || !packed || !y || (!xsum && affine_uses_tc(M))) return W4A16_ERR_INVALID_ARG;
+  const int ov = g_override.load();
+  if (!x || !packed || !y || (!xsum && affine_uses_tc(M, ov))) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(xsum, 16))
     return W4A16_ERR_MISALIGNED;
@@ -287,14 +294,15 @@ int w4a16_gemm_affine(const uint16_t *x, const uint16_t *xsum, const void *packe
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, kFormAffine, false,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
-  return launch_affine(c, xsum, d);
+  return launch_affine(c, xsum, d, ov);
 }
 
 int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int N, int K, int group, uint16_t *y,
                               w4a16_stream_t stream) {
+  const int ov = g_override.load();
   if (!x || !packed || !y) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, N, K, group)) return W4A16_ERR_INVALID_ARG;
-  const bool tc = affine_uses_tc(M);
+  const bool tc = affine_uses_tc(M, ov);
   if (tc && w4a16_xsum_bytes(M, K, group) > kNoAllocXsumBytes) return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256)) return W4A16_ERR_MISALIGNED;
   DeviceInfo d;
@@ -303,16 +311,17 @@ int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   GemmCall c{x, static_cast<const uint8_t *>(packed), y, M, N, K, group, kFormAffine, false, s, d.err, d.device,
              g_overlap.load() != 0};
-  if (!tc) return launch_affine(c, nullptr, d);
+  if (!tc) return launch_affine(c, nullptr, d, ov);
   // every entry the GEMM reads (padding included) is written by this pre-pass
   cudaError_t e = launch_xsum(x, M, K, group, d.noalloc_xsum, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  return launch_affine(c, d.noalloc_xsum, d);
+  return launch_affine(c, d.noalloc_xsum, d, ov);
 }
 
 int w4a16_gateup_silu_affine(const uint16_t *x, const uint16_t *xsum, const void *packed_gateup, int M, int N_each,
                              int K, int group, uint16_t *h, w4a16_stream_t stream) {
-  if (!x || !packed_gateup || !h || (!xsum && affine_uses_tc(M))) return W4A16_ERR_INVALID_ARG;
+  const int ov = g_override.load();
+  if (!x || !packed_gateup || !h || (!xsum && affine_uses_tc(M, ov))) return W4A16_ERR_INVALID_ARG;
   if (!sizes_ok(M, N_each, K, group) || w4a16_gateup_repacked_bytes(N_each, K, group, kFormAffine) == 0)
     return W4A16_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(h, 16) || !aligned(packed_gateup, 256) || !aligned(xsum, 16))
@@ -322,7 +331,7 @@ int w4a16_gateup_silu_affine(const uint16_t *x, const uint16_t *xsum, const void
   if (st != W4A16_OK) return st;
   GemmCall c{x, static_cast<const uint8_t *>(packed_gateup), h, M, N_each, K, group, kFormAffine, true,
              reinterpret_cast<cudaStream_t>(stream), d.err, d.device, g_overlap.load() != 0};
-  return launch_affine(c, xsum, d);
+  return launch_affine(c, xsum, d, ov);
 }
 
 int w4a16_dequantize(const void *packed, int N, int K, int group, int sym, float *w_out,

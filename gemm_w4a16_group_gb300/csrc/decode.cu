@@ -169,14 +169,15 @@ struct Ring {
   uint32_t dst_off;    // offset inside a slot
   bool is_code;
   uint64_t policy;
-  int chunks, upb;  // chunks per tile, units per scale block
+  int chunks;     // chunks per tile
+  int upb_shift;  // log2 of the units per scale block (1, 2 or 4 units)
 
   __device__ void setup(const DecodeParams &p, uint8_t *warp_base, uint64_t *warp_bars, int tile0, int cpg) {
     const int lane = threadIdx.x & 31;
     sbase = smem_u32(warp_base);
     bar0 = smem_u32(warp_bars);
     chunks = p.chunks;
-    upb = 4 * cpg / kUnitChunks;  // a block of four groups spans 4 * cpg chunks
+    upb_shift = __ffs(4 * cpg / kUnitChunks) - 1;  // a block of four groups spans 4 * cpg chunks
     const int kind = lane / TPW, i = lane % TPW;
     const size_t tile = (size_t)min(tile0 + i, p.tiles - 1);
     is_code = kind == 0;
@@ -212,7 +213,7 @@ struct Ring {
       mbar_arrive_expect_tx(bar, TPW * (nch * kChunkBytes + kScaleBlockBytes + kThirdBytes));
     if (lane < kCopies) {
       const uint32_t bytes = is_code ? (uint32_t)(nch * kChunkBytes) : stride;
-      const size_t step = is_code ? (size_t)u : (size_t)(u / upb);
+      const size_t step = is_code ? (size_t)u : (size_t)(u >> upb_shift);
       bulk_copy(sbase + s * kSlotBytes + dst_off, src + step * stride, bytes, bar, policy);
     }
   }

@@ -61,3 +61,29 @@ def test_noalloc_consecutive_calls_on_different_x():
     for x, y in ((pa["x"], ya), (pb["x"], yb)):
         ref, sa = oracle.gemm_affine(x, pa["qweight"], pa["scales"], pa["biases"], M, N, K, group)
         assert_within(host_bits(y), ref, oracle.gemm_bound(ref, sa), "noalloc x")
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_4_mib_limit():
+    """A table of exactly 4 MiB (M = 8,192 rows at K = 5120, group 64): the
+    last rows of the fixed array are written and read. Bitwise equal to the
+    table entry point on two consecutive calls, and within the oracle's bound
+    on sampled outputs."""
+    M, N, K, group = 8192, 64, 5120, 64
+    assert w4.xsum_bytes(M, K, group) == 4 << 20
+    p = synth.make_problem(M, N, K, group, False, seed=17, affine=True)
+    x = dev(p["x"])
+    packed = w4.repack_affine(dev(p["qweight"]), dev(p["scales"]), dev(p["biases"]), N, K, group)
+    y_ref = w4.gemm_affine(x, packed, N, K, group, w4.xsum(x, K, group))
+    y1 = w4.gemm_affine_noalloc(x, packed, N, K, group)
+    y2 = w4.gemm_affine_noalloc(x, packed, N, K, group)
+    torch().cuda.synchronize()
+    assert w4.kernel_status() == 0
+    b_ref = host_bits(y_ref)
+    np.testing.assert_array_equal(host_bits(y1), b_ref)
+    np.testing.assert_array_equal(host_bits(y2), b_ref)
+    mi = np.concatenate([np.arange(M - 8, M), np.arange(0, M, 97)]).astype(np.int64)
+    mi = np.repeat(mi, 4)
+    ni = np.tile(np.array([0, 17, 40, N - 1], dtype=np.int64), mi.size // 4)
+    ref, sa = oracle.gemm_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, group, mi, ni)
+    assert_within(b_ref[mi, ni], ref, oracle.gemm_bound(ref, sa), "noalloc 4 MiB")

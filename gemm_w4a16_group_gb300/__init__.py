@@ -30,7 +30,7 @@ __all__ = [
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
     "KERNEL_XSTAGED",
     "AFFINE", "repack_affine", "repack_affine_gateup", "xsum_bytes", "xsum", "gemm_affine", "gateup_silu_affine",
-    "gemm_affine_noalloc",
+    "gemm_affine_noalloc", "topk", "gemm_topk",
 ]
 
 # symbols declared in include/w4a16.h
@@ -40,6 +40,7 @@ EXPORTS = (
     "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
     "w4a16_set_programmatic_overlap", "w4a16_repack_affine", "w4a16_repack_affine_gateup", "w4a16_xsum_bytes",
     "w4a16_xsum", "w4a16_gemm_affine", "w4a16_gateup_silu_affine", "w4a16_gemm_affine_noalloc",
+    "w4a16_topk", "w4a16_gemm_topk",
 )
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC, KERNEL_XSTAGED = 0, 1, 2, 3, 4
 # the `sym` argument: 0 zero points, 1 symmetric (z = 8), AFFINE scale * q + bias
@@ -112,6 +113,10 @@ def lib(auto_build: bool = True) -> ctypes.CDLL:
     L.w4a16_gateup_silu_affine.restype = i32
     L.w4a16_gemm_affine_noalloc.argtypes = [P, P, i32, i32, i32, i32, P, P]
     L.w4a16_gemm_affine_noalloc.restype = i32
+    L.w4a16_topk.argtypes = [P, i32, i32, i32, P, P, P]
+    L.w4a16_topk.restype = i32
+    L.w4a16_gemm_topk.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P, P, P, P]
+    L.w4a16_gemm_topk.restype = i32
     _lib = L
     return L
 
@@ -284,6 +289,53 @@ def gemm_argmax(x, packed, N, K, group, sym, out=None, logits=False, stream=None
                                  _ptr(idx, (torch.int64,), "index_out", 8 * M, d), _stream(stream, d))
     _check(rc, "w4a16_gemm_argmax")
     return idx, out
+
+
+TOPK_MAX_K = 1024
+
+
+def _topk_outs(M, k, d, index_out, values_out, values):
+    torch = _torch()
+    idx = index_out if index_out is not None else torch.empty((M, k), dtype=torch.int64, device=d)
+    vals = values_out
+    if vals is None and values:
+        vals = torch.empty((M, k), dtype=torch.bfloat16, device=d)
+    return idx, vals
+
+
+def topk(y, k, index_out=None, values_out=None, values=True, stream=None):
+    """The k largest entries of every row of the bf16 logits y [M, N], largest
+    first (equal values lowest column first, -0 = +0, NaN above +inf).
+    Returns (indices int64 [M, k], values bf16 [M, k] or None)."""
+    torch = _torch()
+    if y.dim() != 2:
+        raise ValueError("y must be [M, N]")
+    M, N = y.shape
+    d = y.device
+    idx, vals = _topk_outs(M, k, d, index_out, values_out, values)
+    rc = lib().w4a16_topk(_ptr(y, _bf16_types(), "y", 2 * M * N, d), M, N, k,
+                          _ptr(idx, (torch.int64,), "index_out", 8 * M * k, d),
+                          _ptr(vals, _bf16_types(), "values_out", 2 * M * k, d), _stream(stream, d))
+    _check(rc, "w4a16_topk")
+    return idx, vals
+
+
+def gemm_topk(x, packed, N, K, group, sym, k, out=None, index_out=None, values_out=None, values=True, stream=None):
+    """y = x . dequant(W)^T (bf16, into `out` or a new tensor), then the top-k
+    of each row of y. Returns (indices, values or None, y)."""
+    torch = _torch()
+    M = _x_rows(x, K)
+    d = x.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    idx, vals = _topk_outs(M, k, d, index_out, values_out, values)
+    rc = lib().w4a16_gemm_topk(_ptr(x, _bf16_types(), "x", 0, d),
+                               _ptr(packed, (torch.uint8,), "packed", _packed_bytes(N, K, group, int(sym), False), d),
+                               M, N, K, group, int(sym), k, _ptr(out, _bf16_types(), "out", 2 * M * N, d),
+                               _ptr(idx, (torch.int64,), "index_out", 8 * M * k, d),
+                               _ptr(vals, _bf16_types(), "values_out", 2 * M * k, d), _stream(stream, d))
+    _check(rc, "w4a16_gemm_topk")
+    return idx, vals, out
 
 
 def gateup_silu(x, packed_gateup, N_each, K, group, sym, out=None, stream=None):

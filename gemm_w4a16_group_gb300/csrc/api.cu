@@ -267,6 +267,26 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
   return finish_launch(e);
 }
 
+int w4a16_topk(const uint16_t *y, int M, int N, int k, int64_t *idx, uint16_t *vals, w4a16_stream_t stream) {
+  if (!y || !idx) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, 64, 64) || k < 1 || k > N || k > kTopkMaxK) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(y, 2) || !aligned(idx, 8) || !aligned(vals, 2)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  return finish_launch(launch_topk(y, M, N, k, idx, vals, g_overlap.load() != 0, d.device,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_gemm_topk(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym, int k,
+                    uint16_t *y, int64_t *idx, uint16_t *vals, w4a16_stream_t stream) {
+  if (k < 1 || k > N || k > kTopkMaxK || !idx) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(idx, 8) || !aligned(vals, 2)) return W4A16_ERR_MISALIGNED;
+  const int st = w4a16_gemm(x, packed, nullptr, nullptr, M, N, K, group, sym, y, stream);
+  if (st != W4A16_OK) return st;
+  return w4a16_topk(y, M, N, k, idx, vals, stream);
+}
+
 size_t w4a16_xsum_bytes(int M, int K, int group) {
   if (!sizes_ok(M, 1, K, group)) return 0;
   return (size_t)M * (size_t)affine_kb3(K / group) * sizeof(uint16_t);

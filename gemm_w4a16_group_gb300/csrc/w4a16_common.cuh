@@ -141,12 +141,18 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t zg, uint32_t zg
 // occurrence). High half: the bf16 bits mapped to an order-preserving
 // unsigned code, -0 as +0, every NaN above +inf (a NaN is the maximum).
 // Low half: 0xFFFFFFFF - n. Key 0 is below every output.
-__device__ __forceinline__ unsigned long long argmax_key(uint32_t bits, int n) {
+// The order-preserving 16-bit code of a bf16 value: larger code = larger
+// value, -0 and +0 share 0x8000, every NaN is 0xFFFF (above +inf's 0xFF80).
+__device__ __forceinline__ uint32_t order_key16(uint32_t bits) {
   bits &= 0xFFFFu;
   if (bits == 0x8000u) bits = 0;
   uint32_t o = (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
   if ((bits & 0x7F80u) == 0x7F80u && (bits & 0x7Fu)) o = 0xFFFFu;
-  return ((unsigned long long)o << 32) | (0xFFFFFFFFu - (uint32_t)n);
+  return o;
+}
+
+__device__ __forceinline__ unsigned long long argmax_key(uint32_t bits, int n) {
+  return ((unsigned long long)order_key16(bits) << 32) | (0xFFFFFFFFu - (uint32_t)n);
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
@@ -320,6 +326,19 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
   return v;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u64(uint32_t cluster_addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");

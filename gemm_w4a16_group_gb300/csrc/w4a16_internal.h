@@ -62,5 +62,9 @@ cudaError_t launch_argmax_finalize(int64_t *amax, int M, bool overlap, cudaStrea
 // group, bf16 [M][affine_kb3(K / group)]
 cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xs, cudaStream_t stream);
 cudaError_t launch_row_argmax(const uint16_t *y, int M, int N, int64_t *amax, cudaStream_t stream);
+// the k largest entries of every bf16 row of y [M][N], largest first
+constexpr int kTopkMaxK = 1024;
+cudaError_t launch_topk(const uint16_t *y, int M, int N, int k, int64_t *idx, uint16_t *vals, bool overlap,
+                        int device, cudaStream_t stream);
 
 }  // namespace w4a16

@@ -154,6 +154,35 @@ int w4a16_gemm_argmax(const uint16_t *x, const void *packed, int M, int N, int K
                       uint16_t *y, int64_t *argmax, w4a16_stream_t stream);
 
 /*
+ * Top-k of bf16 rows: the greedy pick on the GPU (lucebox PR #823,
+ * description) widened to the k largest entries of each row of the logits
+ * y [M][N], with the argmax's rules: largest value first; equal values
+ * lowest column first (-0 equals +0); a NaN ranks above +inf (NaNs among
+ * themselves by column). k = 1 gives w4a16_gemm_argmax's index.
+ *
+ *   y     bf16 [M][N], device, 2-byte aligned (16-byte aligned rows with N a
+ *         multiple of 8 take 16-byte loads); read only
+ *   k     1 <= k <= min(N, 1024)
+ *   idx   int64 [M][k], device, 8-byte aligned: the columns, best first
+ *   vals  bf16 [M][k], device, or NULL: y at those columns (bit patterns)
+ *
+ * One kernel on `stream`: per row, one cluster of up to 16 CTAs (two radix
+ * passes of 8 bits over the order-preserving 16-bit codes of the values,
+ * histograms summed over distributed shared memory, then a sort of the k
+ * picks); it allocates nothing and takes part in programmatic overlap when
+ * that is on. Errors: W4A16_ERR_INVALID_ARG (null y or idx, M or N out of
+ * range, k out of range), W4A16_ERR_MISALIGNED, as w4a16_gemm otherwise.
+ */
+int w4a16_topk(const uint16_t *y, int M, int N, int k, int64_t *idx, uint16_t *vals, w4a16_stream_t stream);
+
+/*
+ * w4a16_gemm into y (required: the logits the selection reads), then
+ * w4a16_topk of y. Every argument is checked before the first launch.
+ */
+int w4a16_gemm_topk(const uint16_t *x, const void *packed, int M, int N, int K, int group, int sym, int k,
+                    uint16_t *y, int64_t *idx, uint16_t *vals, w4a16_stream_t stream);
+
+/*
  * Fused feed-forward gate (GRIMOIRE v1.8, "INT4 prompt processing"):
  *   h[M][N_each] = SiLU(x Wg^T) * (x Wu^T),  SiLU(v) = v / (1 + e^-v),
  * with both products accumulated in float32 and never rounded before the

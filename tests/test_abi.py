@@ -119,6 +119,26 @@ def test_argmax_entry_point_argument_checks(L):
     assert g(P(FAKE), P(FAKE), 4, 64, 128, 64, 1, P(FAKE + 2), P(FAKE), None) == MISALIGNED
 
 
+def test_topk_entry_points_argument_checks(L):
+    P = ctypes.c_void_p
+    t = L.w4a16_topk
+    assert t(None, 2, 300, 8, P(FAKE), None, None) == INVALID                    # no y
+    assert t(P(FAKE), 2, 300, 8, None, None, None) == INVALID                    # no idx
+    assert t(P(FAKE), 2, 300, 0, P(FAKE), None, None) == INVALID                 # k < 1
+    assert t(P(FAKE), 2, 300, 301, P(FAKE), None, None) == INVALID               # k > N
+    assert t(P(FAKE), 2, 5000, 1025, P(FAKE), None, None) == INVALID             # k > 1024
+    assert t(P(FAKE), 0, 300, 8, P(FAKE), None, None) == INVALID                 # M < 1
+    assert t(P(FAKE + 1), 2, 300, 8, P(FAKE), None, None) == MISALIGNED          # y
+    assert t(P(FAKE), 2, 300, 8, P(FAKE + 4), None, None) == MISALIGNED          # idx
+    assert t(P(FAKE), 2, 300, 8, P(FAKE), P(FAKE + 1), None) == MISALIGNED       # vals
+    g = L.w4a16_gemm_topk
+    assert g(P(FAKE), P(FAKE), 2, 300, 128, 64, 1, 0, P(FAKE), P(FAKE), None, None) == INVALID
+    assert g(P(FAKE), P(FAKE), 2, 300, 128, 64, 1, 8, None, P(FAKE), None, None) == INVALID   # y required
+    assert g(P(FAKE), P(FAKE), 2, 300, 128, 64, 1, 8, P(FAKE), None, None, None) == INVALID   # no idx
+    assert g(P(FAKE), P(FAKE), 2, 300, 96, 64, 1, 8, P(FAKE), P(FAKE), None, None) == INVALID  # K % G
+    assert g(P(FAKE), P(FAKE), 2, 300, 128, 64, 1, 8, P(FAKE), P(FAKE + 4), None, None) == MISALIGNED
+
+
 def test_affine_layout_and_argument_checks(L):
     P = ctypes.c_void_p
     # the bias section is the scales' size (N=256, K=512, G=128 -> 2048 B), then

@@ -94,6 +94,28 @@ def test_lm_head_argmax(M):
     assert exact >= M - 1
 
 
+@pytest.mark.parametrize("M", [16, 5, 1])
+def test_lm_head_topk(M):
+    """Top-k over all 248,320 columns of the head's logits (w4a16_gemm_topk),
+    element by element against the oracle's top-k of the same logits, at
+    k = 1, 8 and 64; k = 1 is the fused argmax's pick."""
+    name = f"lm_head_m{M}_k5120_n248320"
+    p = problem(name)
+    d = upload(p)
+    packed = packed_of(p, d)
+    fused, _ = w4.gemm_argmax(d["x"], packed, p["N"], p["K"], p["group"], p["sym"])
+    for k in (1, 8, 64):
+        idx, vals, y = w4.gemm_topk(d["x"], packed, p["N"], p["K"], p["group"], p["sym"], k)
+        torch().cuda.synchronize()
+        assert w4.kernel_status() == 0
+        yb = host_bits(y)
+        want_i, want_v = oracle.topk_bf16(yb, k)
+        np.testing.assert_array_equal(idx.cpu().numpy(), want_i)
+        np.testing.assert_array_equal(host_bits(vals), want_v)
+        if k == 1:
+            np.testing.assert_array_equal(idx.cpu().numpy()[:, 0], fused.cpu().numpy())
+
+
 GATEUP_NAMES = [n for n, w in WORKLOADS.items() if w["kind"] == "gateup"]
 
 

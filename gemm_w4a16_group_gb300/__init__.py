@@ -30,7 +30,8 @@ __all__ = [
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
     "KERNEL_XSTAGED",
     "AFFINE", "repack_affine", "repack_affine_gateup", "xsum_bytes", "xsum", "gemm_affine", "gateup_silu_affine",
-    "gemm_affine_noalloc", "topk", "gemm_topk",
+    "gemm_affine_noalloc", "topk", "gemm_topk", "affine_bits_repacked_bytes", "repack_affine_bits",
+    "affine_bits_scratch_bytes", "gemm_affine_bits", "dequantize_affine_bits",
 ]
 
 # symbols declared in include/w4a16.h
@@ -40,7 +41,8 @@ EXPORTS = (
     "w4a16_strerror", "w4a16_last_cuda_error", "w4a16_set_kernel_override",
     "w4a16_set_programmatic_overlap", "w4a16_repack_affine", "w4a16_repack_affine_gateup", "w4a16_xsum_bytes",
     "w4a16_xsum", "w4a16_gemm_affine", "w4a16_gateup_silu_affine", "w4a16_gemm_affine_noalloc",
-    "w4a16_topk", "w4a16_gemm_topk",
+    "w4a16_topk", "w4a16_gemm_topk", "w4a16_affine_bits_repacked_bytes", "w4a16_repack_affine_bits",
+    "w4a16_affine_bits_scratch_bytes", "w4a16_gemm_affine_bits", "w4a16_dequantize_affine_bits",
 )
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC, KERNEL_XSTAGED = 0, 1, 2, 3, 4
 # the `sym` argument: 0 zero points, 1 symmetric (z = 8), AFFINE scale * q + bias
@@ -117,6 +119,16 @@ def lib(auto_build: bool = True) -> ctypes.CDLL:
     L.w4a16_topk.restype = i32
     L.w4a16_gemm_topk.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P, P, P, P]
     L.w4a16_gemm_topk.restype = i32
+    L.w4a16_affine_bits_repacked_bytes.argtypes = [i32, i32, i32, i32]
+    L.w4a16_affine_bits_repacked_bytes.restype = ctypes.c_size_t
+    L.w4a16_repack_affine_bits.argtypes = [P, P, P, i32, i32, i32, i32, P, P]
+    L.w4a16_repack_affine_bits.restype = i32
+    L.w4a16_affine_bits_scratch_bytes.argtypes = [i32, i32, i32, i32]
+    L.w4a16_affine_bits_scratch_bytes.restype = ctypes.c_size_t
+    L.w4a16_gemm_affine_bits.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P]
+    L.w4a16_gemm_affine_bits.restype = i32
+    L.w4a16_dequantize_affine_bits.argtypes = [P, i32, i32, i32, i32, P, P]
+    L.w4a16_dequantize_affine_bits.restype = i32
     _lib = L
     return L
 
@@ -445,6 +457,69 @@ def gemm_affine_noalloc(x, packed, N, K, group, out=None, stream=None):
                                          _stream(stream, d))
     _check(rc, "w4a16_gemm_affine_noalloc")
     return out
+
+
+def affine_bits_repacked_bytes(N: int, K: int, group: int, bits: int) -> int:
+    return int(lib().w4a16_affine_bits_repacked_bytes(N, K, group, bits))
+
+
+def affine_bits_scratch_bytes(M: int, K: int, group: int, bits: int) -> int:
+    return int(lib().w4a16_affine_bits_scratch_bytes(M, K, group, bits))
+
+
+def repack_affine_bits(qweight, scales, biases, N, K, group, bits, stream=None):
+    """Canonical b-bit affine weight (qweight uint32/int32 [N, ceil(K*bits/32)],
+    one bit stream per row; scales and biases bf16 [N, K/G]) -> packed uint8."""
+    torch = _torch()
+    nbytes = affine_bits_repacked_bytes(N, K, group, bits)
+    if nbytes == 0:
+        raise W4A16Error(f"unsupported b-bit affine weight N={N} K={K} group={group} bits={bits}")
+    d = qweight.device
+    out = torch.empty(nbytes, dtype=torch.uint8, device=d)
+    qbytes = N * ((K * bits + 31) // 32) * 4
+    _, sbytes, _ = _canonical_bytes(N, K, group)
+    rc = lib().w4a16_repack_affine_bits(_ptr(qweight, (torch.int32, torch.uint32), "qweight", qbytes, d),
+                                        _ptr(scales, _bf16_types(), "scales", sbytes, d),
+                                        _ptr(biases, _bf16_types(), "biases", sbytes, d), N, K, group, bits,
+                                        _ptr(out, (torch.uint8,), "packed", nbytes, d), _stream(stream, d))
+    _check(rc, "w4a16_repack_affine_bits")
+    return out
+
+
+def gemm_affine_bits(x, packed, N, K, group, bits, scratch=None, out=None, stream=None):
+    """y[M, N] (bf16) = x . (scale * q + bias)^T of a b-bit affine weight;
+    `scratch` (uint8, affine_bits_scratch_bytes) is allocated when not given."""
+    torch = _torch()
+    M = _x_rows(x, K)
+    d = x.device
+    sbytes = affine_bits_scratch_bytes(M, K, group, bits)
+    if sbytes == 0:
+        raise W4A16Error(f"unsupported b-bit affine call M={M} K={K} group={group} bits={bits}")
+    if scratch is None:
+        scratch = torch.empty(sbytes, dtype=torch.uint8, device=d)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+    rc = lib().w4a16_gemm_affine_bits(_ptr(x, _bf16_types(), "x", 2 * M * K, d),
+                                      _ptr(scratch, (torch.uint8,), "scratch", sbytes, d),
+                                      _ptr(packed, (torch.uint8,), "packed", affine_bits_repacked_bytes(N, K, group, bits),
+                                           d),
+                                      M, N, K, group, bits, _ptr(out, _bf16_types(), "out", 2 * M * N, d),
+                                      _stream(stream, d))
+    _check(rc, "w4a16_gemm_affine_bits")
+    return out
+
+
+def dequantize_affine_bits(packed, N, K, group, bits, stream=None):
+    """float32 [N, K]: scale * q + bias read back from a b-bit packed weight."""
+    torch = _torch()
+    d = packed.device
+    w = torch.empty((N, K), dtype=torch.float32, device=d)
+    rc = lib().w4a16_dequantize_affine_bits(_ptr(packed, (torch.uint8,), "packed",
+                                                 affine_bits_repacked_bytes(N, K, group, bits), d),
+                                            N, K, group, bits, _ptr(w, (torch.float32,), "w_out", 4 * N * K, d),
+                                            _stream(stream, d))
+    _check(rc, "w4a16_dequantize_affine_bits")
+    return w
 
 
 def gateup_silu_affine(x, packed_gateup, N_each, K, group, xs=None, out=None, stream=None):

@@ -116,6 +116,14 @@ int launch_affine(GemmCall &c, const uint16_t *xsum, const DeviceInfo &d, int ov
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
 
+// b-bit affine weights: 2-4 bits widened into nibbles, 5-8 bits in two
+// nibble planes over K' = 2K (x's groups each written twice)
+bool bits_ok(int bits) { return bits >= 2 && bits <= 8; }
+int bits_planes(int bits) { return bits > 4 ? 2 : 1; }
+size_t widened_x_bytes(int M, int K, int bits) {
+  return bits > 4 ? align_up((size_t)M * 2 * (size_t)K * sizeof(uint16_t), 256) : 0;
+}
+
 // rows of a gate/up buffer (each weight padded to 128 rows), or -1 if too many
 long long gateup_rows(int N_each) {
   const long long rows = 2LL * ((N_each + 127) / 128 * 128);
@@ -336,6 +344,79 @@ int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int 
   cudaError_t e = launch_xsum(x, M, K, group, d.noalloc_xsum, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return launch_affine(c, d.noalloc_xsum, d, ov);
+}
+
+size_t w4a16_affine_bits_repacked_bytes(int N, int K, int group, int bits) {
+  if (!bits_ok(bits) || !sizes_ok(1, N, K, group)) return 0;
+  const long long Kp = (long long)K * bits_planes(bits);
+  if (!sizes_ok(1, N, Kp, group)) return 0;
+  return make_layout(N, (int)Kp, group, kFormAffine).total;
+}
+
+size_t w4a16_affine_bits_scratch_bytes(int M, int K, int group, int bits) {
+  if (!bits_ok(bits) || !sizes_ok(M, 1, K, group)) return 0;
+  const long long Kp = (long long)K * bits_planes(bits);
+  if (!sizes_ok(M, 1, Kp, group)) return 0;
+  return widened_x_bytes(M, K, bits) + (size_t)M * (size_t)affine_kb3((int)(Kp / group)) * sizeof(uint16_t);
+}
+
+int w4a16_repack_affine_bits(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases, int N, int K,
+                             int group, int bits, void *packed, w4a16_stream_t stream) {
+  if (!qweight || !scales || !biases || !packed) return W4A16_ERR_INVALID_ARG;
+  if (w4a16_affine_bits_repacked_bytes(N, K, group, bits) == 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(qweight, 4) || !aligned(scales, 2) || !aligned(biases, 2))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const Layout L = make_layout(N, K * bits_planes(bits), group, kFormAffine);
+  return finish_launch(launch_repack_affine_bits(reinterpret_cast<const uint32_t *>(qweight), scales, biases, N, K,
+                                                 bits, L, static_cast<uint8_t *>(packed),
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4a16_gemm_affine_bits(const uint16_t *x, void *scratch, const void *packed, int M, int N, int K, int group,
+                           int bits, uint16_t *y, w4a16_stream_t stream) {
+  const int ov = g_override.load();
+  if (!x || !scratch || !packed || !y) return W4A16_ERR_INVALID_ARG;
+  if (!sizes_ok(M, N, K, group) || w4a16_affine_bits_scratch_bytes(M, K, group, bits) == 0 ||
+      w4a16_affine_bits_repacked_bytes(N, K, group, bits) == 0)
+    return W4A16_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(packed, 256) || !aligned(scratch, 256))
+    return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *scr = static_cast<uint8_t *>(scratch);
+  const uint16_t *xin = x;
+  if (bits > 4) {
+    uint16_t *xw = reinterpret_cast<uint16_t *>(scr);
+    cudaError_t e = launch_widen_groups(x, M, K, group, xw, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    xin = xw;
+  }
+  const int Kp = K * bits_planes(bits);
+  GemmCall c{xin, static_cast<const uint8_t *>(packed), y, M, N, Kp, group, kFormAffine, false, s, d.err, d.device,
+             g_overlap.load() != 0};
+  if (!affine_uses_tc(M, ov)) return launch_affine(c, nullptr, d, ov);
+  uint16_t *xs = reinterpret_cast<uint16_t *>(scr + widened_x_bytes(M, K, bits));
+  cudaError_t e = launch_xsum(xin, M, Kp, group, xs, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return launch_affine(c, xs, d, ov);
+}
+
+int w4a16_dequantize_affine_bits(const void *packed, int N, int K, int group, int bits, float *w_out,
+                                 w4a16_stream_t stream) {
+  if (!packed || !w_out) return W4A16_ERR_INVALID_ARG;
+  if (w4a16_affine_bits_repacked_bytes(N, K, group, bits) == 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(w_out, 16)) return W4A16_ERR_MISALIGNED;
+  DeviceInfo d;
+  int st = current_device(d);
+  if (st != W4A16_OK) return st;
+  const Layout L = make_layout(N, K * bits_planes(bits), group, kFormAffine);
+  return finish_launch(launch_dequantize_affine_bits(static_cast<const uint8_t *>(packed), L, N, K, bits, w_out,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int w4a16_gateup_silu_affine(const uint16_t *x, const uint16_t *xsum, const void *packed_gateup, int M, int N_each,

@@ -19,7 +19,51 @@ struct RepackSrc {
   const uint16_t *b[2];  // biases (affine form)
   int n_src;     // rows of each source weight
   int gateup;    // 0: one weight, tile T = rows 16T..; 1: tiles alternate gate, up
+  // b-bit affine codes (bits != 0): qw is one little-endian bit stream per
+  // row of k_src codes; bits <= 4 are widened into the nibbles (layout K =
+  // k_src), bits 5-8 are split into two 4-bit planes (below; layout K =
+  // 2 k_src)
+  int bits;
+  int k_src;
 };
+
+// Two planes of a b-bit code q = 16 qh + ql (bits 5-8): packed group 2g holds
+// qh with scale 16 s and the bias, packed group 2g + 1 holds ql with scale s
+// and bias 0, both against the same x values (the x of group g, repeated).
+// 16 s is exact in bf16 (scales below 2^123 do not overflow).
+__device__ __forceinline__ bool two_planes(const RepackSrc &s) { return s.bits > 4; }
+
+// code k of a row of the b-bit stream
+__device__ __forceinline__ uint32_t stream_code(const uint32_t *row_words, int words, int bits, int k) {
+  const long long bit = (long long)k * bits;
+  const int w = (int)(bit >> 5);
+  uint64_t v = row_words[w];
+  if (w + 1 < words) v |= (uint64_t)row_words[w + 1] << 32;
+  return (uint32_t)((v >> (bit & 31)) & ((1u << bits) - 1u));
+}
+
+// the 4-bit code at packed column k of a source row (b-bit forms)
+__device__ __forceinline__ uint32_t bits_code(const RepackSrc &s, int which, int row, int k, int group) {
+  const int words = (int)(((long long)s.k_src * s.bits + 31) / 32);
+  const uint32_t *rw = s.qw[which] + (size_t)row * words;
+  if (!two_planes(s)) return stream_code(rw, words, s.bits, k);
+  const int gp = k / group, g = gp >> 1;
+  const uint32_t q = stream_code(rw, words, s.bits, g * group + k % group);
+  return (gp & 1) ? (q & 0xFu) : (q >> 4);
+}
+
+// scale (or bias) of packed group gi of a source row
+__device__ __forceinline__ uint16_t group_value(const RepackSrc &s, int which, int row, int gi, int groups,
+                                                bool bias) {
+  const uint16_t *src = bias ? s.b[which] : s.sc[which];
+  if (!s.bits || !two_planes(s)) return src[(size_t)row * groups + gi];
+  const int g = gi >> 1, src_groups = groups / 2;
+  const uint16_t v = src[(size_t)row * src_groups + g];
+  if (gi & 1) return bias ? (uint16_t)0 : v;  // low plane: s, bias 0
+  if (bias) return v;                          // high plane: the bias
+  const float f = __uint_as_float((uint32_t)v << 16) * 16.0f;  // 16 s, exact
+  return (uint16_t)(__float_as_uint(f) >> 16);
+}
 
 // (source, row) of row r (0..15) of tile T; row < 0 for padding
 __device__ __forceinline__ int src_row(const RepackSrc &s, int T, int r, int &which) {
@@ -57,7 +101,14 @@ __global__ void repack_codes_kernel(RepackSrc s, Layout L, uint32_t *out) {
     for (int h = 0; h < 2; ++h) {
       int which;
       int row = src_row(s, T, g + 8 * h, which);
-      src[h] = row < 0 ? 0u : (s.qw[which][(size_t)row * kw + k0 / 8] >> (4 * (k0 % 8)));
+      if (row < 0) {
+        src[h] = 0u;
+      } else if (s.bits) {  // four codes k0 .. k0 + 3 as nibbles
+        src[h] = 0u;
+        for (int q = 0; q < 4; ++q) src[h] |= bits_code(s, which, row, k0 + q, L.group) << (4 * q);
+      } else {
+        src[h] = s.qw[which][(size_t)row * kw + k0 / 8] >> (4 * (k0 % 8));
+      }
     }
     uint32_t word = 0;
 #pragma unroll
@@ -84,8 +135,7 @@ __global__ void repack_scales_kernel(RepackSrc s, Layout L, bool bias, uint16_t 
     const int gi = 4 * blk + j;
     int which;
     const int row = src_row(s, T, g + 8 * h, which);
-    const uint16_t *src = bias ? s.b[which] : s.sc[which];
-    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0 : src[(size_t)row * L.groups + gi];
+    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0 : group_value(s, which, row, gi, L.groups, bias);
   }
 }
 
@@ -123,7 +173,7 @@ __global__ void repack_bias_operand_kernel(RepackSrc s, Layout L, uint16_t *out)
     const int gi = j / 3;
     int which;
     const int row = src_row(s, T, rr, which);
-    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0 : s.b[which][(size_t)row * L.groups + gi];
+    out[idx] = (row < 0 || gi >= L.groups) ? (uint16_t)0 : group_value(s, which, row, gi, L.groups, true);
   }
 }
 
@@ -189,6 +239,51 @@ __global__ void dequantize_kernel(const uint8_t *packed, Layout L, int N, float 
   }
 }
 
+// the 4-bit code at (row n, packed column k) of the tiled layout
+__device__ __forceinline__ uint32_t tiled_code(const uint8_t *packed, const Layout &L, int n, int k) {
+  const int T = n / 16, r = n % 16, gg = r % 8, h = r / 8;
+  const int c = k / 64, kk = k % 64, t = kk / 16, sidx = (kk % 16) / 4, koff = kk % 4;
+  const int j = (koff == 0 ? 0 : koff == 1 ? 4 : koff == 2 ? 2 : 6) + h;  // kofs(j) = koff, row half h
+  const uint32_t *codes = reinterpret_cast<const uint32_t *>(packed + L.codes_off);
+  const uint32_t word = codes[(((size_t)T * L.chunks + c) * 32 + (4 * gg + t)) * 4 + sidx];
+  return (word >> (4 * j)) & 0xFu;
+}
+
+// the bf16 scale (or bias, from `section`) of (row n, packed group gi)
+__device__ __forceinline__ float tiled_group_value(const uint8_t *packed, size_t section, const Layout &L, int n,
+                                                   int gi) {
+  const int T = n / 16, r = n % 16, gg = r % 8, h = r / 8;
+  const uint16_t *v = reinterpret_cast<const uint16_t *>(packed + section);
+  const uint16_t b = v[(((size_t)T * L.gblocks + gi / 4) * 8 + gg) * 8 + (gi & 3) * 2 + h];
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// w[n][k] = scale * q + bias of a b-bit affine weight, rounded once to
+// float32, read back from its tiled planes: q = 16 qh + ql with qh, ql and
+// their scales 16 s and s in packed groups 2g and 2g + 1 (bits 5-8), or the
+// widened code itself (bits 2-4)
+__global__ void dequantize_bits_kernel(const uint8_t *packed, Layout L, int N, int K, int bits, float *w) {
+  const size_t total = (size_t)N * K;
+  const int G = L.group;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(idx / K), k = (int)(idx % K);
+    const int g = k / G;
+    float q, sc, bi;
+    if (bits > 4) {
+      const int khi = 2 * g * G + k % G;
+      q = (float)(16 * tiled_code(packed, L, n, khi) + tiled_code(packed, L, n, khi + G));
+      sc = tiled_group_value(packed, L.scales_off, L, n, 2 * g + 1);
+      bi = tiled_group_value(packed, L.biases_off, L, n, 2 * g);
+    } else {
+      q = (float)tiled_code(packed, L, n, k);
+      sc = tiled_group_value(packed, L.scales_off, L, n, g);
+      bi = tiled_group_value(packed, L.biases_off, L, n, g);
+    }
+    w[idx] = fmaf(sc, q, bi);
+  }
+}
+
 int grid_for(size_t work, int threads) {
   size_t b = (work + threads - 1) / threads;
   if (b > 65535u * 16u) b = 65535u * 16u;
@@ -196,6 +291,31 @@ int grid_for(size_t work, int threads) {
 }
 
 }  // namespace
+
+namespace {
+cudaError_t launch_repack_src(RepackSrc &s, const Layout &L, uint8_t *packed, cudaStream_t stream);
+}
+
+cudaError_t launch_repack_affine_bits(const uint32_t *qw, const uint16_t *sc, const uint16_t *b, int N, int K,
+                                      int bits, const Layout &L, uint8_t *packed, cudaStream_t stream) {
+  RepackSrc s;
+  s.qw[0] = s.qw[1] = qw;
+  s.sc[0] = s.sc[1] = sc;
+  s.z[0] = s.z[1] = nullptr;
+  s.b[0] = s.b[1] = b;
+  s.n_src = N;
+  s.gateup = 0;
+  s.bits = bits;
+  s.k_src = K;
+  return launch_repack_src(s, L, packed, stream);
+}
+
+cudaError_t launch_dequantize_affine_bits(const uint8_t *packed, const Layout &L, int N, int K, int bits, float *w,
+                                          cudaStream_t stream) {
+  const int th = 256;
+  dequantize_bits_kernel<<<grid_for((size_t)N * K, th), th, 0, stream>>>(packed, L, N, K, bits, w);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t *z0, const uint16_t *b0,
                           const int32_t *qw1, const uint16_t *sc1, const int32_t *z1, const uint16_t *b1,
@@ -212,6 +332,13 @@ cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t
   s.b[1] = b1 ? b1 : b0;
   s.n_src = n_src;
   s.gateup = gateup ? 1 : 0;
+  s.bits = 0;
+  s.k_src = L.K;
+  return launch_repack_src(s, L, packed, stream);
+}
+
+namespace {
+cudaError_t launch_repack_src(RepackSrc &s, const Layout &L, uint8_t *packed, cudaStream_t stream) {
   const int th = 256;
   size_t nc = (size_t)L.tiles * L.chunks * 128;
   repack_codes_kernel<<<grid_for(nc, th), th, 0, stream>>>(s, L,
@@ -232,6 +359,7 @@ cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t
   }
   return cudaGetLastError();
 }
+}  // namespace
 
 cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, float *w,
                               cudaStream_t stream) {

@@ -50,6 +50,16 @@ cudaError_t launch_repack(const int32_t *qw0, const uint16_t *sc0, const int32_t
                           cudaStream_t stream);
 cudaError_t launch_dequantize(const uint8_t *packed, const Layout &L, int N, float *w,
                               cudaStream_t stream);
+// b-bit affine codes (canonical: one little-endian bit stream per row of K
+// codes) -> the affine tiled layout L, widened to nibbles (bits <= 4, L.K = K)
+// or split into two nibble planes (bits 5-8, L.K = 2K); and the read-back
+cudaError_t launch_repack_affine_bits(const uint32_t *qw, const uint16_t *sc, const uint16_t *b, int N, int K,
+                                      int bits, const Layout &L, uint8_t *packed, cudaStream_t stream);
+cudaError_t launch_dequantize_affine_bits(const uint8_t *packed, const Layout &L, int N, int K, int bits, float *w,
+                                          cudaStream_t stream);
+// x [M][K] -> xw [M][2K] with each group of x written twice in a row (the
+// x of the two nibble planes of a 5-8-bit affine weight)
+cudaError_t launch_widen_groups(const uint16_t *x, int M, int K, int group, uint16_t *xw, cudaStream_t stream);
 
 cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count);  // 1 <= M <= 16
 cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count);     // M == 1, not gate/up

@@ -60,7 +60,31 @@ __global__ void __launch_bounds__(kXsThreads) xsum_kernel(const uint16_t *x, int
   }
 }
 
+// x [M][K] -> xw [M][2K]: group g of row m written at columns 2gG .. 2gG+G-1
+// and again at 2gG+G .. 2gG+2G-1, 16 bytes per thread and step.
+__global__ void widen_groups_kernel(const uint4 *x, int M, int K, int group, uint4 *xw) {
+  const size_t kv = K / 8, total = (size_t)M * kv;
+  const int gv = group / 8;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t m = i / kv;
+    const int v = (int)(i % kv), g = v / gv, j = v % gv;
+    const uint4 val = x[i];
+    uint4 *out = xw + m * 2 * kv + (size_t)2 * g * gv + j;
+    out[0] = val;
+    out[gv] = val;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_widen_groups(const uint16_t *x, int M, int K, int group, uint16_t *xw, cudaStream_t stream) {
+  const size_t work = (size_t)M * (K / 8);
+  size_t blocks = (work + kXsThreads - 1) / kXsThreads;
+  if (blocks > 65535u * 8u) blocks = 65535u * 8u;
+  widen_groups_kernel<<<(unsigned)(blocks < 1 ? 1 : blocks), kXsThreads, 0, stream>>>(
+      reinterpret_cast<const uint4 *>(x), M, K, group, reinterpret_cast<uint4 *>(xw));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_xsum(const uint16_t *x, int M, int K, int group, uint16_t *xs, cudaStream_t stream) {
   int blocks = (M + kXsThreads / 32 - 1) / (kXsThreads / 32);

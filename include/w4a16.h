@@ -272,6 +272,56 @@ int w4a16_gemm_affine_noalloc(const uint16_t *x, const void *packed, int M, int 
 int w4a16_gateup_silu_affine(const uint16_t *x, const uint16_t *xsum, const void *packed_gateup, int M, int N_each,
                              int K, int group, uint16_t *h, w4a16_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Affine form at other code widths: modules of 2 to 8 bits, every code
+ * keeping its value, scale and bias (TensorFold PR #859, "What this changes"
+ * and the native 2, 3, 5 and 6-bit tiles note): w = scale * q + bias with q in
+ * 0 .. 2^bits - 1.
+ *
+ * Canonical qweight: uint32 [N][ceil(K * bits / 32)], one little-endian bit
+ * stream per row, code k at bits [bits * k, bits * k + bits) of the row's
+ * stream (running into the next word where it does not fit); at 4 bits this
+ * is the nibble packing above. scales, biases: bf16 [N][K/G].
+ *
+ * The repacked weight reuses the 4-bit affine kernels exactly: 2- and 3-bit
+ * codes are widened into the 4-bit tiles (4 bits of memory per code); 5- to
+ * 8-bit codes q = 16 qh + ql become two nibble planes over K' = 2K, group g's
+ * high plane (codes qh, scale 16 * scale, the bias) followed by its low plane
+ * (codes ql, the scale, bias 0), multiplied by x's group g twice (8 bits of
+ * memory per code). 16 * scale is exact in bf16 for |scale| < 2^123.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of the repacked b-bit weight (0 for bits outside 2..8 or unsupported sizes). */
+size_t w4a16_affine_bits_repacked_bytes(int N, int K, int group, int bits);
+
+/* Offline repack of a b-bit affine weight; packed 256-byte aligned. */
+int w4a16_repack_affine_bits(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases, int N, int K,
+                             int group, int bits, void *packed, w4a16_stream_t stream);
+
+/*
+ * Bytes of the caller-owned scratch a w4a16_gemm_affine_bits call needs
+ * (never 0 for supported sizes; 0 means unsupported): for 5-8 bits x with
+ * each group written twice, bf16 [M][2K] (256-byte aligned), then the table of
+ * x group sums of w4a16_xsum for the widened K (written when M > 32).
+ */
+size_t w4a16_affine_bits_scratch_bytes(int M, int K, int group, int bits);
+
+/*
+ * y[M][N] (bf16) = x . (scale * q + bias)^T for a weight from
+ * w4a16_repack_affine_bits. `scratch`: w4a16_affine_bits_scratch_bytes(M, K,
+ * group, bits) bytes of device memory, 256-byte aligned, used only by this
+ * call while it runs on `stream` (calls in flight at once need their own).
+ * Launches: the widened x (5-8 bits), the group sums (M > 32), the affine
+ * GEMM. The output meets the same bound as the 4-bit form.
+ */
+int w4a16_gemm_affine_bits(const uint16_t *x, void *scratch, const void *packed, int M, int N, int K, int group,
+                           int bits, uint16_t *y, w4a16_stream_t stream);
+
+/* Test export: w_out[N][K] (float32) = scale * q + bias of the repacked b-bit
+ * weight, rounded once to float32, q read back from its nibble planes. */
+int w4a16_dequantize_affine_bits(const void *packed, int N, int K, int group, int bits, float *w_out,
+                                 w4a16_stream_t stream);
+
 /*
  * Waits for all work on the current device, then reads and clears the
  * device error word that a kernel sets when one of its bounded waits gave up

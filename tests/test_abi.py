@@ -139,6 +139,37 @@ def test_topk_entry_points_argument_checks(L):
     assert g(P(FAKE), P(FAKE), 2, 300, 128, 64, 1, 8, P(FAKE), P(FAKE + 4), None, None) == MISALIGNED
 
 
+def test_affine_bits_sizes_and_argument_checks(L):
+    P = ctypes.c_void_p
+    rb = L.w4a16_affine_bits_repacked_bytes
+    # 2-4 bits: the 4-bit affine layout; 5-8 bits: the layout of K' = 2K
+    for bits in (2, 3, 4):
+        assert rb(300, 512, 64, bits) == L.w4a16_repacked_bytes(300, 512, 64, 2)
+    for bits in (5, 6, 7, 8):
+        assert rb(300, 512, 64, bits) == L.w4a16_repacked_bytes(300, 1024, 64, 2)
+    assert rb(300, 512, 64, 1) == 0 and rb(300, 512, 64, 9) == 0 and rb(300, 96, 64, 4) == 0
+    sb = L.w4a16_affine_bits_scratch_bytes
+    # the group-sum table (3 parts per group, rounded up to 64 columns), after
+    # the widened x for 5-8 bits
+    assert sb(3, 512, 64, 3) == 3 * 64 * 2
+    assert sb(3, 512, 64, 8) == 3 * 2 * 512 * 2 + 3 * 64 * 2
+    assert sb(300, 5120, 64, 6) == 300 * 2 * 5120 * 2 + 300 * 512 * 2  # 160 groups of the widened K
+    assert sb(3, 512, 64, 1) == 0 and sb(0, 512, 64, 4) == 0
+    r = L.w4a16_repack_affine_bits
+    assert r(P(FAKE), P(FAKE), P(FAKE), 300, 512, 64, 1, P(FAKE), None) == INVALID
+    assert r(P(FAKE), P(FAKE), None, 300, 512, 64, 5, P(FAKE), None) == INVALID
+    assert r(P(FAKE), P(FAKE), P(FAKE), 300, 512, 64, 5, P(FAKE + 16), None) == MISALIGNED
+    g = L.w4a16_gemm_affine_bits
+    assert g(P(FAKE), None, P(FAKE), 4, 64, 512, 64, 6, P(FAKE), None) == INVALID        # no scratch
+    assert g(P(FAKE), P(FAKE), P(FAKE), 4, 64, 512, 64, 9, P(FAKE), None) == INVALID     # bits
+    assert g(P(FAKE), P(FAKE), P(FAKE), 4, 64, 96, 64, 6, P(FAKE), None) == INVALID      # K % G
+    assert g(P(FAKE), P(FAKE + 16), P(FAKE), 4, 64, 512, 64, 6, P(FAKE), None) == MISALIGNED
+    assert g(P(FAKE + 8), P(FAKE), P(FAKE), 4, 64, 512, 64, 6, P(FAKE), None) == MISALIGNED
+    dq = L.w4a16_dequantize_affine_bits
+    assert dq(P(FAKE), 64, 512, 64, 1, P(FAKE), None) == INVALID
+    assert dq(None, 64, 512, 64, 3, P(FAKE), None) == INVALID
+
+
 def test_affine_layout_and_argument_checks(L):
     P = ctypes.c_void_p
     # the bias section is the scales' size (N=256, K=512, G=128 -> 2048 B), then

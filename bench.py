@@ -190,81 +190,86 @@ def job_value(units_per_step: float, steps: int, world: int, ms: float, scale: f
 # ---------------------------------------------------------------------------
 # CUDA arm
 # ---------------------------------------------------------------------------
-def run_cuda(args, rank, world):
-    import torch
-    import gemm_w4a16_group_gb300 as w4
+SPEC_HBM_GBS = 7900.0  # nominal HBM3e bandwidth of one GB300 (context beside the measured copy peak)
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    w4.lib()
-    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3, "xstaged": 4}[args.kernel])
-    # decode calls stream their (read-only, already complete) weights while
-    # the previous kernel finishes; x and y wait for it
-    w4.set_programmatic_overlap(not args.no_overlap)
-    peaks = load_peaks()
 
-    def up(a):
-        a = np.ascontiguousarray(a)
-        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+def quantiles(v):
+    a = np.asarray(v, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90))}
 
-    parts = []
-    if args.argmax and any(w.get("affine", False) for _, w in step_parts(args.workload)):
-        raise SystemExit("--argmax takes the zero-point forms only")
-    if args.noalloc and any(not w.get("affine", False) or w["kind"] != "gemm" for _, w in step_parts(args.workload)):
-        raise SystemExit("--noalloc takes the affine plain-GEMM workloads only")
-    for name, w in step_parts(args.workload):
-        p = new_problem(w)
-        units, unit, is_flops = part_units(w)
-        if args.argmax and not is_flops:
-            units -= 2 * w["M"] * w["N"]  # no logits written
-        wbytes = algorithmic_bytes(1, w["N"], w["K"], w["group"], w["sym"], w.get("affine", False)) * \
-            (2 if w["kind"] == "gateup" else 1)
-        parts.append(dict(name=name, w=w, p=p, units=units, unit=unit, is_flops=is_flops, wbytes=wbytes))
-    # weight copies to rotate through so that L2 never holds the next call's weights
-    total_w = sum(pt["wbytes"] for pt in parts)
-    copies = 1 if parts[0]["is_flops"] else max(2, math.ceil(4 * L2_BYTES / total_w) + 1)
-    for pt in parts:
-        p, w = pt["p"], pt["w"]
-        zd = None if p["zeros"] is None else up(p["zeros"])
-        if p["affine"] and w["kind"] == "gateup":
-            packed = w4.repack_affine_gateup(up(p["qweight"]), up(p["scales"]), up(p["biases"]), up(p["qweight_up"]),
-                                             up(p["scales_up"]), up(p["biases_up"]), w["N"], w["K"], w["group"])
-        elif p["affine"]:
-            packed = w4.repack_affine(up(p["qweight"]), up(p["scales"]), up(p["biases"]), w["N"], w["K"], w["group"])
-        elif w["kind"] == "gateup":
-            packed = w4.repack_gateup(up(p["qweight"]), up(p["scales"]), zd, up(p["qweight_up"]),
-                                      up(p["scales_up"]), None if p["zeros_up"] is None else up(p["zeros_up"]),
-                                      w["N"], w["K"], w["group"], w["sym"])
-        else:
-            packed = w4.repack(up(p["qweight"]), up(p["scales"]), zd, w["N"], w["K"], w["group"], w["sym"])
-        pt["packed"] = [packed] + [packed.clone() for _ in range(copies - 1)]
-        pt["x"] = up(p["x"])
-        pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
-        # affine form on the tcgen05 GEMM: the group sums of x, formed every call
-        pt["xs"] = (torch.empty(w4.xsum_bytes(w["M"], w["K"], w["group"]) // 2, dtype=torch.bfloat16, device=dev)
-                    if p["affine"] and (w["M"] > 32 or args.kernel == "tc") else None)
-        pt["idx"] = torch.empty(w["M"], dtype=torch.int64, device=dev)
-        pt["idx_host"] = torch.empty(w["M"], dtype=torch.int64).pin_memory()
-        pt["x_host"] = torch.from_numpy(p["x"].view(np.int16)).pin_memory()
-        pt["y_host"] = torch.empty((w["M"], w["N"]), dtype=torch.int16).pin_memory()
-        del pt["p"]
-    torch.cuda.synchronize()
 
-    # Device time comes from CUDA-graph replays: a decode server launches its
-    # steps from graphs, and an eager Python loop would time the host's launch
-    # path instead of the kernels (a decode call is ~10-30 us of device work).
-    s = torch.cuda.Stream(device=dev) if not args.eager else stream
+class Workload:
+    """One workload's device buffers (weights rotated over enough copies that
+    L2 never holds the next call's weights) and the library calls of a step."""
 
-    def call(pt, c, x=None, y=None):
-        w = pt["w"]
-        if args.argmax and w["kind"] != "gateup":
-            # the greedy pick only: the logits are not stored
-            idx, _ = w4.gemm_argmax(pt["x"] if x is None else x, pt["packed"][c], w["N"], w["K"], w["group"],
-                                    w["sym"], stream=s, index_out=pt["idx"])
-            return
+    def __init__(self, name, args, dev, mode="y", topk_k=8, max_copies=None):
+        import torch
+        import gemm_w4a16_group_gb300 as w4
+        self.torch, self.w4, self.args, self.mode, self.topk_k = torch, w4, args, mode, topk_k
+
+        def up(a):
+            a = np.ascontiguousarray(a)
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+        parts = []
+        for pname, w in step_parts(name):
+            p = new_problem(w)
+            units, unit, is_flops = part_units(w)
+            if mode == "argmax" and not is_flops:
+                units -= 2 * w["M"] * w["N"]  # no logits written
+            wbytes = algorithmic_bytes(1, w["N"], w["K"], w["group"], w["sym"], w.get("affine", False)) * \
+                (2 if w["kind"] == "gateup" else 1)
+            parts.append(dict(name=pname, w=w, p=p, units=units, unit=unit, is_flops=is_flops, wbytes=wbytes))
+        total_w = sum(pt["wbytes"] for pt in parts)
+        copies = 1 if parts[0]["is_flops"] else max(2, math.ceil(4 * L2_BYTES / total_w) + 1)
+        if max_copies:
+            copies = min(copies, max_copies)
+        for pt in parts:
+            p, w = pt["p"], pt["w"]
+            zd = None if p["zeros"] is None else up(p["zeros"])
+            if p["affine"] and w["kind"] == "gateup":
+                packed = w4.repack_affine_gateup(up(p["qweight"]), up(p["scales"]), up(p["biases"]),
+                                                 up(p["qweight_up"]), up(p["scales_up"]), up(p["biases_up"]), w["N"],
+                                                 w["K"], w["group"])
+            elif p["affine"]:
+                packed = w4.repack_affine(up(p["qweight"]), up(p["scales"]), up(p["biases"]), w["N"], w["K"],
+                                          w["group"])
+            elif w["kind"] == "gateup":
+                packed = w4.repack_gateup(up(p["qweight"]), up(p["scales"]), zd, up(p["qweight_up"]),
+                                          up(p["scales_up"]), None if p["zeros_up"] is None else up(p["zeros_up"]),
+                                          w["N"], w["K"], w["group"], w["sym"])
+            else:
+                packed = w4.repack(up(p["qweight"]), up(p["scales"]), zd, w["N"], w["K"], w["group"], w["sym"])
+            pt["packed"] = [packed] + [packed.clone() for _ in range(copies - 1)]
+            pt["x"] = up(p["x"])
+            pt["y"] = torch.empty((w["M"], w["N"]), dtype=torch.bfloat16, device=dev)
+            # affine form on the tcgen05 GEMM: the group sums of x, formed every call
+            pt["xs"] = (torch.empty(w4.xsum_bytes(w["M"], w["K"], w["group"]) // 2, dtype=torch.bfloat16, device=dev)
+                        if p["affine"] and (w["M"] > 32 or args.kernel == "tc") else None)
+            pt["idx"] = torch.empty(w["M"], dtype=torch.int64, device=dev)
+            pt["tk_idx"] = torch.empty((w["M"], topk_k), dtype=torch.int64, device=dev)
+            pt["tk_val"] = torch.empty((w["M"], topk_k), dtype=torch.bfloat16, device=dev)
+            pt["idx_host"] = torch.empty(w["M"], dtype=torch.int64).pin_memory()
+            pt["x_host"] = torch.from_numpy(p["x"].view(np.int16)).pin_memory()
+            pt["y_host"] = torch.empty((w["M"], w["N"]), dtype=torch.int16).pin_memory()
+            del pt["p"]
+        self.parts, self.copies, self.total_w = parts, copies, total_w
+
+    def call(self, pt, c, s, x=None, y=None):
+        w4, w, args = self.w4, pt["w"], self.args
         xin = pt["x"] if x is None else x
+        if self.mode == "argmax" and w["kind"] != "gateup":
+            # the greedy pick only: the logits are not stored
+            w4.gemm_argmax(xin, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"], stream=s,
+                           index_out=pt["idx"])
+            return
+        if self.mode == "gemm_topk":
+            w4.gemm_topk(xin, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"], self.topk_k,
+                         out=pt["y"] if y is None else y, index_out=pt["tk_idx"], values_out=pt["tk_val"], stream=s)
+            return
+        if self.mode == "topk":  # the selection alone, over logits already in pt["y"]
+            w4.topk(pt["y"], self.topk_k, index_out=pt["tk_idx"], values_out=pt["tk_val"], stream=s)
+            return
         if w.get("affine", False) and args.noalloc:
             w4.gemm_affine_noalloc(xin, pt["packed"][c], w["N"], w["K"], w["group"], out=pt["y"] if y is None else y,
                                    stream=s)
@@ -279,55 +284,184 @@ def run_cuda(args, rank, world):
         fn = w4.gateup_silu if w["kind"] == "gateup" else w4.gemm
         fn(xin, pt["packed"][c], w["N"], w["K"], w["group"], w["sym"], out=pt["y"] if y is None else y, stream=s)
 
-    def steps(first, n, only=None):
-        for i in range(n):
-            for j, pt in enumerate(parts):
-                if only is None or j == only:
-                    call(pt, (first + i) % copies)
+    def launches_per_call(self, pt):
+        if self.mode == "argmax" and pt["w"]["kind"] != "gateup":
+            return 3  # zero the keys, the GEMM, keys to indices
+        if self.mode == "gemm_topk":
+            return 2
+        return 2 if pt["xs"] is not None else 1  # the affine tcgen05 GEMM's group-sum pre-pass
 
-    def capture(first, n, only=None):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            steps(first, n, only)
+    def steps(self, first, n, s, only=None):
+        for i in range(n):
+            for j, pt in enumerate(self.parts):
+                if only is None or j == only:
+                    self.call(pt, (first + i) % self.copies, s)
+
+    def capture(self, first, n, s, only=None):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g, stream=s):
+            self.steps(first, n, s, only)
         return g
 
-    def timed(fn):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        a.record(s)
-        fn()
-        b.record(s)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        return a.elapsed_time(b)
 
-    nsteps, nwarm = args.steps, args.warmup
-    with torch.cuda.stream(s):
-        steps(0, nwarm)
+def timed(fn, s, world):
+    """Milliseconds of fn()'s device work on stream s, CUDA events on s, a
+    barrier and a synchronize on both sides."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
     torch.cuda.synchronize()
-    if args.eager:
-        run_all = lambda: steps(nwarm, nsteps)  # noqa: E731
-        run_part = [lambda j=j: steps(nwarm, nsteps, j) for j in range(len(parts))]
+    a.record(s)
+    fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    return a.elapsed_time(b)
+
+
+def measure(wl, nsteps, nwarm, s, world, eager=False, stats_ms=200.0, max_replays=400):
+    """Exactly nsteps timed steps (one graph replay, or an eager loop) after
+    nwarm untimed ones; per-call times from graphs of the same launches of
+    each call alone; then the same graphs replayed again until each has run
+    for stats_ms, for the median and the 10th / 90th percentiles."""
+    import torch
+    with torch.cuda.stream(s):
+        wl.steps(0, nwarm, s)
+    torch.cuda.synchronize()
+    if eager:
+        run_all = lambda: wl.steps(nwarm, nsteps, s)  # noqa: E731
+        run_part = [lambda j=j: wl.steps(nwarm, nsteps, s, j) for j in range(len(wl.parts))]
     else:
-        g_all = capture(nwarm, nsteps)
-        g_part = [capture(nwarm, nsteps, j) for j in range(len(parts))]
+        g_all = wl.capture(nwarm, nsteps, s)
+        g_part = [wl.capture(nwarm, nsteps, s, j) for j in range(len(wl.parts))]
         for g in [g_all] + g_part:  # upload and run each graph once, untimed
             with torch.cuda.stream(s):
                 g.replay()
         run_all = g_all.replay
         run_part = [g.replay for g in g_part]
+    with torch.cuda.stream(s):
+        ms = timed(run_all, s, world)
+        per_call = [timed(run_part[j], s, world) / nsteps for j in range(len(wl.parts))]
+        step_samples, call_samples = [], [[] for _ in wl.parts]
+        while sum(step_samples) < stats_ms and len(step_samples) < max_replays:
+            step_samples.append(timed(run_all, s, world) / nsteps)
+        for j in range(len(wl.parts)):
+            acc = 0.0
+            while acc < stats_ms and len(call_samples[j]) < max_replays:
+                t = timed(run_part[j], s, world)
+                acc += t
+                call_samples[j].append(t / nsteps)
+    return {"ms": ms, "per_call_ms": per_call,
+            "stats": {"replays": len(step_samples), "calls_per_replay": nsteps,
+                      "ms_per_step": quantiles(step_samples),
+                      "per_call_ms": [quantiles(c) for c in call_samples],
+                      "replays_per_call": [len(c) for c in call_samples]}}
+
+
+def secondary_block(args, dev, s, peaks):
+    """The other headline numbers in the same run: the 4,096-row fused prompt
+    GEMM (TFLOP/s against the bf16 burst peak), the 248,320-row head at 1 and
+    5 rows (GB/s), the head's top-k, and the cuBLAS bf16 GEMM of the prompt's
+    shape as a yardstick. Each: its per-call median and 10th / 90th
+    percentiles over >= 200 ms of graph replays."""
+    import torch
+    out = {}
+
+    def entry(wl, name, steps):
+        m = measure(wl, steps, 3, s, 1)
+        pt = wl.parts[0]
+        q = m["stats"]["per_call_ms"][0]
+        scale = 1e-12 if pt["is_flops"] else 1e-9
+        val = pt["units"] / (q["median"] * 1e-3) * scale
+        peak = peaks["bf16_tflops"] if pt["is_flops"] else peaks["hbm_gbs"]
+        e = {"workload": name, "unit": pt["unit"], "value": round(val, 2), "per_call_ms": q,
+             "calls_timed": sum(m["stats"]["replays_per_call"]) * steps,
+             "roofline": {"bound": "tensor" if pt["is_flops"] else "hbm", "achieved": round(val, 2), "peak": peak,
+                          "frac": round(val / peak, 4), "peak_src": peaks["src"] + (" bf16 burst" if pt["is_flops"]
+                                                                                   else " copy")},
+             "l2": (f"rotating {wl.copies} weight copies" if wl.copies > 1 else "compute-bound; one weight copy")}
+        if not pt["is_flops"]:
+            e["roofline"]["frac_of_spec"] = round(val / SPEC_HBM_GBS, 4)
+        return e
+
+    wl = Workload("prompt_gateup_m4096_k5120_n17408", args, dev)
+    out["prompt_gateup_m4096_k5120_n17408"] = entry(wl, "prompt_gateup_m4096_k5120_n17408", 10)
+    del wl
+    for M in (1, 5):
+        name = f"lm_head_m{M}_k5120_n248320"
+        wl = Workload(name, args, dev)
+        out[name] = entry(wl, name, 20)
+        if M == 1:
+            # the top-8 of the head's logits: the selection alone, and the GEMM with it
+            wl.mode = "topk"
+            m = measure(wl, 20, 3, s, 1)
+            out["topk_k8_m1_n248320"] = {"unit": "us per call", "per_call_us": {
+                k: round(v * 1e3, 3) for k, v in m["stats"]["per_call_ms"][0].items()}}
+            wl.mode = "gemm_topk"
+            m = measure(wl, 20, 3, s, 1)
+            out["lm_head_topk8_m1_k5120_n248320"] = {"unit": "us per call", "per_call_us": {
+                k: round(v * 1e3, 3) for k, v in m["stats"]["per_call_ms"][0].items()}}
+        del wl
+    torch.cuda.empty_cache()
+    # yardstick: cuBLAS bf16 GEMM of the prompt's shape (a library call, not the path)
+    Mp, Kp, Np = 4096, 5120, 2 * 17408
+    a = torch.randn(Mp, Kp, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(Np, Kp, device=dev, dtype=torch.bfloat16)
+    c = torch.empty(Mp, Np, device=dev, dtype=torch.bfloat16)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            torch.matmul(a, b.t(), out=c)
+        samples = []
+        while sum(samples) < 200.0 and len(samples) < 400:
+            samples.append(timed(lambda: torch.matmul(a, b.t(), out=c), s, 1))
+    q = quantiles(samples)
+    tf = 2.0 * Mp * Kp * Np / (q["median"] * 1e-3) * 1e-12
+    out["cublas_bf16_m4096_k5120_n34816"] = {
+        "unit": "TFLOP/s", "value": round(tf, 2), "per_call_ms": q, "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+        "note": "torch.matmul on bf16 operands (cuBLAS); a yardstick, not the W4A16 path"}
+    del a, b, c
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_cuda(args, rank, world):
+    import torch
+    import gemm_w4a16_group_gb300 as w4
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w4.lib()
+    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3, "xstaged": 4}[args.kernel])
+    # decode calls stream their (read-only, already complete) weights while
+    # the previous kernel finishes; x and y wait for it
+    w4.set_programmatic_overlap(not args.no_overlap)
+    peaks = load_peaks()
+
+    if args.argmax and any(w.get("affine", False) for _, w in step_parts(args.workload)):
+        raise SystemExit("--argmax takes the zero-point forms only")
+    if args.noalloc and any(not w.get("affine", False) or w["kind"] != "gemm" for _, w in step_parts(args.workload)):
+        raise SystemExit("--noalloc takes the affine plain-GEMM workloads only")
+    wl = Workload(args.workload, args, dev, mode="argmax" if args.argmax else "y")
+    parts = wl.parts
+    torch.cuda.synchronize()
+
+    # Device time comes from CUDA-graph replays: a decode server launches its
+    # steps from graphs, and an eager Python loop would time the host's launch
+    # path instead of the kernels (a decode call is ~10-30 us of device work).
+    s = torch.cuda.Stream(device=dev) if not args.eager else torch.cuda.current_stream()
+    nsteps, nwarm = args.steps, args.warmup
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.25)
     t_begin = time.time()
-    with torch.cuda.stream(s):
-        ms = timed(run_all)
-        # per-launch duration of each call: the same launches of that call alone
-        per_call_ms = [timed(run_part[j]) / nsteps for j in range(len(parts))]
+    m = measure(wl, nsteps, nwarm, s, world, eager=args.eager)
     t_end = time.time()
+    ms, per_call_ms = m["ms"], m["per_call_ms"]
+    copies = wl.copies
+    launches_per_step = sum(wl.launches_per_call(pt) for pt in parts)
     if w4.kernel_status() != 0:
         raise RuntimeError("a kernel's bounded wait gave up during the timed region")
     ms = max_over_ranks(ms, world)
@@ -344,16 +478,22 @@ def run_cuda(args, rank, world):
         for i in range(nsteps):
             for j, pt in enumerate(parts):
                 xd[j].copy_(pt["x_host"].view(pt["x"].dtype), non_blocking=True)
-                call(pt, (nwarm + nsteps + i) % copies, x=xd[j])
+                wl.call(pt, (nwarm + nsteps + i) % wl.copies, s, x=xd[j])
                 if args.argmax and pt["w"]["kind"] != "gateup":
                     pt["idx_host"].copy_(pt["idx"], non_blocking=True)
                 else:
                     pt["y_host"].copy_(pt["y"].view(torch.int16), non_blocking=True)
         e_stop.record(s)
     torch.cuda.synchronize()
-    sampler.stop()
     e2e_ms = e_start.elapsed_time(e_stop)
     e2e_ms = max_over_ranks(e2e_ms, world)
+
+    secondary = None
+    if rank == 0 and not args.no_secondary and args.workload == DEFAULT and world == 1:
+        secondary = secondary_block(args, dev, s, peaks)
+        if w4.kernel_status() != 0:
+            raise RuntimeError("a kernel's bounded wait gave up during the secondary measurements")
+    sampler.stop()
     if rank != 0:
         return None
 
@@ -370,33 +510,41 @@ def run_cuda(args, rank, world):
     h2d = sum(pt["x"].numel() * 2 for pt in parts)
     d2h = sum(pt["idx"].numel() * 8 if args.argmax and pt["w"]["kind"] != "gateup" else pt["y"].numel() * 2
               for pt in parts)
+    roof = {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
+            "achieved": round(achieved, 2), "peak": peak, "unit": d["unit"],
+            "frac": round(achieved / peak, 4), "traffic": stored_traffic(d["name"]),
+            "peak_src": peaks["src"] + (" bf16 burst" if is_flops else " copy")}
+    if not is_flops:
+        # the same figure against the nominal HBM3e bandwidth (the copy peak above is the denominator)
+        roof["spec_peak"] = SPEC_HBM_GBS
+        roof["frac_of_spec"] = round(achieved / SPEC_HBM_GBS, 4)
     line = {
         "metric": metric_name(args.workload), "value": round(value, 2), "unit": parts[0]["unit"],
         "n_gpus": world, "steps": nsteps, "warmup": nwarm, "ms_per_step": ms / nsteps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload table)",
         "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
-                   "l2": (f"rotating {copies} weight copies ({copies * total_w / 1e6:.0f} MB > 4x L2)"
+                   "l2": (f"rotating {copies} weight copies ({copies * wl.total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
                    "parallelism": f"replicas x{world}", "output": "argmax" if args.argmax else "y",
-                   "entry": "w4a16_gemm_affine_noalloc" if args.noalloc else "default", "launch": ("eager" if args.eager else "cuda graph")
+                   "entry": "w4a16_gemm_affine_noalloc" if args.noalloc else "default",
+                   "launch": ("eager" if args.eager else "cuda graph")
                    + ("" if args.no_overlap else ", programmatic overlap"),
-                   "per_call_ms": [round(v, 5) for v in per_call_ms]},
-        "roofline": {"bound": "tensor" if is_flops else "hbm", "kernel": d["name"],
-                     "achieved": round(achieved, 2), "peak": peak, "unit": d["unit"],
-                     "frac": round(achieved / peak, 4), "traffic": stored_traffic(d["name"]),
-                     "peak_src": peaks["src"] + (" bf16 burst" if is_flops else " copy")},
+                   "per_call_ms": [round(v, 5) for v in per_call_ms],
+                   "repeats": ("value and ms_per_step: exactly --steps steps in one timed region; stats: the "
+                               "same step graph (and each call's graph) replayed again until >= 200 ms each")},
+        "roofline": roof,
+        "stats": m["stats"],
         "e2e": {"value": round(e2e, 2), "unit": parts[0]["unit"], "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        # kernels of this library per timed step: one per call (three for the
-        # argmax form: zero the keys, the GEMM, keys to indices; two for the
-        # affine form on the tcgen05 GEMM: the group sums of x, the GEMM)
-        "gpu_launches": nsteps * sum(3 if args.argmax and pt["w"]["kind"] != "gateup" else
-                                     2 if pt["xs"] is not None else 1 for pt in parts),
+        # kernels of this library per timed step
+        "gpu_launches": nsteps * launches_per_step,
         "clocks": clocks,
     }
+    if secondary is not None:
+        line["secondary"] = secondary
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds, single_s=args.cpu_single_seconds)
     return line
 
 
@@ -408,7 +556,7 @@ def _oracle_problems(workload):
     return [(name, w, new_problem(w)) for name, w in parts], part_units(parts[0][1])[2]
 
 
-def _oracle_step(probs, is_flops, frac=1.0):
+def _oracle_step(probs, is_flops, frac=1.0, nthreads=0):
     """One step of the float64 oracle over every part of the workload: M rows
     (at most 16 for gate/up and where the unit is FLOP/s) by all output
     columns, or with `frac` < 1 that share of the columns, evenly spaced,
@@ -426,18 +574,18 @@ def _oracle_step(probs, is_flops, frac=1.0):
         t0 = time.perf_counter()
         if gate and p["affine"]:
             oracle.gateup_silu_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], p["qweight_up"],
-                                         p["scales_up"], p["biases_up"], M, N, K, G, mi, ni)
+                                         p["scales_up"], p["biases_up"], M, N, K, G, mi, ni, nthreads)
         elif gate:
             oracle.gateup_silu_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["qweight_up"], p["scales_up"],
-                                  p["zeros_up"], M, N, K, G, w["sym"], mi, ni)
+                                  p["zeros_up"], M, N, K, G, w["sym"], mi, ni, nthreads)
         elif ncols == N and p["affine"]:
-            oracle.gemm_affine(p["x"][:rows], p["qweight"], p["scales"], p["biases"], rows, N, K, G)
+            oracle.gemm_affine(p["x"][:rows], p["qweight"], p["scales"], p["biases"], rows, N, K, G, nthreads)
         elif ncols == N:
-            oracle.gemm(p["x"][:rows], p["qweight"], p["scales"], p["zeros"], rows, N, K, G, w["sym"])
+            oracle.gemm(p["x"][:rows], p["qweight"], p["scales"], p["zeros"], rows, N, K, G, w["sym"], nthreads)
         elif p["affine"]:
-            oracle.gemm_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, G, mi, ni)
+            oracle.gemm_affine_at(p["x"], p["qweight"], p["scales"], p["biases"], M, N, K, G, mi, ni, nthreads)
         else:
-            oracle.gemm_at(p["x"], p["qweight"], p["scales"], p["zeros"], M, N, K, G, w["sym"], mi, ni)
+            oracle.gemm_at(p["x"], p["qweight"], p["scales"], p["zeros"], M, N, K, G, w["sym"], mi, ni, nthreads)
         seconds += time.perf_counter() - t0
         if is_flops:
             units += gemm_flops(rows, (2 if gate else 1) * ncols, K)
@@ -459,17 +607,32 @@ def _oracle_result(units, seconds, reps, desc, is_flops):
             "sample": f"{desc}, {reps} repetition(s), {seconds:.1f} s", "seconds": seconds, "reps": reps}
 
 
-def cpu_baseline(workload, budget_s=10.0):
+def cpu_baseline(workload, budget_s=10.0, single_s=5.0):
     """The float64 oracle as it stands, on every host core, over whole steps
     of the workload's bounded sample until `budget_s` seconds of oracle work;
-    returns value in the workload's unit."""
+    returns value in the workload's unit. `single_thread`: the same oracle on
+    one thread, over an evenly spaced share of the output columns sized so
+    that about `single_s` seconds of work run."""
     probs, is_flops = _oracle_problems(workload)
     seconds, units, reps = 0.0, 0.0, 0
     while True:  # at least one step
         s, u, desc = _oracle_step(probs, is_flops)
         seconds, units, reps = seconds + s, units + u, reps + 1
         if seconds >= budget_s:
-            return _oracle_result(units, seconds, reps, desc, is_flops)
+            break
+    res = _oracle_result(units, seconds, reps, desc, is_flops)
+    if single_s > 0:
+        probe, _, _ = _oracle_step(probs, is_flops, 0.01, nthreads=1)
+        frac = min(1.0, max(1e-4, 0.01 * (single_s / 3.0) / max(probe, 1e-6)))
+        s1, u1, r1 = 0.0, 0.0, 0
+        while True:
+            s, u, desc1 = _oracle_step(probs, is_flops, frac, nthreads=1)
+            s1, u1, r1 = s1 + s, u1 + u, r1 + 1
+            if s1 >= single_s:
+                break
+        one = _oracle_result(u1, s1, r1, desc1, is_flops)
+        res["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1, "sample": one["sample"]}
+    return res
 
 
 REFERENCE_BUDGET_S = 120.0  # the reference arm's warm-up and timed steps together
@@ -519,6 +682,10 @@ def main():
     ap.add_argument("--noalloc", action="store_true",
                     help="affine plain GEMM through w4a16_gemm_affine_noalloc (group sums in the library's array)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-single-seconds", type=float, default=5.0,
+                    help="budget of the single-threaded oracle figure in cpu_baseline")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the prompt GEMM, LM head, top-k and cuBLAS figures of the default line")
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
     ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc", "xstaged"],
                     help="kernel override for A/B measurement (default: automatic choice)")

@@ -53,6 +53,10 @@ constexpr int kWarps = 4;       // warps per CTA
 #endif
 constexpr int kUnitChunks = W4A16_UNIT_CHUNKS;  // 64-wide K chunks per ring slot
 static_assert(kUnitChunks == 2 || kUnitChunks == 4, "a unit is 128 or 256 k");
+#ifndef W4A16_DECODE_UNIT_LOADS
+#define W4A16_DECODE_UNIT_LOADS 1
+#endif
+constexpr bool kDecodeUnitLoads = W4A16_DECODE_UNIT_LOADS != 0;
 
 struct DecodeParams {
   const uint16_t *x;
@@ -377,10 +381,14 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[i][mt][r] = 0.f;
 
+  // One x tile (M <= 8): the unit's x (4 chunks x 2 x 16 bytes per lane) is
+  // loaded before the slot wait, at immediate offsets from one address per
+  // unit, and the unit's codes are read from the slot at once. More x tiles:
   // x is loaded one 64-wide chunk ahead of its use (xn), so the load latency
-  // overlaps the previous chunk's unpack and MMAs
+  // overlaps the previous chunk's unpack and MMAs.
+  constexpr bool kUnitX = MT == 1 && kDecodeUnitLoads;
   uint4 xn[MT][2];
-  {
+  if (!kUnitX) {
     const int c0 = min(kUnitChunks * ub, p.chunks - 1);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
@@ -391,9 +399,36 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
   int it = 0;
   for (; it < nu; ++it) {
     const int u = ub + it;
-    const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);  // groups in this unit
+    const int nch = min(kUnitChunks, p.chunks - kUnitChunks * u);
+    const int ngu = nch / CPG;  // groups in this unit
+    uint4 xu[kUnitX ? kUnitChunks : 1][2];
+    if (kUnitX) {
+      const uint4 *xb = xp[0] + (size_t)u * (kUnitChunks * 8);
+      if (nch == kUnitChunks) {
+#pragma unroll
+        for (int cl = 0; cl < (kUnitX ? kUnitChunks : 1); ++cl) {
+          xu[cl][0] = ldg_keep(xb + cl * 8);
+          xu[cl][1] = ldg_keep(xb + cl * 8 + 1);
+        }
+      } else {  // a ragged last unit: its chunks only
+#pragma unroll
+        for (int cl = 0; cl < (kUnitX ? kUnitChunks : 1); ++cl) {
+          const int cc = min(cl, nch - 1);
+          xu[cl][0] = ldg_keep(xb + cc * 8);
+          xu[cl][1] = ldg_keep(xb + cc * 8 + 1);
+        }
+      }
+    }
     if (!wait_slot<SLOTS>(ring.bar0, it, abort_flag, p.err)) break;
     const uint32_t sl = ring.slot(it % SLOTS);
+    uint4 wu[kUnitX ? TPW : 1][kUnitX ? kUnitChunks : 1];
+    if (kUnitX) {
+#pragma unroll
+      for (int i = 0; i < (kUnitX ? TPW : 1); ++i)
+#pragma unroll
+        for (int cl = 0; cl < (kUnitX ? kUnitChunks : 1); ++cl)
+          wu[i][cl] = lds128(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
+    }
 #pragma unroll
     for (int j = 0; j < GPU; ++j) {
       if (j < ngu) {
@@ -414,20 +449,27 @@ __global__ void __launch_bounds__(kWarps * 32) smallm_mma_kernel(DecodeParams p)
 #pragma unroll
         for (int cc = 0; cc < CPG; ++cc) {
           const int cl = j * CPG + cc;  // chunk within the unit
-          const int c = kUnitChunks * u + cl;
           uint4 xx[MT][2];
-          const int cn = min(c + 1, p.chunks - 1);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            xx[mt][0] = xn[mt][0];
-            xx[mt][1] = xn[mt][1];
-            xn[mt][0] = ldg_keep(xp[mt] + (size_t)cn * 8);
-            xn[mt][1] = ldg_keep(xp[mt] + (size_t)cn * 8 + 1);
-          }
           uint4 w[TPW];
+          if (kUnitX) {
+            xx[0][0] = xu[kUnitX ? cl : 0][0];
+            xx[0][1] = xu[kUnitX ? cl : 0][1];
 #pragma unroll
-          for (int i = 0; i < TPW; ++i)
-            w[i] = lds128(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
+            for (int i = 0; i < TPW; ++i) w[i] = wu[kUnitX ? i : 0][kUnitX ? cl : 0];
+          } else {
+            const int c = kUnitChunks * u + cl;
+            const int cn = min(c + 1, p.chunks - 1);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              xx[mt][0] = xn[mt][0];
+              xx[mt][1] = xn[mt][1];
+              xn[mt][0] = ldg_keep(xp[mt] + (size_t)cn * 8);
+              xn[mt][1] = ldg_keep(xp[mt] + (size_t)cn * 8 + 1);
+            }
+#pragma unroll
+            for (int i = 0; i < TPW; ++i)
+              w[i] = lds128(sl + i * R::kTileCode + (cl * 32 + lane) * 16);
+          }
 #pragma unroll
           for (int st = 0; st < 4; ++st) {
             // B fragment: x words 2st (k+0, k+1) and 2st+1 (k+2, k+3) of this lane's 16 k

@@ -444,7 +444,10 @@ def run_cuda(args, rank, world):
         raise SystemExit("--argmax takes the zero-point forms only")
     if args.noalloc and any(not w.get("affine", False) or w["kind"] != "gemm" for _, w in step_parts(args.workload)):
         raise SystemExit("--noalloc takes the affine plain-GEMM workloads only")
-    wl = Workload(args.workload, args, dev, mode="argmax" if args.argmax else "y")
+    if args.topk and any(w["kind"] == "gateup" or w.get("affine", False) for _, w in step_parts(args.workload)):
+        raise SystemExit("--topk takes the zero-point GEMM workloads only")
+    mode = "argmax" if args.argmax else ("gemm_topk" if args.topk else "y")
+    wl = Workload(args.workload, args, dev, mode=mode, topk_k=args.topk or 8)
     parts = wl.parts
     torch.cuda.synchronize()
 
@@ -526,7 +529,8 @@ def run_cuda(args, rank, world):
         "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
                    "l2": (f"rotating {copies} weight copies ({copies * wl.total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
-                   "parallelism": f"replicas x{world}", "output": "argmax" if args.argmax else "y",
+                   "parallelism": f"replicas x{world}",
+                   "output": "argmax" if args.argmax else (f"y and top-{args.topk}" if args.topk else "y"),
                    "entry": "w4a16_gemm_affine_noalloc" if args.noalloc else "default",
                    "launch": ("eager" if args.eager else "cuda graph")
                    + ("" if args.no_overlap else ", programmatic overlap"),
@@ -679,6 +683,8 @@ def main():
     ap.add_argument("--no-overlap", action="store_true", help="no programmatic overlap between decode calls")
     ap.add_argument("--argmax", action="store_true",
                     help="time the fused argmax (w4a16_gemm_argmax, no logits stored) instead of the GEMM")
+    ap.add_argument("--topk", type=int, default=0,
+                    help="time w4a16_gemm_topk with this k (the GEMM, then the top-k of its logits)")
     ap.add_argument("--noalloc", action="store_true",
                     help="affine plain GEMM through w4a16_gemm_affine_noalloc (group sums in the library's array)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -57,6 +57,24 @@
 namespace w4a16 {
 namespace {
 
+// Output stores with an L2 evict-first hint: the output (143-285 MB at 4,096
+// rows) streams through L2 once, and without the hint it displaces the x tiles
+// and weight tiles that the other pairs are still reading.
+#ifndef W4A16_PROMPT_Y_EVICT_FIRST
+#define W4A16_PROMPT_Y_EVICT_FIRST 1
+#endif
+__device__ __forceinline__ uint64_t y_store_policy() {
+  uint64_t pol = 0;
+  if (W4A16_PROMPT_Y_EVICT_FIRST) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_y(uint16_t *a, uint16_t v, uint64_t pol) {
+  if (W4A16_PROMPT_Y_EVICT_FIRST)
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(a), "h"(v), "l"(pol) : "memory");
+  else
+    *a = v;
+}
+
 constexpr int BW = 256, BK = 64;  // pair tile: weight rows, k per stage
 constexpr int HW = BW / 2;        // weight rows of one CTA
 constexpr int NT16 = HW / 16;     // 16-row weight tiles of one CTA
@@ -429,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ epilogue
     constexpr int EC = G::EC;
     const int q = warp & 3;                    // TMEM lanes 32q .. 32q+31: this CTA's weight rows
+    const uint64_t ypol = y_store_policy();
     const int ch2 = (warp - 4 - G::DQW) >> 2;  // D columns EC*ch2 .. +EC-1 (x rows mt*BX + EC*ch2 ..)
     const int wr = 32 * q + lane;     // weight row within the CTA's 128
     // this row's scale in a scale block: tile wr/16, g = wr%8, half (wr/8)%2
@@ -499,14 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float other = __shfl_xor_sync(0xffffffffu, gate ? acc[c + H2] : acc[c], 16);
           const float gv = gate ? mine : other, uv = gate ? other : mine;
           const int m = m0 + c + (gate ? 0 : H2);
-          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(silu_f32(gv) * uv);
+          if (n < p.N && m < p.M) st_y(p.y + (size_t)m * p.ld + n, bf16_bits(silu_f32(gv) * uv), ypol);
         }
       } else {
         const int n = nt * BW + (int)rank * HW + wr;
         if (n < p.N) {
 #pragma unroll
           for (int c = 0; c < EC; ++c)
-            if (m0 + c < p.M) p.y[(size_t)(m0 + c) * p.ld + n] = bf16_bits(acc[c]);
+            if (m0 + c < p.M) st_y(p.y + (size_t)(m0 + c) * p.ld + n, bf16_bits(acc[c]), ypol);
         }
       }
     }
@@ -524,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // split K: the first pair adds the other pairs' partial sums (same parity
     // CTA, ranks 2j + rank), in pair order, and stores the tile
     if (kpart == 0 && !*abort_flag) {
+      const uint64_t ypol = y_store_policy();
       const float *part = reinterpret_cast<const float *>(smem + G::OFF_X);
       const uint32_t part_s = smem_u32(smem + G::OFF_X);
       const int mt = pair % p.mtiles, nt = pair / p.mtiles;
@@ -539,13 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float gv = sum_at(col * HW + 32 * q + l), uv = sum_at(col * HW + 32 * q + 16 + l);
           const int n = 16 * (nt * (BW / 32) + (int)rank * (NT16 / 2) + q) + l;
           const int m = mt * G::BX + col;
-          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(silu_f32(gv) * uv);
+          if (n < p.N && m < p.M) st_y(p.y + (size_t)m * p.ld + n, bf16_bits(silu_f32(gv) * uv), ypol);
         }
       } else {
         for (int e = tid; e < G::BX * HW; e += kThreads) {
           const int col = e / HW, row = e % HW;
           const int n = nt * BW + (int)rank * HW + row, m = mt * G::BX + col;
-          if (n < p.N && m < p.M) p.y[(size_t)m * p.ld + n] = bf16_bits(sum_at(e));
+          if (n < p.N && m < p.M) st_y(p.y + (size_t)m * p.ld + n, bf16_bits(sum_at(e)), ypol);
         }
       }
     }

@@ -426,6 +426,14 @@ def secondary_block(args, dev, s, peaks):
     return out
 
 
+def workload_config(args, world):
+    """What the step computes (the same dict on both arms of a run)."""
+    return {"workload": args.workload, "calls_per_step": [name for name, _ in step_parts(args.workload)],
+            "kernel": args.kernel, "parallelism": f"replicas x{world}",
+            "output": "argmax" if args.argmax else (f"y and top-{args.topk}" if args.topk else "y"),
+            "entry": "w4a16_gemm_affine_noalloc" if args.noalloc else "default"}
+
+
 def run_cuda(args, rank, world):
     import torch
     import gemm_w4a16_group_gb300 as w4
@@ -526,12 +534,9 @@ def run_cuda(args, rank, world):
         "n_gpus": world, "steps": nsteps, "warmup": nwarm, "ms_per_step": ms / nsteps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload table)",
-        "config": {"workload": args.workload, "kernel": args.kernel, "calls_per_step": [pt["name"] for pt in parts],
-                   "l2": (f"rotating {copies} weight copies ({copies * wl.total_w / 1e6:.0f} MB > 4x L2)"
+        "config": workload_config(args, world),
+        "timing": {"l2": (f"rotating {copies} weight copies ({copies * wl.total_w / 1e6:.0f} MB > 4x L2)"
                           if copies > 1 else "compute-bound; one weight copy"),
-                   "parallelism": f"replicas x{world}",
-                   "output": "argmax" if args.argmax else (f"y and top-{args.topk}" if args.topk else "y"),
-                   "entry": "w4a16_gemm_affine_noalloc" if args.noalloc else "default",
                    "launch": ("eager" if args.eager else "cuda graph")
                    + ("" if args.no_overlap else ", programmatic overlap"),
                    "per_call_ms": [round(v, 5) for v in per_call_ms],
@@ -664,7 +669,7 @@ def run_reference(args, rank, world):
             "unit": cb["unit"], "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": cb["seconds"] * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
+            "config": workload_config(args, world),
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

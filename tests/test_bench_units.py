@@ -79,13 +79,17 @@ def test_oracle_step_whole_and_sampled_columns():
 
 def test_reference_line_echoes_the_launch():
     import argparse
-    args = argparse.Namespace(workload="tiny_gemv_m1_k512_n256", steps=2, warmup=3)
+    args = argparse.Namespace(workload="tiny_gemv_m1_k512_n256", steps=2, warmup=3, kernel="auto", argmax=False,
+                              topk=0, noalloc=False)
     assert bench.run_reference(args, 1, 2) is None  # only rank 0 works and prints
     line = bench.run_reference(args, 0, 2)
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["steps"] == 2 and line["warmup"] == 3
     assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["sample"].startswith("whole step, 2 repetition(s)")
+    # the same config dict as the CUDA arm's line for the same launch
+    assert line["config"] == bench.workload_config(args, 2)
+    assert line["config"]["calls_per_step"] == ["tiny_gemv_m1_k512_n256"]
 
 
 def test_cpu_baseline_runs_at_least_one_step():

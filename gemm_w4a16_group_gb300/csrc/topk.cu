@@ -7,15 +7,19 @@
 //
 // One cluster of S CTAs (S <= 16) per row, each CTA a contiguous slice of the
 // row. Every value becomes its 16-bit order code (order_key16) and the k-th
-// largest code is found by two radix passes of 8 bits: each CTA counts its
-// slice into a 256-bin shared histogram, the cluster's histograms are summed
-// over distributed shared memory (every CTA forms the same total, so all of
-// them agree on the threshold), and one warp walks the bins from the top.
-// Then each CTA collects the codes above the threshold code, and the codes
-// equal to it in column order; the slices' counts give each CTA its offsets,
-// and every pick is written into rank 0's shared memory, which sorts the k
-// picks by (code, lowest column first) with a bitonic network and writes the
-// columns and their bf16 values. Nothing is allocated; no workspace.
+// largest code is found by radix passes of 8 bits: each CTA counts its slice
+// into a 256-bin shared histogram, the cluster's histograms are summed over
+// distributed shared memory (every CTA forms the same total, so all of them
+// agree on the threshold), and one warp walks the bins from the top. When the
+// codes in and above the k-th code's high-byte bin number at most 2,048 (the
+// usual case for logits), all of them are gathered into rank 0 and sorted.
+// Otherwise a second pass finds the exact threshold code from the low bytes;
+// each CTA collects the codes above it, and the codes equal to it in column
+// order (in any order when every one of them is picked); the slices' counts
+// give each CTA its offsets, and every pick goes into rank 0's shared memory.
+// Rank 0 sorts by (code, lowest column first) with a bitonic network and
+// writes the columns and their bf16 values. Nothing is allocated; no
+// workspace.
 #include "w4a16_internal.h"
 
 namespace w4a16 {
@@ -25,14 +29,20 @@ constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// A row's candidates at or above the threshold bin when there are few of
+// them (the common case for logits): every one is gathered and sorted.
+constexpr int kTkFewCand = 2048;
+
 struct TopkSmem {
-  uint32_t hist[256];                   // this CTA's slice
-  uint32_t tot[256];                    // the cluster's sum
-  unsigned long long pick[kTopkMaxK];   // rank 0: the row's k picks
-  unsigned long long gt[kTopkMaxK];     // this slice's codes above the threshold
-  unsigned long long eq[kTopkMaxK];     // this slice's first codes equal to it, column order
+  uint32_t hist[2][256];   // this CTA's slice: pass 1 (high byte), pass 2 (low byte)
+  uint32_t tot[2][256];    // the cluster's sums
+  // few-candidates path: [0, 2048) this slice's candidates, [2048, 4096)
+  // rank 0's gathered row; three-pass path: [0, 1024) rank 0's picks,
+  // [1024, 2048) this slice's codes above the threshold, [2048, 3072) its
+  // first codes equal to the threshold in column order
+  unsigned long long buf[4096];
   uint32_t wsum[kTkWarps];
-  uint32_t bin, above, ngt, neq, chunk;
+  uint32_t bin, above, ngt, neq, chunk, gbase, ebase;
 };
 
 // add `active` lanes' bins; lanes of a warp with the same bin add once
@@ -76,16 +86,18 @@ __device__ __forceinline__ void find_threshold(const uint32_t *h, uint32_t base,
   }
 }
 
-// The cluster's histogram: every CTA sums every rank's `hist` into its `tot`.
-__device__ __forceinline__ void cluster_total(TopkSmem &sm, uint32_t S, uint32_t rank) {
+// The cluster's histogram of pass `ps`: once every rank has counted its slice,
+// every CTA sums every rank's hist[ps] into its tot[ps] (the histograms of the
+// two passes are separate, so no rank overwrites one that another still reads).
+__device__ __forceinline__ void cluster_total(TopkSmem &sm, int ps, uint32_t S, uint32_t rank) {
   cluster_sync_all();
   if (threadIdx.x < 256) {
-    const uint32_t a = smem_u32(&sm.hist[threadIdx.x]);
+    const uint32_t a = smem_u32(&sm.hist[ps][threadIdx.x]);
     uint32_t s = 0;
-    for (uint32_t r = 0; r < S; ++r) s += r == rank ? sm.hist[threadIdx.x] : ld_cluster_u32(mapa_shared(a, r));
-    sm.tot[threadIdx.x] = s;
+    for (uint32_t r = 0; r < S; ++r) s += r == rank ? sm.hist[ps][threadIdx.x] : ld_cluster_u32(mapa_shared(a, r));
+    sm.tot[ps][threadIdx.x] = s;
   }
-  cluster_sync_all();  // no CTA clears its histogram before every rank has read it
+  __syncthreads();
 }
 
 // VEC values per thread and step: 8 (16-byte loads; rows 16-byte aligned, N
@@ -105,6 +117,39 @@ __device__ __forceinline__ void load_keys(const uint16_t *row, int v, uint32_t (
   }
 }
 
+__device__ __forceinline__ unsigned long long pick_key(uint32_t code, uint32_t col) {
+  return ((unsigned long long)code << 32) | (0xFFFFFFFFu - col);
+}
+
+// Block-wide bitonic sort of a[0, P) descending, P a power of two.
+__device__ __forceinline__ void sort_desc(unsigned long long *a, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < P; i += kTkThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const unsigned long long x = a[i], c = a[j];
+          const bool desc = (i & size) == 0;
+          if (desc ? (x < c) : (x > c)) {
+            a[i] = c;
+            a[j] = x;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Offsets of this CTA's `cnt` entries among the cluster's, in rank order
+// (cluster-wide barrier first, so every rank's count is final).
+__device__ __forceinline__ uint32_t rank_offset(const uint32_t *cnt, uint32_t rank) {
+  uint32_t o = 0;
+  for (uint32_t r = 0; r < rank; ++r) o += ld_cluster_u32(mapa_shared(smem_u32(cnt), r));
+  return o;
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const uint16_t *y, int N, int k, int64_t *idx_out,
                                                              uint16_t *val_out) {
@@ -121,8 +166,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const uint16_t *y, 
   grid_launch_dependents();
   grid_dependency_wait();
 
-  // pass 1: the high byte of every code
-  for (int i = tid; i < 256; i += kTkThreads) sm.hist[i] = 0;
+  for (int i = tid; i < 512; i += kTkThreads) (&sm.hist[0][0])[i] = 0;
   if (tid == 0) {
     sm.bin = 0;
     sm.above = 0;
@@ -130,34 +174,77 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const uint16_t *y, 
     sm.neq = 0;
   }
   __syncthreads();
+
+  // pass 1: the high byte of every code
   for (int b = v0; b < v1; b += kTkThreads) {
     const int v = b + tid;
     const bool ok = v < v1;
     uint32_t key[VEC];
     if (ok) load_keys<VEC>(row, v, key);
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) hist_add(sm.hist, ok ? key[j] >> 8 : 0u, ok);
+    for (int j = 0; j < VEC; ++j) hist_add(sm.hist[0], ok ? key[j] >> 8 : 0u, ok);
   }
-  cluster_total(sm, S, rank);
-  if (warp == 0) find_threshold(sm.tot, 0, K, &sm.bin, &sm.above);
+  cluster_total(sm, 0, S, rank);
+  if (warp == 0) find_threshold(sm.tot[0], 0, K, &sm.bin, &sm.above);
   __syncthreads();
   const uint32_t hb = sm.bin, above1 = sm.above;
+  const uint32_t pick0 = smem_u32(&sm.buf[0]);
+
+  if (above1 + sm.tot[0][hb] <= (uint32_t)kTkFewCand) {
+    // few candidates: every code whose high byte is hb or above, gathered
+    // into rank 0 (slots [2048, 4096)) and sorted there
+    unsigned long long *cand = sm.buf;
+    for (int b = v0; b < v1; b += kTkThreads) {
+      const int v = b + tid;
+      const bool ok = v < v1;
+      uint32_t key[VEC];
+      if (ok) load_keys<VEC>(row, v, key);
+      uint32_t n = 0;
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) n += ok && (key[j] >> 8) >= hb;
+      if (n) {
+        uint32_t slot = atomicAdd(&sm.ngt, n);  // the cluster holds at most kTkFewCand of them
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+          if (ok && (key[j] >> 8) >= hb) cand[slot++] = pick_key(key[j], (uint32_t)(VEC * v + j));
+      }
+    }
+    cluster_sync_all();
+    if (tid == 0) sm.gbase = rank_offset(&sm.ngt, rank);
+    __syncthreads();
+    const uint32_t rdst = mapa_shared(pick0 + 8u * kTkFewCand, 0);
+    for (uint32_t i = tid; i < sm.ngt; i += kTkThreads) st_cluster_u64(rdst + 8u * (sm.gbase + i), cand[i]);
+    cluster_sync_all();
+    if (rank != 0) return;
+    const uint32_t total = above1 + sm.tot[0][hb];
+    unsigned long long *all = sm.buf + kTkFewCand;
+    int P = 1;
+    while ((uint32_t)P < total) P <<= 1;
+    for (int i = (int)total + tid; i < P; i += kTkThreads) all[i] = 0ull;
+    sort_desc(all, P);
+    for (int j = tid; j < k; j += kTkThreads) {
+      const uint32_t n = 0xFFFFFFFFu - (uint32_t)(all[j] & 0xFFFFFFFFull);
+      idx_out[row_id * (size_t)k + j] = (int64_t)n;
+      if (val_out) val_out[row_id * (size_t)k + j] = row[n];
+    }
+    return;
+  }
 
   // pass 2: the low byte of the codes whose high byte is hb
-  for (int i = tid; i < 256; i += kTkThreads) sm.hist[i] = 0;
-  __syncthreads();
   for (int b = v0; b < v1; b += kTkThreads) {
     const int v = b + tid;
     const bool ok = v < v1;
     uint32_t key[VEC];
     if (ok) load_keys<VEC>(row, v, key);
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) hist_add(sm.hist, ok ? key[j] & 0xFFu : 0u, ok && (key[j] >> 8) == hb);
+    for (int j = 0; j < VEC; ++j) hist_add(sm.hist[1], ok ? key[j] & 0xFFu : 0u, ok && (key[j] >> 8) == hb);
   }
-  cluster_total(sm, S, rank);
-  if (warp == 0) find_threshold(sm.tot, above1, K, &sm.bin, &sm.above);
+  cluster_total(sm, 1, S, rank);
+  if (warp == 0) find_threshold(sm.tot[1], above1, K, &sm.bin, &sm.above);
   __syncthreads();
   const uint32_t thr = (hb << 8) | sm.bin, above = sm.above, need = K - above;
+  const bool all_eq = sm.tot[1][sm.bin] == need;  // every code equal to thr is picked: no order needed
+  unsigned long long *gt = sm.buf + 1024, *eq = sm.buf + 2048;
 
   // pass 3: this slice's codes above thr (any order), and its codes equal to
   // thr in column order (the first `need` of them are all that can be picked)
@@ -176,7 +263,16 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const uint16_t *y, 
       uint32_t slot = atomicAdd(&sm.ngt, ngt);  // below `above` <= kTopkMaxK
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
-        if (ok && key[j] > thr) sm.gt[slot++] = ((unsigned long long)key[j] << 32) | (0xFFFFFFFFu - (uint32_t)(VEC * v + j));
+        if (ok && key[j] > thr) gt[slot++] = pick_key(key[j], (uint32_t)(VEC * v + j));
+    }
+    if (all_eq) {
+      if (neq) {
+        uint32_t slot = atomicAdd(&sm.neq, neq);  // below `need`
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+          if (ok && key[j] == thr) eq[slot++] = pick_key(key[j], (uint32_t)(VEC * v + j));
+      }
+      continue;
     }
     // block exclusive scan of neq (threads in column order)
     uint32_t inc = neq;
@@ -204,7 +300,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const uint16_t *y, 
 #pragma unroll
       for (int j = 0; j < VEC; ++j)
         if (ok && key[j] == thr) {
-          if (pos < need) sm.eq[pos] = ((unsigned long long)key[j] << 32) | (0xFFFFFFFFu - (uint32_t)(VEC * v + j));
+          if (pos < need) eq[pos] = pick_key(key[j], (uint32_t)(VEC * v + j));
           ++pos;
         }
     }
@@ -215,48 +311,27 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const uint16_t *y, 
 
   // offsets from the slices before this one, then every pick into rank 0
   cluster_sync_all();
-  __shared__ uint32_t gt_base, eq_base;
   if (tid == 0) {
-    uint32_t g = 0, e = 0;
-    for (uint32_t r = 0; r < rank; ++r) {
-      g += ld_cluster_u32(mapa_shared(smem_u32(&sm.ngt), r));
-      e += ld_cluster_u32(mapa_shared(smem_u32(&sm.neq), r));
-    }
-    gt_base = g;
-    eq_base = e;
+    sm.gbase = rank_offset(&sm.ngt, rank);
+    sm.ebase = rank_offset(&sm.neq, rank);
   }
   __syncthreads();
-  const uint32_t pick0 = smem_u32(&sm.pick[0]);
+  const uint32_t gt_base = sm.gbase, eq_base = sm.ebase;
   const uint32_t rpick = rank == 0 ? pick0 : mapa_shared(pick0, 0);
-  for (uint32_t i = tid; i < sm.ngt; i += kTkThreads) st_cluster_u64(rpick + 8 * (gt_base + i), sm.gt[i]);
+  for (uint32_t i = tid; i < sm.ngt; i += kTkThreads) st_cluster_u64(rpick + 8 * (gt_base + i), gt[i]);
   const uint32_t neq_take = eq_base >= need ? 0u : min(sm.neq, need - eq_base);
-  for (uint32_t i = tid; i < neq_take; i += kTkThreads) st_cluster_u64(rpick + 8 * (above + eq_base + i), sm.eq[i]);
+  for (uint32_t i = tid; i < neq_take; i += kTkThreads) st_cluster_u64(rpick + 8 * (above + eq_base + i), eq[i]);
   cluster_sync_all();
   if (rank != 0) return;
 
   // rank 0: the k picks sorted descending (padding below every pick)
+  unsigned long long *pick = sm.buf;
   int P = 1;
   while (P < k) P <<= 1;
-  for (int i = k + tid; i < P; i += kTkThreads) sm.pick[i] = 0ull;
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = tid; i < P; i += kTkThreads) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const unsigned long long a = sm.pick[i], c = sm.pick[j];
-          const bool desc = (i & size) == 0;
-          if (desc ? (a < c) : (a > c)) {
-            sm.pick[i] = c;
-            sm.pick[j] = a;
-          }
-        }
-      }
-    }
-  }
-  __syncthreads();
+  for (int i = k + tid; i < P; i += kTkThreads) pick[i] = 0ull;
+  sort_desc(pick, P);
   for (int j = tid; j < k; j += kTkThreads) {
-    const uint32_t n = 0xFFFFFFFFu - (uint32_t)(sm.pick[j] & 0xFFFFFFFFull);
+    const uint32_t n = 0xFFFFFFFFu - (uint32_t)(pick[j] & 0xFFFFFFFFull);
     idx_out[row_id * (size_t)k + j] = (int64_t)n;
     if (val_out) val_out[row_id * (size_t)k + j] = row[n];
   }

@@ -442,7 +442,7 @@ def run_cuda(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w4.lib()
-    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3, "xstaged": 4}[args.kernel])
+    w4.set_kernel_override({"auto": 0, "gemv": 1, "smallm": 2, "tc": 3, "xstaged": 4, "decode_tc": 5}[args.kernel])
     # decode calls stream their (read-only, already complete) weights while
     # the previous kernel finishes; x and y wait for it
     w4.set_programmatic_overlap(not args.no_overlap)
@@ -698,7 +698,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the prompt GEMM, LM head, top-k and cuBLAS figures of the default line")
     ap.add_argument("--print-source-hash", action="store_true", help="print the kernel source hash and exit")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc", "xstaged"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "gemv", "smallm", "tc", "xstaged", "decode_tc"],
                     help="kernel override for A/B measurement (default: automatic choice)")
     args = ap.parse_args()
     if args.print_source_hash:

@@ -28,7 +28,7 @@ __all__ = [
     "EXPORTS", "W4A16Error", "lib", "library_path", "repacked_bytes", "gateup_repacked_bytes",
     "repack", "repack_gateup", "gemm", "gemm_argmax", "gateup_silu", "dequantize", "kernel_status",
     "set_kernel_override", "set_programmatic_overlap", "strerror", "KERNEL_AUTO", "KERNEL_GEMV", "KERNEL_SMALLM", "KERNEL_TC",
-    "KERNEL_XSTAGED",
+    "KERNEL_XSTAGED", "KERNEL_DECODE_TC",
     "AFFINE", "repack_affine", "repack_affine_gateup", "xsum_bytes", "xsum", "gemm_affine", "gateup_silu_affine",
     "gemm_affine_noalloc", "topk", "gemm_topk", "affine_bits_repacked_bytes", "repack_affine_bits",
     "affine_bits_scratch_bytes", "gemm_affine_bits", "dequantize_affine_bits",
@@ -44,7 +44,7 @@ EXPORTS = (
     "w4a16_topk", "w4a16_gemm_topk", "w4a16_affine_bits_repacked_bytes", "w4a16_repack_affine_bits",
     "w4a16_affine_bits_scratch_bytes", "w4a16_gemm_affine_bits", "w4a16_dequantize_affine_bits",
 )
-KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC, KERNEL_XSTAGED = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_GEMV, KERNEL_SMALLM, KERNEL_TC, KERNEL_XSTAGED, KERNEL_DECODE_TC = 0, 1, 2, 3, 4, 5
 # the `sym` argument: 0 zero points, 1 symmetric (z = 8), AFFINE scale * q + bias
 AFFINE = 2
 

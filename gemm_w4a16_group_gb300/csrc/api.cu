@@ -228,6 +228,7 @@ int w4a16_gemm(const uint16_t *x, const void *packed, const uint16_t *scales, co
   // M <= 32: a tensor-core decode kernel (measured faster than the CUDA-core
   // GEMV at M = 1 on every decode shape); the GEMV stays selectable.
   if (M == 1 && ov == 1) return finish_launch(launch_gemv_m1(c, d.sm_count));
+  if (ov == 5 && smallm_tc_supports(c)) return finish_launch(launch_smallm_tc(c, d.sm_count));
   if (use_decode(M, ov)) return finish_launch(launch_decode_kernel(c, d.sm_count, ov));
   return finish_launch(launch_prompt_tc(c, d.sm_count));
 }
@@ -479,7 +480,7 @@ const char *w4a16_strerror(int status) {
 int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
 
 int w4a16_set_kernel_override(int which) {
-  if (which < 0 || which > 4) return -1;
+  if (which < 0 || which > 5) return -1;
   return g_override.exchange(which);
 }
 

@@ -3,6 +3,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "w4a16_common.cuh"
@@ -64,6 +65,13 @@ cudaError_t launch_widen_groups(const uint16_t *x, int M, int K, int group, uint
 cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count);  // 1 <= M <= 16
 cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count);     // M == 1, not gate/up
 cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count);   // any M
+// 2-D tiled tensor map (driver entry point found once); false if unavailable
+// or rejected
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+// tcgen05 decode kernel: 1 <= M <= 32, plain zero-point or symmetric GEMM
+bool smallm_tc_supports(const GemmCall &c);
+cudaError_t launch_smallm_tc(const GemmCall &c, int sm_count);
 // argmax of bf16 y rows: keys (zeroed before) -> indices in place; and, for
 // y already written, the keys of every row
 cudaError_t launch_argmax_init(int64_t *amax, int M, bool overlap, cudaStream_t stream);

@@ -342,7 +342,9 @@ int w4a16_last_cuda_error(void);
  * the small-M tensor-core kernel with per-warp weight rings for M <= 32, 3 =
  * force the tcgen05 GEMM for any M, 4 = force the small-M kernel that stages x
  * once per CTA for M <= 16 (automatic choice: M <= 8 calls whose grid of
- * 128-row CTAs fills the GPU, e.g. the output-vocabulary head).
+ * 128-row CTAs fills the GPU, e.g. the output-vocabulary head), 5 = force the
+ * tcgen05 decode kernel (weights dequantised into tensor memory) for plain
+ * zero-point and symmetric w4a16_gemm calls with M <= 32.
  * Returns the previous value. Process-wide; not thread-safe against
  * concurrent calls.
  */

@@ -97,6 +97,9 @@ def test_strerror_and_override(L):
     prev = w4.set_kernel_override(w4.KERNEL_SMALLM)
     assert w4.set_kernel_override(prev) == w4.KERNEL_SMALLM
     assert w4.set_kernel_override(7) == -1
+    assert w4.set_kernel_override(6) == -1
+    prev = w4.set_kernel_override(w4.KERNEL_DECODE_TC)
+    assert w4.set_kernel_override(prev) == w4.KERNEL_DECODE_TC
 
 
 def test_programmatic_overlap_switch(L):

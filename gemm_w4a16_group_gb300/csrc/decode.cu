@@ -317,7 +317,7 @@ struct DecodeSmem {
 template <int SLOTS>
 __device__ __forceinline__ bool wait_slot(uint32_t bar0, int it, volatile int *abort_flag, int *err) {
   const int s = it % SLOTS;
-  const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar0 + 8 * s, (it / SLOTS) & 1, abort_flag));
+  const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait<true>(bar0 + 8 * s, (it / SLOTS) & 1, abort_flag));
   if (!ok && (threadIdx.x & 31) == 0) {
     *abort_flag = 1;
     atomicExch(err, kErrTimeout);
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kXsThreads) smallm_xs_kernel(DecodeParams p) {
       const int s = issued % kXsSlots;
       // every compute warp has released the slot (its previous unit)
       bool got = true;
-      if (lane == 0) got = mbar_wait(empty0 + 8 * s, ((issued / kXsSlots) - 1) & 1, abort_flag);
+      if (lane == 0) got = mbar_wait<true>(empty0 + 8 * s, ((issued / kXsSlots) - 1) & 1, abort_flag);
       got = __shfl_sync(0xFFFFFFFFu, got, 0);
       if (!got) {
         ok = false;
@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(kXsThreads) smallm_xs_kernel(DecodeParams p) {
       const int u = ub + it;
       const int ngu = min(GPU, (p.chunks - kUnitChunks * u) / CPG);
       const int s = it % kXsSlots;
-      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * s, (it / kXsSlots) & 1, abort_flag));
+      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait<true>(full0 + 8 * s, (it / kXsSlots) & 1, abort_flag));
       if (!got) {
         if (lane == 0) {
           *abort_flag = 1;

@@ -261,9 +261,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase. On a phase already complete it costs ~17
+// cycles, against ~51 for try_wait with the suspend hint (measured on GB300).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: true when the phase completed, false after kWaitLimitNs or
-// when *abort became non-zero (another role gave up).
+// when *abort became non-zero (another role gave up). TEST_FIRST: look with
+// the cheap test before sleeping in try_wait (the decode kernels' slot waits
+// usually find the phase complete: 0.3-0.8 % faster; the tcgen05 GEMM's
+// issuing thread is 4.5 % slower with it, so it keeps the plain form).
+template <bool TEST_FIRST = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (TEST_FIRST && mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {

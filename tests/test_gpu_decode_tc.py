@@ -96,3 +96,20 @@ def test_decode_tc_agrees_with_the_mma_sync_kernel_within_bound():
     packed = packed_of(p, d)
     check_gemm_full(p, run_gemm(p, DTC, d, packed))
     check_gemm_full(p, run_gemm(p, w4.KERNEL_SMALLM, d, packed))
+
+
+@pytest.mark.parametrize("name", ["decode_gateup_m1_k5120_n34816", "decode_down_m1_k17408_n5120",
+                                  "smallm_m16_k5120_n34816", "verify_m32_k5120_n34816"])
+def test_decode_tc_full_size_sampled(name):
+    """The full-size workload through this kernel (as `bench.py --kernel
+    decode_tc` times it), on sampled outputs the oracle computes one by one."""
+    from synth.workloads import WORKLOADS
+    from gpu_helpers import assert_within, sample_pairs
+    w = WORKLOADS[name]
+    p = synth.make_problem(w["M"], w["N"], w["K"], w["group"], w["sym"], scale_range=w["scale_range"],
+                           x_scale=w["x_scale"], seed=0)
+    y = run_gemm(p, DTC)
+    mi, ni = sample_pairs(p["M"], p["N"], 1500, seed=len(name))
+    ref, sa = oracle.gemm_at(p["x"], p["qweight"], p["scales"], p["zeros"], p["M"], p["N"], p["K"], p["group"],
+                             p["sym"], mi, ni)
+    assert_within(y[mi, ni], ref, oracle.gemm_bound(ref, sa), name)

@@ -1,8 +1,9 @@
 """Programmatic overlap of consecutive decode calls: a call that reads the
 previous call's output must see all of it.
 
-Two M <= 16 matmuls are chained (the second one's x is the first one's y) and
-run many times back to back, eagerly and from a CUDA graph, with the overlap
+Two M <= 16 matmuls are chained (the second one's x is the first one's y),
+on the automatic kernel choice and on the tcgen05 decode kernel, and run many
+times back to back, eagerly and from a CUDA graph, with the overlap
 switch on. The kernels are deterministic, so every result must equal, bit for
 bit, the same chain run with the switch off; the chain's final output is also
 checked against the oracle, given the first call's output as its input.
@@ -15,7 +16,7 @@ import synth
 
 import gemm_w4a16_group_gb300 as w4
 
-from gpu_helpers import assert_within, bf16_f64, host_bits, packed_of, torch, upload
+from gpu_helpers import assert_within, bf16_f64, host_bits, kernel, packed_of, torch, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -27,8 +28,14 @@ def overlap_off_after():
     w4.set_programmatic_overlap(prev)
 
 
+@pytest.mark.parametrize("which", [w4.KERNEL_AUTO, w4.KERNEL_DECODE_TC])
 @pytest.mark.parametrize("M", [1, 5, 16])
-def test_chained_calls_overlap(M, overlap_off_after):
+def test_chained_calls_overlap(M, which, overlap_off_after):
+    with kernel(which):
+        _chained_calls_overlap(M)
+
+
+def _chained_calls_overlap(M):
     t = torch()
     K1, N1, N2, G = 1024, 2048, 520, 64
     pa = synth.make_problem(M, N1, K1, G, False, seed=31 + M)

@@ -90,7 +90,8 @@ int finish_launch(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : cuda_fai
 
 // The decode kernels (M <= 32): override 2 keeps the per-warp-ring kernel, override 4
 // forces the x-staged one, otherwise the x-staged kernel takes M <= 8 calls
-// whose grid fills a wave
+// whose grid fills a wave and 9-16-row zero-point calls on grids of at least
+// 1.5 CTAs per SM (launch_smallm_mma)
 cudaError_t launch_decode_kernel(GemmCall &c, int sm_count, int ov) {
   c.xs_mode = ov == 4 ? 2 : ov == 2 ? 0 : 1;
   return launch_smallm_mma(c, sm_count);

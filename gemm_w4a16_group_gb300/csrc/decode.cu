@@ -1256,10 +1256,18 @@ cudaError_t run_gemv(const DecodeParams &p, int sm_count, cudaStream_t s) {
 cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count) {
   const Layout L = make_layout(packed_rows(c), c.K, c.group, c.sym);
   DecodeParams p = make_params(c, L);
-  // the x-staged kernel: forced, or chosen for M <= 8 when its grid fills a wave
-  if (c.M <= 16 && (c.xs_mode == 2 || (c.xs_mode == 1 && c.M <= 8))) {
+  // The x-staged kernel: forced; chosen for M <= 8 when its grid fills a
+  // wave; and for 9-16 rows of a zero-point weight whose grid of 8-tile CTAs
+  // spans at least 1.5 CTAs per SM (graph-timed against the per-warp-ring
+  // kernel: 4-7 % faster at N = 34,816 for M = 9, 13 and 16 at K = 5120 and
+  // 17,408; equal at N = 65,536; slower on grids below that, on the symmetric
+  // 248,320-row head (0.7 %) and on the affine form (3 %)).
+  const long long xs_ctas = (L.tiles + 7) / 8;
+  const bool xs_mid = c.xs_mode == 1 && c.M >= 9 && c.sym == kFormZero && !c.gateup && !c.amax &&
+                      2 * xs_ctas >= 3LL * sm_count;
+  if (c.M <= 16 && (c.xs_mode == 2 || xs_mid || (c.xs_mode == 1 && c.M <= 8))) {
     bool launched = false;
-    const bool only_full = c.xs_mode == 1;
+    const bool only_full = c.xs_mode == 1 && !xs_mid;
     const cudaError_t e = c.gateup ? run_xs_all<true>(p, sm_count, c.sym, c.group, c.stream, only_full, &launched)
                                    : run_xs_all<false>(p, sm_count, c.sym, c.group, c.stream, only_full, &launched);
     if (e != cudaSuccess || launched) return e;

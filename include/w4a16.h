@@ -121,7 +121,8 @@ int w4a16_repack_gateup(const int32_t *qw_gate, const uint16_t *sc_gate, const i
  * `packed`, and both must be NULL (else W4A16_ERR_INVALID_ARG).
  * Kernel choice: M <= 32 -> a decode kernel (each weight read and unpacked
  * once for all rows, multiply-adds on the tensor core): the one that stages x
- * once per CTA when M <= 8 and its grid fills the GPU, else the one with a
+ * once per CTA when M <= 8 and its grid fills the GPU, or for 9-16 rows of a
+ * zero-point weight whose grid spans 1.5 CTAs per SM, else the one with a
  * weight ring per warp; M > 32 -> the tcgen05 GEMM. A CUDA-core one-row GEMV
  * is selectable (w4a16_set_kernel_override).
  * Results are bitwise reproducible run to run (no atomics in any sum).

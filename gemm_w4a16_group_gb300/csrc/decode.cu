@@ -11,7 +11,7 @@
 //    cost no registers, and the per-slot bookkeeping is spread over 32 to 64
 //    packed words per lane.
 //
-//  * smallm_mma_kernel (M = 1..16): a lane's two rows x 16 k are the A
+//  * smallm_mma_kernel (M = 1..32): a lane's two rows x 16 k are the A
 //    fragment of mma.sync m16n8k16 (bf16 in, f32 accumulate); x rows are the
 //    B fragment. Each packed word becomes four bf16x2 registers of exact
 //    q - z: three shifts and four LOP3s give 128 + q (bf16 0x4300 is 128 with

@@ -58,8 +58,9 @@ constexpr int kTcRows = 128;         // weight rows per tile: the MMA's M
 constexpr int kTcT16 = kTcRows / 16; // 16-row tiles of the packed layout per tile
 constexpr int kStageChunks = 2;      // 64-wide K chunks per pipeline stage
 // warp roles: the MMAs of even and odd stages are issued by two threads on
-// different SM sub-partitions (each shares its sub-partition with a
-// dequantising and an epilogue warp, which otherwise delay a lone issuer)
+// different SM sub-partitions (measured no faster than one thread, which the
+// round trip of a TMEM stage paces either way; kept since a stage then never
+// waits for the previous stage's issue)
 constexpr int kWarpProducer = 0, kWarpMma0 = 1, kWarpX = 3, kWarpDq0 = 4, kWarpFold0 = 8;
 
 template <int NMMA, int SPG>

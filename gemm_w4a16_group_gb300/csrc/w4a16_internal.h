@@ -35,7 +35,7 @@ struct GemmCall {
   bool overlap;  // programmatic overlap with the previous kernel (M <= 32 kernels)
   int64_t *amax = nullptr;  // argmax keys per x row (M <= 32 plain GEMM), or null
   const uint16_t *xsum = nullptr;  // affine form, tcgen05 GEMM: x group sums, bf16 parts [M][kb3]
-  int xs_mode = 1;  // M <= 16, the kernel that stages x once per CTA: 0 never, 1 when it fits, 2 always
+  int xs_mode = 1;  // M <= 16, the kernel that stages x once per CTA: 0 never, 1 where measured faster, 2 always
 };
 
 // Rows covered by the packed buffer of a call (padded; interleaved for gate/up).
@@ -62,7 +62,7 @@ cudaError_t launch_dequantize_affine_bits(const uint8_t *packed, const Layout &L
 // x of the two nibble planes of a 5-8-bit affine weight)
 cudaError_t launch_widen_groups(const uint16_t *x, int M, int K, int group, uint16_t *xw, cudaStream_t stream);
 
-cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count);  // 1 <= M <= 16
+cudaError_t launch_smallm_mma(const GemmCall &c, int sm_count);  // 1 <= M <= 32
 cudaError_t launch_gemv_m1(const GemmCall &c, int sm_count);     // M == 1, not gate/up
 cudaError_t launch_prompt_tc(const GemmCall &c, int sm_count);   // any M
 // 2-D tiled tensor map (driver entry point found once); false if unavailable
